@@ -1,0 +1,135 @@
+/*
+ * mxfp4_oracle.h -- the CPU oracle for the MXFP4 dequant / matvec / small-batch
+ * matmul / routed-expert path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously-correct
+ * statement of what the GPU library computes.  Only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA library, and it never calls it.
+ *
+ * Conventions (all from "cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs"):
+ *   - A [rows, cols] MXFP4 matrix is one byte buffer: the code plane
+ *     (rows*cols/2 bytes) followed by the scale plane (rows*cols/32 bytes).
+ *     (PEROP struct MxP: sbase = rows*cols/8 words; kernel mxfp4_mv.)
+ *   - Group g of row r holds elements c = 32g .. 32g+31.  Its codes are four
+ *     little-endian u32 words at word index (r*gpr + g)*4 + k, and nibble j of
+ *     word k (bits 4j..4j+3) is element 32g + 8k + j.  (mxfp4_mv's group walk.)
+ *   - Its E8M0 scale is byte (r*gpr + g) of the scale plane, i.e. byte i&3 of
+ *     word sbase + (i>>2), little-endian.  (PEROP fn mx_scale.)
+ *   - Arithmetic: every element decoded scalar by scalar to float; every product
+ *     and every sum in double.  (The f64 reference of the page's device tests.)
+ *
+ * Every function is extern "C" so that Python's ctypes can call it.
+ */
+#ifndef MXFP4_ORACLE_H
+#define MXFP4_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* E2M1 code (low 4 bits of n) -> float.  Magnitudes 0,0.5,1,1.5,2,3,4,6 for
+ * n&7 = 0..7; bit 3 is the sign, so code 8 is -0.0.  (DECODE fn mx_e2m1.) */
+float mxo_e2m1(unsigned n);
+
+/* E8M0 scale byte -> float 2^(k-127); k = 0 gives the subnormal 2^-127 and
+ * k = 255 gives NaN.  (DECODE fn mx_e8m0.) */
+float mxo_e8m0(unsigned k);
+
+/* Exact page length rows*cols*17/32 (codes + scales), 0 when cols % 32 != 0 or
+ * a size is not positive.  (MoeBankCodec::lens; tests bank_codec_lengths.) */
+size_t mxo_nbytes_exact(int rows, int cols);
+
+/* Code nibble of element (r, c) and scale byte of group (r, g). */
+unsigned mxo_code_at(const uint8_t* w, int rows, int cols, int r, int c);
+unsigned mxo_scale_at(const uint8_t* w, int rows, int cols, int r, int g);
+
+/* Decoded element w[r][c] = e2m1(code) * e8m0(scale), rounded to float (the
+ * product is exact: the magnitude has at most two significant bits and the
+ * scale is a power of two). */
+float mxo_weight_at(const uint8_t* w, int rows, int cols, int r, int c);
+
+/* Whole matrix -> out[r*cols + c]. */
+void mxo_dequant(const uint8_t* w, int rows, int cols, float* out);
+
+/* y[t*(r1-r0) + (r-r0)] = sum_c w[r][c] * x[t*cols + c] in double, and
+ * l1[...] = sum_c |w[r][c] * x[t*cols + c]|, for tokens t < nb and rows
+ * r0 <= r < r1.  nb = 1 is mxfp4_mv; nb > 1 is mxfp4_mm.  (PEROP kernels
+ * mxfp4_mv / mxfp4_mm; host entry matmat: out[t*rows + r].) */
+void mxo_matmat(const uint8_t* w, int rows, int cols, const float* x, int nb,
+                int r0, int r1, double* y, double* l1);
+
+/* Same as mxo_matmat over a list of (token, row) samples:
+ * y[i], l1[i] for t = tok[i], r = row[i]. */
+void mxo_matmat_samples(const uint8_t* w, int rows, int cols, const float* x,
+                        const int32_t* tok, const int32_t* row, int n,
+                        double* y, double* l1);
+
+/* float -> bfloat16 -> float, round to nearest even; Inf and NaN pass
+ * through.  (GLOBAL fn mxg_bf16.) */
+float mxo_bf16_rne(float v);
+void mxo_round_bf16(const float* in, float* out, size_t n);
+
+/* SiLU in double: g / (1 + exp(-g)).  (dsv4_global_gate_up_mxfp4 tail.) */
+double mxo_silu(double g);
+/* d silu / d g, used only to propagate error bounds. */
+double mxo_silu_grad(double g);
+
+/* Routed-expert gate/up stage.  Expert e's gate and up matrices are
+ * [inter, hidden] MXFP4 buffers at byte offset e * stride_bytes of their banks.
+ * For pair p = t*top_k + j (token t, slot j) with expert e = ids[p] and every
+ * row r < inter:
+ *   g = gate_e[r] . x_t,  u = up_e[r] . x_t   (double),
+ *   act = silu(g) * u                          (double),
+ * written at [p*inter + r] together with the L1 bounds of g and u.
+ * A pair whose expert id is out of range gets NaN everywhere.
+ * (dsv4_global_gate_up_mxfp4 in its f32 form: no BF16 rounding, no limit,
+ * no pre-weighting; cortiq-engine 0.8.77 moe_fast.rs gate_up_block.) */
+void mxo_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
+                     size_t stride_bytes, int n_experts, int hidden, int inter,
+                     const float* x, int n_tokens, int top_k,
+                     const int32_t* ids, double* g, double* u, double* l1g,
+                     double* l1u, double* act);
+
+/* Routed-expert down stage on a given float activation act[p*inter + c]:
+ *   o_p[r] = down_e[r] . act_p                        (double, per pair),
+ *   out[t*hidden + r] = sum_j route_w[t*top_k + j] * o_{t*top_k+j}[r],
+ * summed over slots j in order, with
+ *   l1_out[t*hidden + r] = sum_j |route_w| * sum_c |down_e[r][c] * act_p[c]|.
+ * o_pairs / l1_pairs may be NULL.  (dsv4_global_down_mxfp4, generic f32 mode;
+ * moe_fast.rs down_block; rlx-cpu gguf_matmul.rs grouped_moe_unpermute_out.) */
+void mxo_moe_down(const uint8_t* down_bank, size_t stride_bytes, int n_experts,
+                  int hidden, int inter, const float* act, int n_tokens,
+                  int top_k, const int32_t* ids, const float* route_w,
+                  double* o_pairs, double* l1_pairs, double* out,
+                  double* l1_out);
+
+/* The whole layer in double (the act is never rounded):
+ *   out[t] = sum_j w_tj * down_e(silu(gate_e x_t) * (up_e x_t)).
+ * bound_l1[t*hidden + r] = sum_j |w_tj| sum_c |down_e[r][c] a_c| and
+ * bound_prop[...] = sum_j |w_tj| sum_c |down_e[r][c]| *
+ *                   (|silu'(g_c)| L1g_c |u_c| + |silu(g_c)| L1u_c),
+ * the two terms an implementation with relative-to-L1 error eps in each dot
+ * product must stay within (times eps). */
+void mxo_moe_forward(const uint8_t* gate_bank, const uint8_t* up_bank,
+                     const uint8_t* down_bank, size_t gu_stride_bytes,
+                     size_t down_stride_bytes, int n_experts, int hidden,
+                     int inter, const float* x, int n_tokens, int top_k,
+                     const int32_t* ids, const float* route_w, double* out,
+                     double* bound_l1, double* bound_prop);
+
+/* Routing plan by counting sort (rlx-cpu gguf_matmul.rs grouped_moe_sort_plan):
+ * offsets[e] .. offsets[e+1] index the pairs of expert e in pair_of[], in
+ * increasing pair order.  Returns the number of pairs with an invalid id (they
+ * are left out of the plan). */
+int mxo_moe_plan(const int32_t* ids, int n_pairs, int n_experts,
+                 int32_t* offsets, int32_t* pair_of);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_ORACLE_H */

@@ -1,0 +1,343 @@
+"""Pins for the CPU oracle: each of its functions checked against something
+other than itself -- the page's closed forms (fixtures under tests/golden/),
+an independent encoder of the layout, numpy/scipy/torch library routines and
+brute force on tiny shapes.  CPU only."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from golden_io import bits_to_f32, f32_to_bits, parse_value, rows
+from mx_encode import dense, encode, random_case
+
+
+def same_f32(a, b) -> bool:
+    """Bit-identical float32, except that any NaN equals any NaN."""
+    a, b = np.float32(a), np.float32(b)
+    if np.isnan(a) or np.isnan(b):
+        return bool(np.isnan(a) and np.isnan(b))
+    return f32_to_bits(a) == f32_to_bits(b)
+
+
+def assert_same_f32_arrays(got, want):
+    got = np.asarray(got, dtype=np.float32)
+    want = np.asarray(want, dtype=np.float32)
+    assert got.shape == want.shape
+    gn, wn = np.isnan(got), np.isnan(want)
+    assert np.array_equal(gn, wn), "NaN positions differ"
+    assert np.array_equal(got[~gn].view(np.uint32), want[~wn].view(np.uint32))
+
+
+# --- scalar decode -----------------------------------------------------------
+
+def test_e2m1_all_16_codes_match_page_construction(orc):
+    seen = 0
+    for code, bits, _ in rows("e2m1_codes.txt"):
+        got = orc.e2m1(int(code))
+        assert f32_to_bits(got) == int(bits, 16), (code, hex(f32_to_bits(got)))
+        seen += 1
+    assert seen == 16
+
+
+def test_e2m1_code8_is_negative_zero(orc):
+    v = orc.e2m1(8)
+    assert v == 0.0 and math.copysign(1.0, v) == -1.0
+
+
+def test_e8m0_edge_bytes_match_page(orc):
+    for k, bits in rows("e8m0_bytes.txt"):
+        got = orc.e8m0(int(k))
+        if bits == "nan":
+            assert math.isnan(got)
+        else:
+            assert f32_to_bits(got) == int(bits, 16), (k, hex(f32_to_bits(got)))
+
+
+def test_e8m0_every_byte_is_a_power_of_two(orc):
+    for k in range(255):
+        want = np.ldexp(np.float32(1.0), k - 127)  # 2^-127 is a float32 subnormal
+        assert same_f32(orc.e8m0(k), want), k
+    assert math.isnan(orc.e8m0(255))
+
+
+def test_decode_exhaustive_code_by_scale(orc):
+    # 256 rows (one per scale byte) x 32 columns (each code twice).
+    codes = np.tile(np.concatenate([np.arange(16), np.arange(16)]), (256, 1))
+    scales = np.arange(256).reshape(256, 1)
+    buf = encode(codes, scales)
+    got = orc.dequant(buf, 256, 32)
+    assert_same_f32_arrays(got, dense(codes, scales))
+    # the subnormal scale keeps its products exact (no flush to zero)
+    assert got[0, 1] == np.float32(2.0 ** -128) and got[0, 7] == np.float32(6 * 2.0 ** -127)
+
+
+# --- layout ------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [(1, 32), (3, 64), (7, 96), (16, 256), (5, 512)])
+def test_layout_against_independent_encoder(orc, shape):
+    rng = np.random.default_rng(sum(shape))
+    codes, scales = random_case(rng, *shape, lo=0, hi=255)
+    buf = encode(codes, scales)
+    assert_same_f32_arrays(orc.dequant(buf, *shape), dense(codes, scales))
+    r, c = shape[0] - 1, shape[1] - 3
+    assert orc.code_at(buf, *shape, r, c) == codes[r, c]
+    assert orc.scale_at(buf, *shape, r, c // 32) == scales[r, c // 32]
+
+
+def test_hand_worked_group(orc):
+    lines = list(rows("hand_group.txt"))
+    words = [int(w, 16) for w in lines[0][1:]]
+    x = np.arange(1, 33, dtype=np.float32)
+    for k, y_s, l1_s in lines[1:]:
+        buf = np.zeros(32, dtype=np.uint8)
+        buf[:16] = np.array(words, dtype="<u4").view(np.uint8)
+        buf[16] = int(k)
+        y, l1 = orc.matmat(buf, 1, 32, x, 1)
+        want_y, want_l1 = parse_value(y_s), parse_value(l1_s)
+        if math.isnan(want_y):
+            assert math.isnan(y[0, 0]) and math.isnan(l1[0, 0])
+        else:
+            assert y[0, 0] == want_y and l1[0, 0] == want_l1, (k, y, l1)
+
+
+def test_hand_worked_two_rows(orc):
+    lines = list(rows("hand_two_rows.txt"))
+    code_bytes = [int(b, 16) for b in lines[0][1:]]
+    scale_bytes = [int(b) for b in lines[1][1:]]
+    buf = np.zeros(80, dtype=np.uint8)
+    for i, b in enumerate(code_bytes):
+        buf[16 * i:16 * (i + 1)] = b
+    buf[64:68] = scale_bytes
+    x = np.concatenate([np.ones(32), 2 * np.ones(32)]).astype(np.float32)
+    y, l1 = orc.matmat(buf, 2, 64, x, 1)
+    for r, y_s, l1_s in lines[2:]:
+        r = int(r)
+        wy = parse_value(y_s)
+        if math.isnan(wy):
+            assert math.isnan(y[0, r])
+        else:
+            assert y[0, r] == wy and l1[0, r] == parse_value(l1_s)
+
+
+def test_nbytes_matches_page_examples(orc):
+    for r, c, n in rows("nbytes.txt"):
+        assert orc.nbytes_exact(int(r), int(c)) == int(n)
+    assert orc.nbytes_exact(4, 48) == 0 and orc.nbytes_exact(0, 32) == 0
+
+
+# --- products ----------------------------------------------------------------
+
+@pytest.mark.parametrize("shape,nb", [((1, 32), 1), ((9, 64), 2), ((33, 96), 3),
+                                      ((64, 128), 5), ((17, 32), 8)])
+def test_matmat_brute_force(orc, shape, nb):
+    rng = np.random.default_rng(7 * shape[0] + nb)
+    codes, scales = random_case(rng, *shape)
+    W = dense(codes, scales).astype(np.float64)
+    x = rng.standard_normal((nb, shape[1])).astype(np.float32)
+    y, l1 = orc.matmat(encode(codes, scales), *shape, x, nb)
+    want = x.astype(np.float64) @ W.T
+    want_l1 = np.abs(x.astype(np.float64)) @ np.abs(W).T
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-12 * want_l1.max())
+    np.testing.assert_allclose(l1, want_l1, rtol=1e-13)
+
+
+def test_matmat_exact_small_integers(orc):
+    # integer activations and scales near 1: every product and partial sum is
+    # exact in double, so any correct summation order gives the same bits.
+    rng = np.random.default_rng(3)
+    codes, scales = random_case(rng, 40, 256, lo=126, hi=128)
+    x = rng.integers(-4, 5, size=(3, 256)).astype(np.float32)
+    y, _ = orc.matmat(encode(codes, scales), 40, 256, x, 3)
+    want = x.astype(np.float64) @ dense(codes, scales).astype(np.float64).T
+    assert np.array_equal(y, want)
+
+
+def test_matmat_row_window_and_samples_agree(orc):
+    rng = np.random.default_rng(5)
+    codes, scales = random_case(rng, 20, 64)
+    buf = encode(codes, scales)
+    x = rng.standard_normal((4, 64)).astype(np.float32)
+    y, l1 = orc.matmat(buf, 20, 64, x, 4)
+    yw, _ = orc.matmat(buf, 20, 64, x, 4, 5, 11)
+    assert np.array_equal(yw, y[:, 5:11])
+    tok = np.array([0, 3, 2, 1]); row = np.array([19, 0, 7, 7])
+    ys, l1s = orc.matmat_samples(buf, 20, 64, x, tok, row)
+    assert np.array_equal(ys, y[tok, row]) and np.array_equal(l1s, l1[tok, row])
+
+
+def test_matmat_nan_scale_poisons_only_its_row(orc):
+    rng = np.random.default_rng(11)
+    codes, scales = random_case(rng, 6, 64)
+    scales[2, 1] = 255
+    y, _ = orc.matmat(encode(codes, scales), 6, 64, np.ones((1, 64), np.float32), 1)
+    assert np.isnan(y[0, 2]) and not np.isnan(np.delete(y[0], 2)).any()
+
+
+def test_matmat_zero_activation_gives_zero(orc):
+    rng = np.random.default_rng(12)
+    codes, scales = random_case(rng, 8, 64)
+    y, l1 = orc.matmat(encode(codes, scales), 8, 64, np.zeros((2, 64), np.float32), 2)
+    assert not y.any() and not l1.any()
+
+
+def test_bf16_rounding_fixture(orc):
+    for a, b in rows("bf16_rne.txt"):
+        got = orc.bf16_rne(bits_to_f32(int(a, 16)))
+        assert f32_to_bits(got) == int(b, 16), (a, hex(f32_to_bits(got)))
+    assert math.isnan(orc.bf16_rne(float("nan")))
+
+
+def test_bf16_rounding_matches_torch(orc):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(0)
+    with np.errstate(over="ignore", invalid="ignore"):
+        v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                            rng.integers(0, 2**32, 20000, dtype=np.uint64).astype(np.uint32)
+                            .view(np.float32)]).astype(np.float32)
+    v = v[np.isfinite(v)]
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
+    assert_same_f32_arrays(orc.round_bf16(v), want)
+
+
+def test_silu_and_its_derivative(orc):
+    scipy_special = pytest.importorskip("scipy.special")
+    for g in [-50.0, -3.5, -1e-3, 0.0, 0.7, 4.0, 30.0]:
+        assert orc.silu(g) == pytest.approx(g * scipy_special.expit(g), rel=1e-14, abs=1e-300)
+        h = 1e-6
+        num = (g + h) * scipy_special.expit(g + h) - (g - h) * scipy_special.expit(g - h)
+        assert orc.silu_grad(g) == pytest.approx(num / (2 * h), rel=1e-6, abs=1e-9)
+    assert orc.silu_grad(0.0) == 0.5
+
+
+# --- routed experts ----------------------------------------------------------
+
+def _tiny_moe(seed=0, E=5, hidden=64, inter=32, T=3, K=2):
+    rng = np.random.default_rng(seed)
+    banks, mats = {}, {}
+    for role, (r, c) in {"gate": (inter, hidden), "up": (inter, hidden),
+                         "down": (hidden, inter)}.items():
+        bufs, ms = [], []
+        for _ in range(E):
+            codes, scales = random_case(rng, r, c)
+            bufs.append(encode(codes, scales)); ms.append(dense(codes, scales).astype(np.float64))
+        banks[role], mats[role] = np.concatenate(bufs), ms
+    x = rng.standard_normal((T, hidden)).astype(np.float32)
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    wts = rng.random((T, K)).astype(np.float32)
+    stride_gu = synth.padded_nbytes(inter, hidden)
+    stride_dn = synth.padded_nbytes(hidden, inter)
+    return dict(E=E, hidden=hidden, inter=inter, T=T, K=K, banks=banks, mats=mats, x=x,
+                ids=ids, wts=wts, stride_gu=stride_gu, stride_dn=stride_dn)
+
+
+def test_moe_gate_up_against_dense_numpy(orc):
+    m = _tiny_moe()
+    res = orc.moe_gate_up(m["banks"]["gate"], m["banks"]["up"], m["stride_gu"], m["E"],
+                          m["hidden"], m["inter"], m["x"], m["T"], m["K"], m["ids"])
+    for t in range(m["T"]):
+        for j in range(m["K"]):
+            p, e = t * m["K"] + j, m["ids"][t, j]
+            xt = m["x"][t].astype(np.float64)
+            g = m["mats"]["gate"][e] @ xt
+            u = m["mats"]["up"][e] @ xt
+            np.testing.assert_allclose(res["g"][p], g, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(res["u"][p], u, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(res["l1g"][p], np.abs(m["mats"]["gate"][e]) @ np.abs(xt),
+                                       rtol=1e-12)
+            with np.errstate(over="ignore"):
+                act = g / (1.0 + np.exp(-g)) * u
+            np.testing.assert_allclose(res["act"][p], act, rtol=1e-11, atol=1e-12)
+
+
+def test_moe_down_against_dense_numpy(orc):
+    m = _tiny_moe(seed=1)
+    rng = np.random.default_rng(9)
+    act = rng.standard_normal((m["T"] * m["K"], m["inter"])).astype(np.float32)
+    res = orc.moe_down(m["banks"]["down"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                       act, m["T"], m["K"], m["ids"], m["wts"], want_pairs=True)
+    for t in range(m["T"]):
+        want = np.zeros(m["hidden"])
+        for j in range(m["K"]):
+            p, e = t * m["K"] + j, m["ids"][t, j]
+            o = m["mats"]["down"][e] @ act[p].astype(np.float64)
+            np.testing.assert_allclose(res["o_pairs"][p], o, rtol=1e-12, atol=1e-12)
+            want += np.float64(m["wts"][t, j]) * o
+        np.testing.assert_allclose(res["out"][t], want, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_forward_is_gate_up_then_down_in_double(orc):
+    m = _tiny_moe(seed=2)
+    fw = orc.moe_forward(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
+                         m["stride_gu"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                         m["x"], m["T"], m["K"], m["ids"], m["wts"])
+    for t in range(m["T"]):
+        want = np.zeros(m["hidden"])
+        for j in range(m["K"]):
+            e = m["ids"][t, j]
+            xt = m["x"][t].astype(np.float64)
+            g = m["mats"]["gate"][e] @ xt
+            u = m["mats"]["up"][e] @ xt
+            with np.errstate(over="ignore"):
+                a = g / (1.0 + np.exp(-g)) * u
+            want += np.float64(m["wts"][t, j]) * (m["mats"]["down"][e] @ a)
+        np.testing.assert_allclose(fw["out"][t], want, rtol=1e-11, atol=1e-11)
+    assert (fw["bound_l1"] >= np.abs(fw["out"]) * (1 - 1e-12)).all()
+    assert (fw["bound_prop"] > 0).all()
+
+
+def test_moe_plan_is_a_stable_counting_sort(orc):
+    rng = np.random.default_rng(4)
+    ids = rng.integers(0, 16, size=200).astype(np.int32)
+    ids[[5, 77]] = [-1, 16]  # two invalid ids
+    offsets, pair_of, bad = orc.moe_plan(ids, 16)
+    assert bad == 2
+    valid = np.flatnonzero((ids >= 0) & (ids < 16))
+    order = valid[np.argsort(ids[valid], kind="stable")]
+    assert np.array_equal(pair_of[:order.size], order)
+    assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(np.bincount(ids[valid],
+                                                                            minlength=16))]))
+
+
+# --- the seeded generator ----------------------------------------------------
+
+def test_splitmix64_published_outputs():
+    # First outputs of SplitMix64 from state 0 (Vigna's reference splitmix64.c).
+    want = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F, 0xF88BB8A8724C81EC]
+    assert [int(v) for v in synth.splitmix64(0, 4)] == want
+    assert [int(v) for v in synth.splitmix64(0, 2, start=2)] == want[2:]
+
+
+def test_generator_is_deterministic_and_shaped():
+    a = synth.TINY.weights()
+    b = synth.TINY.weights()
+    assert np.array_equal(a, b) and a.size == synth.padded_nbytes(256, 512) == 69632
+    s = a[256 * 512 // 2: 256 * 512 // 2 + 256 * 16]
+    assert s[3 * 16 + 5] == 0 and s[250 * 16 + 11] == 255
+    body = np.delete(s, [3 * 16 + 5, 250 * 16 + 11])
+    assert body.min() >= 118 and body.max() <= 136
+    x = synth.TINY.activations()
+    assert x.shape == (1, 512) and x.dtype == np.float32 and abs(x.mean()) < 0.2
+
+
+def test_route_generator_distinct_ids_and_softmax():
+    ids, w = synth.routes(3, 32, 4, 64)
+    assert ids.shape == (32, 4) and (ids >= 0).all() and (ids < 64).all()
+    assert all(len(set(r)) == 4 for r in ids.tolist())
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-6)
+    assert (w > 0).all()
+
+
+def test_expert_banks_have_distinct_scale_planes():
+    E, r, c = 5, 32, 64
+    bank = synth.expert_bank(E, r, c, 3, 118, 130, "gate")
+    stride = synth.padded_nbytes(r, c)
+    planes = [bank[e * stride + r * c // 2: e * stride + r * c // 2 + r * c // 32].tobytes()
+              for e in range(E)]
+    assert len(set(planes)) == E
+
+
+def test_adjacent_distinct_scale_pattern():
+    buf = synth.mxfp4_matrix(8, 128, 4, 119, 123, scale_pattern="adjacent_distinct")
+    s = buf[8 * 64: 8 * 64 + 32].astype(int)
+    assert (np.diff(s) != 0).all() and s.min() >= 119 and s.max() <= 123
