@@ -229,6 +229,8 @@ void moe_down_impl(const uint8_t* down_bank, size_t stride_bytes, int n_experts,
                 }
                 if (o_pairs) o_pairs[p * hidden + r] = o;
                 if (l1_pairs) l1_pairs[p * hidden + r] = m;
+                // A pair routed to an out-of-range expert contributes nothing.
+                if (!valid_expert(e, n_experts)) continue;
                 out[static_cast<size_t>(t) * hidden + r] += wt * o;
                 l1_out[static_cast<size_t>(t) * hidden + r] += std::fabs(wt) * m;
             }
@@ -271,10 +273,7 @@ void mxo_moe_forward(const uint8_t* gate_bank, const uint8_t* up_bank,
             for (int j = 0; j < top_k; ++j) {
                 const size_t p = static_cast<size_t>(t) * top_k + j;
                 const int32_t e = ids[p];
-                if (!valid_expert(e, n_experts)) {
-                    acc = std::numeric_limits<double>::quiet_NaN();
-                    continue;
-                }
+                if (!valid_expert(e, n_experts)) continue;   // contributes nothing
                 const uint8_t* de = down_bank + static_cast<size_t>(e) * down_stride_bytes;
                 double s = 0.0;
                 for (int c = 0; c < inter; ++c)

@@ -99,7 +99,8 @@ void mxo_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
  *   out[t*hidden + r] = sum_j route_w[t*top_k + j] * o_{t*top_k+j}[r],
  * summed over slots j in order, with
  *   l1_out[t*hidden + r] = sum_j |route_w| * sum_c |down_e[r][c] * act_p[c]|.
- * o_pairs / l1_pairs may be NULL.  (dsv4_global_down_mxfp4, generic f32 mode;
+ * A pair whose expert id is out of range gets NaN in o_pairs / l1_pairs and
+ * contributes nothing to out.  o_pairs / l1_pairs may be NULL.  (dsv4_global_down_mxfp4, generic f32 mode;
  * moe_fast.rs down_block; rlx-cpu gguf_matmul.rs grouped_moe_unpermute_out.) */
 void mxo_moe_down(const uint8_t* down_bank, size_t stride_bytes, int n_experts,
                   int hidden, int inter, const float* act, int n_tokens,

@@ -341,3 +341,20 @@ def test_adjacent_distinct_scale_pattern():
     buf = synth.mxfp4_matrix(8, 128, 4, 119, 123, scale_pattern="adjacent_distinct")
     s = buf[8 * 64: 8 * 64 + 32].astype(int)
     assert (np.diff(s) != 0).all() and s.min() >= 119 and s.max() <= 123
+
+
+def test_moe_invalid_pair_contributes_nothing(orc):
+    m = _tiny_moe(seed=3)
+    ids = m["ids"].copy()
+    ids[1, 0] = m["E"]          # out of range
+    rng = np.random.default_rng(2)
+    act = rng.standard_normal((m["T"] * m["K"], m["inter"])).astype(np.float32)
+    res = orc.moe_down(m["banks"]["down"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                       act, m["T"], m["K"], ids, m["wts"], want_pairs=True)
+    p_bad = 1 * m["K"] + 0
+    assert np.isnan(res["o_pairs"][p_bad]).all()
+    e1 = ids[1, 1]
+    want = np.float64(m["wts"][1, 1]) * (m["mats"]["down"][e1] @ act[p_bad + 1].astype(np.float64))
+    np.testing.assert_allclose(res["out"][1], want, rtol=1e-12, atol=1e-12)
+    offsets, pair_of, bad = orc.moe_plan(ids.reshape(-1), m["E"])
+    assert bad == 1 and p_bad not in pair_of[:offsets[-1]]
