@@ -1,0 +1,178 @@
+/*
+ * mxfp4.h -- C ABI of libmxfp4.so: fused MXFP4 dequantisation with matrix-vector,
+ * small-batch and large-batch matrix products and the two routed-expert (MoE)
+ * passes, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Source of the operations: the docs.rs page "cortiq-engine 0.8.40
+ * src/gpu_wgpu/mxfp4.rs" (const DECODE, const PEROP kernels mxfp4_mv /
+ * mxfp4_mm, const GLOBAL kernels dsv4_global_gate_up_mxfp4 /
+ * dsv4_global_down_mxfp4, host fn matmat), with the expert grouping of
+ * "rlx-cpu 0.2.17 src/gguf_matmul.rs" (grouped_moe_sort_plan,
+ * grouped_moe_unpermute_out).
+ *
+ * ---------------------------------------------------------------------------
+ * Weight format (one [rows, cols] matrix, cols % 32 == 0, gpr = cols / 32):
+ *   bytes [0, rows*cols/2)               code plane: for row r and group g, four
+ *                                        little-endian u32 words at word index
+ *                                        (r*gpr + g)*4 + k; nibble j (bits
+ *                                        4j..4j+3) of word k is element
+ *                                        c = 32g + 8k + j.  (PEROP mxfp4_mv.)
+ *   bytes [rows*cols/2, +rows*gpr)       scale plane: E8M0 byte r*gpr + g.
+ *                                        (PEROP fn mx_scale, struct MxP sbase.)
+ *   then padding up to mxfp4_nbytes(rows, cols) (never read as data).
+ * Decode: E2M1 code n -> +-{0, .5, 1, 1.5, 2, 3, 4, 6}[n & 7], bit 3 = sign
+ * (code 8 = -0.0); E8M0 byte k -> 2^(k-127), k = 0 -> 2^-127 (subnormal, kept),
+ * k = 255 -> NaN; element = code value * scale.  (DECODE mx_e2m1 / mx_e8m0.)
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  Except the
+ *     host-buffer wrapper mxfp4_matmat_host, the library allocates nothing and
+ *     copies nothing between host and device.
+ *   - Weight pointers must be 16-byte aligned and hold mxfp4_nbytes(rows, cols)
+ *     bytes; float pointers must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream); calls are
+ *     asynchronous (no device synchronisation) unless stated otherwise.
+ *   - Return value: an MXFP4_STATUS_* code.  On any non-zero code nothing was
+ *     enqueued, except MXFP4_STATUS_LAUNCH_FAILED, which reports the CUDA error
+ *     left by a launch (mxfp4_last_cuda_error() gives the cudaError_t).  There
+ *     is no CPU fallback.  (The page's matmat returns false for every refusal.)
+ *   - Results are deterministic: the same inputs give the same bits, run after
+ *     run (no floating-point atomics).
+ * ---------------------------------------------------------------------------
+ */
+#ifndef MXFP4_H
+#define MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MXFP4_STATUS_OK = 0,
+    MXFP4_STATUS_INVALID_ARGUMENT = 1, /* shape, count or id out of range    */
+    MXFP4_STATUS_BAD_POINTER = 2,      /* NULL or misaligned pointer         */
+    MXFP4_STATUS_LAUNCH_FAILED = 3,    /* CUDA reported an error             */
+    MXFP4_STATUS_WORKSPACE_TOO_SMALL = 4
+};
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* mxfp4_status_string(int status);
+
+/* cudaError_t recorded by the last MXFP4_STATUS_LAUNCH_FAILED on this thread. */
+int mxfp4_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int mxfp4_version(void);
+
+/* Bytes a [rows, cols] weight buffer must hold: rows*cols*17/32 (code plane +
+ * scale plane, the page's MoeBankCodec::lens / tests bank_codec_lengths length)
+ * rounded up to a multiple of 16 so that every row can be read with 16-byte
+ * loads.  0 if rows < 1, cols < 32 or cols % 32 != 0. */
+size_t mxfp4_nbytes(int rows, int cols);
+
+/* Standalone decode: out[r*cols + c] = element (r, c) as float, bit-exact
+ * (E2M1 value times E8M0 scale is exact in float; NaN for k = 255).
+ * out: [rows*cols] floats.  (DECODE; the page's tests decode the whole matrix
+ * with cortiq_core::mxfp4::dequant as their reference.) */
+int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t stream);
+
+/* Matrix-vector product, one token: y[r] = sum_c W[r][c] * x[c], FP32
+ * arithmetic on the CUDA cores (per group: the 32 code values dotted with x,
+ * then scaled; the row's group partials reduced across a warp).
+ * x: [cols] floats, y: [rows] floats.  Error bound: |y - exact| <= 1e-5 *
+ * sum_c |W[r][c] x[c]| (a NaN scale makes the row NaN).  (PEROP mxfp4_mv.) */
+int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
+             cudaStream_t stream);
+
+/* Batched product: Y[t*rows + r] = sum_c W[r][c] * X[t*cols + c], t < nb.
+ * X: [nb, cols] row-major floats, Y: [nb, rows] (the page's matmat output
+ * layout).  Dispatch on nb:
+ *   nb <= MXFP4_MM_SMALL_MAX: the small-batch path -- each weight group is
+ *     decoded once and applied to up to 8 tokens at a time (PEROP mxfp4_mm);
+ *     same error bound as mxfp4_mv.
+ *   nb >  MXFP4_MM_SMALL_MAX: the tensor-core path of mxfp4_mm_bf16 (below):
+ *     X is rounded to bfloat16 first. */
+#define MXFP4_MM_SMALL_MAX 64
+int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+             cudaStream_t stream);
+
+/* The small-batch path for any nb >= 1, regardless of MXFP4_MM_SMALL_MAX.  Per
+ * token the result is bit-identical to mxfp4_mv on that token (same group walk,
+ * same reduction tree), the invariant the page's device test checks
+ * ("the batch equal to the matvec per token bit for bit"). */
+int mxfp4_mm_fp32(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                  cudaStream_t stream);
+
+/* Large-batch (prefill) product on the tensor cores: W decoded exactly to
+ * bfloat16, X rounded to nearest-even bfloat16 (GLOBAL fn mxg_bf16), products
+ * accumulated in FP32.  Same shapes and layouts as mxfp4_mm, any nb >= 1.
+ * Error bound against the product of W and bf16(X): 2e-2 * sum_c |W bf16(X)|
+ * (tighter in practice).  The decoded weight is exact in bfloat16 for every
+ * scale byte (scale bytes 0 and 1 give bfloat16 subnormals, which the tensor
+ * cores keep). */
+int mxfp4_mm_bf16(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                  cudaStream_t stream);
+
+/* p2-style host entry (the page's fn matmat): X and Y are HOST buffers, the
+ * weight stays resident on the device.  Copies X to x_dev, runs mxfp4_mm
+ * (mxfp4_mv when nb == 1), copies the result back to Y and synchronises the
+ * stream.  x_dev: >= nb*cols floats, y_dev: >= nb*rows floats (device, owned by
+ * the caller).  Pinned host memory gives asynchronous copies. */
+int mxfp4_matmat_host(const void* w, int rows, int cols, const float* X_host, int nb,
+                      float* Y_host, float* x_dev, float* y_dev, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Routed experts.  Banks: expert e's gate and up matrices ([inter, hidden]) are
+ * at byte offset e * mxfp4_nbytes(inter, hidden) of gate_bank / up_bank, its
+ * down matrix ([hidden, inter]) at e * mxfp4_nbytes(hidden, inter) of
+ * down_bank.  Pairs: p = t*top_k + j for token t < n_tokens and slot
+ * j < top_k; expert_ids[p] and route_w[p] are the routing choice and weight
+ * (the page's gg_sel / gd_wt in their [batch, slots] layout).
+ * -------------------------------------------------------------------------- */
+
+/* Workspace bytes the two passes need (routing plan + per-pair down outputs). */
+size_t mxfp4_moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden,
+                                 int inter);
+
+/* Gate/up pass: builds the routing plan (counting sort of the pairs by expert,
+ * rlx-cpu grouped_moe_sort_plan) into `workspace`, then for every touched
+ * expert reads its gate and up matrices ONCE for all of its pairs and writes
+ *   act[p*inter + r] = silu(g) * u,  g = gate_e[r] . x_t,  u = up_e[r] . x_t,
+ * silu(g) = g / (1 + exp(-g)), FP32 (dsv4_global_gate_up_mxfp4 without BF16
+ * rounding, limit or pre-weighting).  x: [n_tokens, hidden]; act:
+ * [n_tokens*top_k, inter].  Pairs with an out-of-range expert id are skipped
+ * (their act rows are left untouched) and counted in the plan's error word,
+ * readable with mxfp4_moe_plan_errors.  The plan stays valid for
+ * mxfp4_moe_down only while expert_ids and workspace are unchanged. */
+int mxfp4_moe_gate_up(const void* gate_bank, const void* up_bank, int n_experts,
+                      int hidden, int inter, const float* x, int n_tokens, int top_k,
+                      const int32_t* expert_ids, float* act, void* workspace,
+                      size_t ws_bytes, cudaStream_t stream);
+
+/* Down pass + weighted combine, reusing the plan left in `workspace` by
+ * mxfp4_moe_gate_up: per touched expert, its down matrix is read once for all
+ * its pairs, o_p[r] = down_e[r] . act_p (FP32, kept in the workspace), then
+ *   y[t*hidden + r] = sum_j route_w[t*top_k + j] * o_{t*top_k + j}[r]
+ * summed over j in slot order (dsv4_global_down_mxfp4's generic f32 mode, which
+ * fuses the combine; rlx-cpu grouped_moe_unpermute_out).  A pair with an
+ * invalid id contributes nothing.  y: [n_tokens, hidden]. */
+int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter,
+                   const float* act, int n_tokens, int top_k, const int32_t* expert_ids,
+                   const float* route_w, float* y, void* workspace, size_t ws_bytes,
+                   cudaStream_t stream);
+
+/* Copies the plan's count of out-of-range expert ids to *n_invalid (host) and
+ * synchronises the stream.  For tests and debugging; the passes themselves
+ * never synchronise. */
+int mxfp4_moe_plan_errors(const void* workspace, size_t ws_bytes, int* n_invalid,
+                          cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_H */

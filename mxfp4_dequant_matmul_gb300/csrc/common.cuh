@@ -1,0 +1,82 @@
+// common.cuh -- device-side MXFP4 decode and small helpers shared by the
+// kernels of libmxfp4.so (sm_103a).
+//
+// Format ("cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs", const DECODE and
+// const PEROP): a [rows, cols] matrix is a code plane of rows*cols/2 bytes --
+// group g of row r is 16 bytes at byte (r*gpr + g)*16, four little-endian u32
+// words, nibble j of word k being element 32g + 8k + j -- followed by a scale
+// plane with one E8M0 byte per group at byte rows*cols/2 + r*gpr + g.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mxk {
+
+constexpr int kGroup = 32;        // elements per scale group
+constexpr int kGroupBytes = 16;   // code bytes per group
+
+// E8M0 byte -> float (DECODE fn mx_e8m0): the bits k << 23 give 2^(k-127);
+// k = 0 gives the subnormal 2^-127 (bits 0x00400000), k = 255 gives NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t k) {
+    uint32_t bits = (k == 0u) ? 0x00400000u : (k << 23);
+    bits = (k == 255u) ? 0x7FC00000u : bits;
+    return __uint_as_float(bits);
+}
+
+// Two f16 halves of a register -> two floats (exact widening).
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return make_float2(lo, hi);
+}
+
+// The four bytes of a code word (8 E2M1 codes) -> four f16x2 registers with
+// the hardware E2M1 pair conversion: byte b holds codes 2b (low nibble) and
+// 2b+1 (high nibble), which land in the low and high half of result b.  Every
+// E2M1 value (0, +-0.5 .. +-6, -0 for code 8) is exact in f16.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// One code word -> its 8 element values as floats (exact).
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(w, h);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const float2 f = f16x2_to_f32x2(h[b]);
+        v[2 * b] = f.x;
+        v[2 * b + 1] = f.y;
+    }
+}
+
+// Device pointer arithmetic on the two planes.
+__device__ __forceinline__ const uint4* group_codes(const uint8_t* w, size_t gpr, size_t row,
+                                                    size_t g) {
+    return reinterpret_cast<const uint4*>(w + (row * gpr + g) * kGroupBytes);
+}
+
+__device__ __forceinline__ uint32_t group_scale_byte(const uint8_t* scales, size_t gpr,
+                                                     size_t row, size_t g) {
+    return __ldg(scales + row * gpr + g);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+    // Weights are read once per call: do not keep them in L1.
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+}  // namespace mxk

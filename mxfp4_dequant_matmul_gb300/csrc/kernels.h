@@ -1,0 +1,40 @@
+// kernels.h -- host-side launchers of the libmxfp4.so kernels (internal).
+// The C ABI in mxfp4_api.cu validates every argument before calling these.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mxk {
+
+// Standalone decode of a whole matrix to float (bit-exact).
+cudaError_t launch_dequant(const uint8_t* w, int rows, int cols, float* out, cudaStream_t s);
+
+// FP32 small-batch product (nb = 1 is the matvec).  Per token bit-identical
+// whatever nb is.
+cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                               float* Y, cudaStream_t s);
+
+// Tensor-core product with X rounded to bfloat16.
+cudaError_t launch_mm_bf16(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                           float* Y, cudaStream_t s);
+
+// Routed experts.  The workspace layout is owned by moe.cu.
+size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter);
+cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,
+                               int hidden, int inter, const float* x, int n_tokens, int top_k,
+                               const int32_t* ids, float* act, void* ws, cudaStream_t s);
+cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden, int inter,
+                            const float* act, int n_tokens, int top_k, const int32_t* ids,
+                            const float* route_w, float* y, void* ws, cudaStream_t s);
+cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
+
+// Bytes of one [rows, cols] buffer, padded to 16.
+inline size_t padded_nbytes(int rows, int cols) {
+    const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) / 32 * 17;
+    return (n + 15) / 16 * 16;
+}
+
+}  // namespace mxk

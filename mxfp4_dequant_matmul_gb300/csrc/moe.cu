@@ -1,0 +1,298 @@
+// moe.cu -- routed-expert passes over MXFP4 expert banks (sm_103a).
+//
+// Sources: "cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs" kernels
+// dsv4_global_gate_up_mxfp4 (act = silu(gate.x) * (up.x) per routed pair) and
+// dsv4_global_down_mxfp4 (down . act, weighted by the route weight and summed
+// over the token's slots); "rlx-cpu 0.2.17 src/gguf_matmul.rs"
+// grouped_moe_sort_plan (counting sort of the routed pairs by expert) and
+// grouped_moe_unpermute_out (back to token order); "cortiq-engine 0.8.77
+// src/qtensor/moe_fast.rs" (gate and up read once for all of an expert's
+// tokens; act laid out [pair, inter]).
+//
+// Unlike the page's kernels, which walk every routed slot of every token and
+// so read an expert's weights once per pair, the work here is grouped by
+// expert: each touched expert's gate, up and down matrices are read once per
+// call, their decode shared by all of the expert's pairs.
+//
+// Pipeline (all stream-ordered, no inter-CTA waits):
+//   k_moe_plan      one CTA: counts, offsets, touched-expert list, pair lists
+//   k_moe_gate_up   persistent CTAs over (touched expert, row block) units
+//   k_moe_down      same units over the down matrices -> per-pair outputs
+//   k_moe_combine   y[t] = sum_j w[t,j] * o[t*top_k + j], slots in order
+#include <mutex>
+
+#include "matmat_core.cuh"
+#include "kernels.h"
+
+namespace mxk {
+namespace {
+
+// Workspace layout (all offsets 16-byte aligned; o_pairs 256-byte aligned).
+struct WsLayout {
+    size_t hdr, offsets, touched, pair_of, o_pairs, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(int n_experts, int n_pairs, int hidden) {
+    WsLayout l;
+    l.hdr = 0;                                            // int32[4]: invalid, touched
+    l.offsets = 16;                                       // int32[E + 1]
+    l.touched = align_up(l.offsets + 4 * (static_cast<size_t>(n_experts) + 1), 16);
+    l.pair_of = align_up(l.touched + 4 * static_cast<size_t>(n_experts), 16);
+    l.o_pairs = align_up(l.pair_of + 4 * static_cast<size_t>(n_pairs), 256);
+    l.total = l.o_pairs + 4 * static_cast<size_t>(n_pairs) * hidden;
+    return l;
+}
+
+struct Plan {
+    int32_t* hdr;
+    int32_t* offsets;
+    int32_t* touched;
+    int32_t* pair_of;
+    float* o_pairs;
+};
+
+Plan plan_view(void* ws, int n_experts, int n_pairs, int hidden) {
+    const WsLayout l = ws_layout(n_experts, n_pairs, hidden);
+    char* b = static_cast<char*>(ws);
+    return Plan{reinterpret_cast<int32_t*>(b + l.hdr), reinterpret_cast<int32_t*>(b + l.offsets),
+                reinterpret_cast<int32_t*>(b + l.touched),
+                reinterpret_cast<int32_t*>(b + l.pair_of),
+                reinterpret_cast<float*>(b + l.o_pairs)};
+}
+
+// ---------------------------------------------------------------------------
+// Routing plan, one CTA.  Thread e counts and then lists the pairs of expert e
+// (stable: increasing pair index), as the counting sort of
+// grouped_moe_sort_plan does; thread 0 prefix-sums the counts.
+__global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ ids, int n_pairs,
+                                                   int n_experts, Plan plan) {
+    __shared__ int s_invalid;
+    if (threadIdx.x == 0) s_invalid = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) {
+        const int32_t e = __ldg(ids + p);
+        bad += (e < 0 || e >= n_experts) ? 1 : 0;
+    }
+    if (bad) atomicAdd(&s_invalid, bad);
+    for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+        int count = 0;
+        for (int p = 0; p < n_pairs; ++p) count += (__ldg(ids + p) == e) ? 1 : 0;
+        plan.offsets[e + 1] = count;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0, touched = 0;
+        plan.offsets[0] = 0;
+        for (int e = 0; e < n_experts; ++e) {
+            const int c = plan.offsets[e + 1];
+            if (c > 0) plan.touched[touched++] = e;
+            run += c;
+            plan.offsets[e + 1] = run;
+        }
+        plan.hdr[0] = s_invalid;
+        plan.hdr[1] = touched;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
+        int pos = plan.offsets[e];
+        for (int p = 0; p < n_pairs; ++p)
+            if (__ldg(ids + p) == e) plan.pair_of[pos++] = p;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of up to NB pairs of expert e against NM matrices; `rows` rows,
+// `cols` columns.  Epilogue by pass.
+enum class Pass { kGateUp, kDown };
+
+template <Pass P, int R, int NB>
+__device__ __forceinline__ void expert_chunk(const uint8_t* const (&wm)[P == Pass::kGateUp ? 2 : 1],
+                                             int rows, int cols, long row_w,
+                                             const int32_t* pairs, int n, int top_k,
+                                             const float* vec_base, float* out, float* xs) {
+    constexpr int NM = P == Pass::kGateUp ? 2 : 1;
+    const int lane = threadIdx.x & 31;
+    const float* xt[NB];
+    int pr[NB];
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+        pr[t] = t < n ? pairs[t] : 0;
+        // gate/up reads the token's x; down reads the pair's act row
+        const size_t vrow = P == Pass::kGateUp ? static_cast<size_t>(pr[t] / top_k)
+                                               : static_cast<size_t>(pr[t]);
+        xt[t] = t < n ? vec_base + vrow * cols : nullptr;
+    }
+    float acc[NM][R][NB];
+    zero(acc);
+    cta_group_walk<R, NB, NM, false>(wm, rows, cols, row_w, xt, xs, acc);
+    warp_allreduce(acc);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int t = 0; t < NB; ++t)
+            if (lane == ((i * NB + t) & 31) && row_w + i < rows && t < n) {
+                const size_t o = static_cast<size_t>(pr[t]) * rows + row_w + i;
+                if constexpr (P == Pass::kGateUp) {
+                    const float g = acc[0][i][t];
+                    const float u = acc[1][i][t];
+                    out[o] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                } else {
+                    out[o] = acc[0][i][t];
+                }
+            }
+}
+
+// Persistent over units (touched expert u, row block rb), u-major.
+template <Pass P, int R>
+__global__ void __launch_bounds__(kThreads) k_moe_pass(const uint8_t* __restrict__ bank0,
+                                                       const uint8_t* __restrict__ bank1,
+                                                       size_t stride, int rows, int cols,
+                                                       int top_k, const float* __restrict__ vec,
+                                                       Plan plan, float* __restrict__ out) {
+    extern __shared__ float4 smem4[];
+    float* xs = reinterpret_cast<float*>(smem4);
+    constexpr int NM = P == Pass::kGateUp ? 2 : 1;
+    const int warp = threadIdx.x >> 5;
+    const int n_touched = plan.hdr[1];
+    const int rbn = (rows + kWarps * R - 1) / (kWarps * R);
+    const int total = n_touched * rbn;
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+        const int u = unit / rbn, rb = unit - u * rbn;
+        const int e = plan.touched[u];
+        const int beg = plan.offsets[e], n_e = plan.offsets[e + 1] - beg;
+        const long row_w = static_cast<long>(rb) * (kWarps * R) + warp * R;
+        const uint8_t* wm[NM];
+        wm[0] = bank0 + static_cast<size_t>(e) * stride;
+        if constexpr (NM == 2) wm[1] = bank1 + static_cast<size_t>(e) * stride;
+        const uint8_t* const(&wmc)[NM] = wm;
+        for (int c = 0; c < n_e; c += 8) {
+            const int n = min(8, n_e - c);
+            const int32_t* pairs = plan.pair_of + beg + c;
+            if (n == 1)
+                expert_chunk<P, R, 1>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+            else if (n == 2)
+                expert_chunk<P, R, 2>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+            else if (n <= 4)
+                expert_chunk<P, R, 4>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+            else
+                expert_chunk<P, R, 8>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+        }
+    }
+}
+
+// y[t*hidden + r] = sum over slots j (in order) of w[t,j] * o[(t*top_k+j)*hidden + r].
+__global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ o_pairs,
+                                                     const int32_t* __restrict__ ids,
+                                                     const float* __restrict__ route_w,
+                                                     int n_experts, int n_tokens, int top_k,
+                                                     int hidden, float* __restrict__ y) {
+    const size_t n = static_cast<size_t>(n_tokens) * hidden;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t t = i / hidden, r = i - t * hidden;
+        float acc = 0.0f;
+        for (int j = 0; j < top_k; ++j) {
+            const size_t p = t * top_k + j;
+            const int32_t e = __ldg(ids + p);
+            if (e >= 0 && e < n_experts)
+                acc = __fmaf_rn(__ldg(route_w + p), __ldg(o_pairs + p * hidden + r), acc);
+        }
+        y[i] = acc;
+    }
+}
+
+// Persistent grid size for a kernel: resident CTAs per SM times the SM count.
+int persistent_grid(const void* kernel, size_t smem) {
+    static std::mutex mu;
+    static int cache_dev[16] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    static int cache_sms[16];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 16 && cache_dev[dev] == dev) {
+            sms = cache_sms[dev];
+        } else {
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                sms = 152;
+            if (dev < 16) {
+                cache_dev[dev] = dev;
+                cache_sms[dev] = sms;
+            }
+        }
+    }
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    return sms * per_sm;
+}
+
+constexpr int kRowsPerWarp = 2;
+
+template <Pass P>
+cudaError_t launch_pass(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
+                        int rows, int cols, int top_k, const float* vec, Plan plan, float* out,
+                        cudaStream_t s) {
+    auto kernel = k_moe_pass<P, kRowsPerWarp>;
+    const long rbn = (rows + kWarps * kRowsPerWarp - 1) / (kWarps * kRowsPerWarp);
+    const long max_units = static_cast<long>(n_experts) * rbn;
+    const long cap = persistent_grid(reinterpret_cast<const void*>(kernel), kStageBytes);
+    const unsigned grid = static_cast<unsigned>(max_units < cap ? max_units : cap);
+    kernel<<<grid, kThreads, kStageBytes, s>>>(bank0, bank1, stride, rows, cols, top_k, vec, plan,
+                                               out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter) {
+    (void)inter;
+    return ws_layout(n_experts, n_tokens * top_k, hidden).total;
+}
+
+cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,
+                               int hidden, int inter, const float* x, int n_tokens, int top_k,
+                               const int32_t* ids, float* act, void* ws, cudaStream_t s) {
+    const int n_pairs = n_tokens * top_k;
+    const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
+    k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t stride = padded_nbytes(inter, hidden);
+    return launch_pass<Pass::kGateUp>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k,
+                                      x, plan, act, s);
+}
+
+cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden, int inter,
+                            const float* act, int n_tokens, int top_k, const int32_t* ids,
+                            const float* route_w, float* y, void* ws, cudaStream_t s) {
+    const int n_pairs = n_tokens * top_k;
+    const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
+    const size_t stride = padded_nbytes(hidden, inter);
+    cudaError_t e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_experts, hidden, inter,
+                                             top_k, act, plan, plan.o_pairs, s);
+    if (e != cudaSuccess) return e;
+    const size_t n = static_cast<size_t>(n_tokens) * hidden;
+    const unsigned blocks = static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    k_moe_combine<<<blocks, 256, 0, s>>>(plan.o_pairs, ids, route_w, n_experts, n_tokens, top_k,
+                                         hidden, y);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s) {
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    *n_invalid = v;
+    return cudaSuccess;
+}
+
+}  // namespace mxk

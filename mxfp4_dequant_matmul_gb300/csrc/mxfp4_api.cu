@@ -1,0 +1,188 @@
+// mxfp4_api.cu -- the extern "C" boundary of libmxfp4.so (declared in
+// include/mxfp4.h).  Every entry point validates its arguments on the host,
+// refuses with a status code (launching nothing) when they are wrong, and
+// otherwise enqueues kernels on the caller's stream.  The refusal rules follow
+// "cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs" host fn matmat (b == 0,
+// rows == 0, cols % 32 != 0 or short buffers are refused), without its CPU
+// fallback.
+#include <cstdint>
+
+#include "../../include/mxfp4.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MXFP4_STATUS_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return MXFP4_STATUS_LAUNCH_FAILED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// rows >= 1, cols >= 32 and a multiple of 32, rows*cols small enough that every
+// byte offset fits comfortably in 63 bits and every row index in an int.
+int check_shape(int rows, int cols) {
+    if (rows < 1 || cols < 32 || cols % 32 != 0) return MXFP4_STATUS_INVALID_ARGUMENT;
+    if (static_cast<long long>(rows) * cols > (1LL << 46)) return MXFP4_STATUS_INVALID_ARGUMENT;
+    return MXFP4_STATUS_OK;
+}
+
+int check_ptr(const void* p) {
+    return (p == nullptr || !aligned16(p)) ? MXFP4_STATUS_BAD_POINTER : MXFP4_STATUS_OK;
+}
+
+#define MXFP4_TRY(expr)                            \
+    do {                                           \
+        const int _st = (expr);                    \
+        if (_st != MXFP4_STATUS_OK) return _st;    \
+    } while (0)
+
+int check_product(const void* w, int rows, int cols, const float* X, int nb, const float* Y) {
+    MXFP4_TRY(check_shape(rows, cols));
+    if (nb < 1 || nb > (1 << 24)) return MXFP4_STATUS_INVALID_ARGUMENT;
+    MXFP4_TRY(check_ptr(w));
+    MXFP4_TRY(check_ptr(X));
+    MXFP4_TRY(check_ptr(Y));
+    return MXFP4_STATUS_OK;
+}
+
+const uint8_t* u8(const void* p) { return static_cast<const uint8_t*>(p); }
+
+}  // namespace
+
+extern "C" {
+
+const char* mxfp4_status_string(int status) {
+    switch (status) {
+        case MXFP4_STATUS_OK: return "ok";
+        case MXFP4_STATUS_INVALID_ARGUMENT: return "invalid argument";
+        case MXFP4_STATUS_BAD_POINTER: return "null or misaligned pointer";
+        case MXFP4_STATUS_LAUNCH_FAILED: return "CUDA launch failed";
+        case MXFP4_STATUS_WORKSPACE_TOO_SMALL: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+int mxfp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+int mxfp4_version(void) { return 100; }
+
+size_t mxfp4_nbytes(int rows, int cols) {
+    if (check_shape(rows, cols) != MXFP4_STATUS_OK) return 0;
+    return mxk::padded_nbytes(rows, cols);
+}
+
+int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t stream) {
+    MXFP4_TRY(check_shape(rows, cols));
+    MXFP4_TRY(check_ptr(w));
+    MXFP4_TRY(check_ptr(out));
+    return from_cuda(mxk::launch_dequant(u8(w), rows, cols, out, stream));
+}
+
+int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y, cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, x, 1, y));
+    return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, x, 1, y, stream));
+}
+
+int mxfp4_mm_fp32(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                  cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
+    return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, X, nb, Y, stream));
+}
+
+int mxfp4_mm_bf16(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                  cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
+    return from_cuda(mxk::launch_mm_bf16(u8(w), rows, cols, X, nb, Y, stream));
+}
+
+int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+             cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
+    if (nb <= MXFP4_MM_SMALL_MAX)
+        return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, X, nb, Y, stream));
+    return from_cuda(mxk::launch_mm_bf16(u8(w), rows, cols, X, nb, Y, stream));
+}
+
+int mxfp4_matmat_host(const void* w, int rows, int cols, const float* X_host, int nb,
+                      float* Y_host, float* x_dev, float* y_dev, cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, x_dev, nb, y_dev));
+    if (X_host == nullptr || Y_host == nullptr) return MXFP4_STATUS_BAD_POINTER;
+    const size_t xb = static_cast<size_t>(nb) * cols * sizeof(float);
+    const size_t yb = static_cast<size_t>(nb) * rows * sizeof(float);
+    cudaError_t e = cudaMemcpyAsync(x_dev, X_host, xb, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    const int st = nb == 1 ? mxfp4_mv(w, rows, cols, x_dev, y_dev, stream)
+                           : mxfp4_mm(w, rows, cols, x_dev, nb, y_dev, stream);
+    if (st != MXFP4_STATUS_OK) return st;
+    e = cudaMemcpyAsync(Y_host, y_dev, yb, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(cudaStreamSynchronize(stream));
+}
+
+size_t mxfp4_moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter) {
+    if (n_experts < 1 || n_tokens < 1 || top_k < 1 || hidden < 32 || inter < 32) return 0;
+    return mxk::moe_workspace_bytes(n_experts, n_tokens, top_k, hidden, inter);
+}
+
+namespace {
+
+int check_moe(int n_experts, int hidden, int inter, int n_tokens, int top_k, const void* ws,
+              size_t ws_bytes) {
+    if (n_experts < 1 || n_experts > (1 << 20) || n_tokens < 1 || top_k < 1 ||
+        static_cast<long long>(n_tokens) * top_k > (1 << 22))
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    MXFP4_TRY(check_shape(inter, hidden));   // gate / up: [inter, hidden]
+    MXFP4_TRY(check_shape(hidden, inter));   // down: [hidden, inter]
+    if (static_cast<long long>(n_experts) * inter * hidden > (1LL << 46))
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    MXFP4_TRY(check_ptr(ws));
+    if (ws_bytes < mxk::moe_workspace_bytes(n_experts, n_tokens, top_k, hidden, inter))
+        return MXFP4_STATUS_WORKSPACE_TOO_SMALL;
+    return MXFP4_STATUS_OK;
+}
+
+}  // namespace
+
+int mxfp4_moe_gate_up(const void* gate_bank, const void* up_bank, int n_experts, int hidden,
+                      int inter, const float* x, int n_tokens, int top_k,
+                      const int32_t* expert_ids, float* act, void* workspace, size_t ws_bytes,
+                      cudaStream_t stream) {
+    MXFP4_TRY(check_moe(n_experts, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
+    MXFP4_TRY(check_ptr(gate_bank));
+    MXFP4_TRY(check_ptr(up_bank));
+    MXFP4_TRY(check_ptr(x));
+    MXFP4_TRY(check_ptr(act));
+    if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
+        return MXFP4_STATUS_BAD_POINTER;
+    return from_cuda(mxk::launch_moe_gate_up(u8(gate_bank), u8(up_bank), n_experts, hidden, inter,
+                                             x, n_tokens, top_k, expert_ids, act, workspace,
+                                             stream));
+}
+
+int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter, const float* act,
+                   int n_tokens, int top_k, const int32_t* expert_ids, const float* route_w,
+                   float* y, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_moe(n_experts, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
+    MXFP4_TRY(check_ptr(down_bank));
+    MXFP4_TRY(check_ptr(act));
+    MXFP4_TRY(check_ptr(y));
+    if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u) ||
+        route_w == nullptr || (reinterpret_cast<uintptr_t>(route_w) & 3u))
+        return MXFP4_STATUS_BAD_POINTER;
+    return from_cuda(mxk::launch_moe_down(u8(down_bank), n_experts, hidden, inter, act, n_tokens,
+                                          top_k, expert_ids, route_w, y, workspace, stream));
+}
+
+int mxfp4_moe_plan_errors(const void* workspace, size_t ws_bytes, int* n_invalid,
+                          cudaStream_t stream) {
+    if (workspace == nullptr || n_invalid == nullptr || !aligned16(workspace))
+        return MXFP4_STATUS_BAD_POINTER;
+    if (ws_bytes < 16) return MXFP4_STATUS_WORKSPACE_TOO_SMALL;
+    return from_cuda(mxk::moe_plan_errors(workspace, n_invalid, stream));
+}
+
+}  // extern "C"
