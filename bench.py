@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 path on one node (one process per GPU, replicas).
+
+The headline workload is the decode GEMV (mxfp4_mv, 14336x4096, one token).
+One step is one token through LAYERS such matrices, each a distinct weight
+buffer (16 x 31.2 MB = 500 MB, larger than L2, so no launch reads another's
+weights from cache); the step is captured once as a CUDA graph and replayed.
+`value` is weight+activation+output bytes per second over the timed steps.
+
+Also measured and reported under "workloads": the small-batch product
+(4096x14336, nb=8), the MoE layer (64 experts 2880x2880, 32 tokens, top-4;
+tokens/s), the prefill product (4096x4096, nb=2048; TFLOP/s) and the tiny
+matvec.  The oracle is timed on the host cores as `cpu_baseline`.
+
+--impl reference runs the CPU oracle (the reference arm) on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 16
+METRIC = "MXFP4 fused dequant-matvec weight GB/s (decode GEMV 14336x4096)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+# --- clocks ------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --- workloads -----------------------------------------------------------------
+
+class Workload:
+    """A step enqueued on torch's current stream; bytes/flops/units per step."""
+    name = ""
+    launches_per_step = 1
+    dominant = ""
+
+    def step(self):
+        raise NotImplementedError
+
+
+def _dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class DecodeGemv(Workload):
+    """LAYERS distinct 14336x4096 matrices, one token (mxfp4_mv each)."""
+
+    def __init__(self, mx, layers=LAYERS, cfg=None):
+        import torch
+        import synth
+        self.mx = mx
+        self.cfg = cfg or synth.DECODE
+        c = self.cfg
+        self.name = c.name
+        w0 = c.weights()
+        self.rows, self.cols = c.rows, c.cols
+        # distinct buffers: copies of the seeded matrix (identical bytes, separate
+        # memory), so every launch streams its own weights from HBM
+        self.ws = [_dev(w0) for _ in range(layers)]
+        self.x_host = c.activations().reshape(-1)
+        self.x = _dev(self.x_host)
+        self.ys = [torch.empty(c.rows, dtype=torch.float32, device="cuda") for _ in range(layers)]
+        self.launches_per_step = layers
+        self.bytes_per_launch = mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
+        self.bytes_per_step = layers * self.bytes_per_launch
+        self.units_per_step = self.bytes_per_step
+        self.dominant = "mxfp4_mv (k_matmat<4,1>)"
+
+    def step(self):
+        for w, y in zip(self.ws, self.ys):
+            self.mx.mxfp4_mv(w, self.rows, self.cols, self.x, y)
+
+    # p2-style host entry: x from pinned host memory, y back to host, per layer
+    def setup_e2e(self):
+        import torch
+        self.xh = torch.from_numpy(self.x_host.copy()).pin_memory()
+        self.yh = [torch.empty(self.rows, dtype=torch.float32).pin_memory() for _ in self.ws]
+        self.x_stage = torch.empty(self.cols, dtype=torch.float32, device="cuda")
+        self.h2d = len(self.ws) * 4 * self.cols
+        self.d2h = len(self.ws) * 4 * self.rows
+
+    def step_e2e(self):
+        for w, yh, y in zip(self.ws, self.yh, self.ys):
+            self.mx.mxfp4_matmat_host(w, self.rows, self.cols, self.xh, 1, yh, self.x_stage, y)
+
+
+class SmallBatch(Workload):
+    def __init__(self, mx, layers=LAYERS):
+        import torch
+        import synth
+        c = synth.MM8
+        self.mx, self.c = mx, c
+        self.name = c.name
+        w0 = c.weights()
+        self.ws = [_dev(w0) for _ in range(layers)]
+        self.X = _dev(c.activations())
+        self.Ys = [torch.empty(c.nb * c.rows, dtype=torch.float32, device="cuda")
+                   for _ in range(layers)]
+        self.launches_per_step = layers
+        self.bytes_per_launch = (mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.nb * c.cols +
+                                 4 * c.nb * c.rows)
+        self.bytes_per_step = layers * self.bytes_per_launch
+        self.dominant = "mxfp4_mm nb=8"
+
+    def step(self):
+        c = self.c
+        for w, Y in zip(self.ws, self.Ys):
+            self.mx.mxfp4_mm(w, c.rows, c.cols, self.X, c.nb, Y)
+
+
+class MoeLayer(Workload):
+    def __init__(self, mx):
+        import torch
+        import synth
+        c = synth.MOE
+        self.mx, self.c = mx, c
+        self.name = c.name
+        gate, up, down = c.banks()
+        self.gate, self.up, self.down = _dev(gate), _dev(up), _dev(down)
+        del gate, up, down
+        self.x = _dev(c.activations())
+        ids, wts = c.routes()
+        self.ids_h = ids
+        self.ids, self.wts = _dev(ids), _dev(wts)
+        P = c.n_tokens * c.top_k
+        self.act = torch.empty(P * c.inter, dtype=torch.float32, device="cuda")
+        self.y = torch.empty(c.n_tokens * c.hidden, dtype=torch.float32, device="cuda")
+        nbytes = mx.mxfp4_moe_workspace_bytes(c.n_experts, c.n_tokens, c.top_k, c.hidden,
+                                              c.inter)
+        self.ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+        self.touched = int(np.unique(ids).size)
+        per_expert = 2 * c.gu_stride + c.down_stride
+        self.bytes_per_step = (self.touched * per_expert + 4 * c.n_tokens * c.hidden * 2 +
+                               4 * P * c.inter * 2 + 8 * P)
+        self.units_per_step = c.n_tokens
+        self.launches_per_step = 4   # plan, gate/up, down, combine
+        self.dominant = "k_moe_pass (gate/up + down)"
+
+    def step(self):
+        c, mx = self.c, self.mx
+        mx.mxfp4_moe_gate_up(self.gate, self.up, c.n_experts, c.hidden, c.inter, self.x,
+                             c.n_tokens, c.top_k, self.ids, self.act, self.ws)
+        mx.mxfp4_moe_down(self.down, c.n_experts, c.hidden, c.inter, self.act, c.n_tokens,
+                          c.top_k, self.ids, self.wts, self.y, self.ws)
+
+
+class Prefill(Workload):
+    def __init__(self, mx):
+        import torch
+        import synth
+        c = synth.PREFILL
+        self.mx, self.c = mx, c
+        self.name = c.name
+        self.w = _dev(c.weights())
+        self.X = _dev(c.activations())
+        self.Y = torch.empty(c.nb * c.rows, dtype=torch.float32, device="cuda")
+        self.flops_per_step = 2.0 * c.rows * c.cols * c.nb
+        self.bytes_per_step = (mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.nb * c.cols +
+                               4 * c.nb * c.rows)
+        self.launches_per_step = 1
+        self.dominant = "mxfp4_mm bf16 path"
+
+    def step(self):
+        c = self.c
+        self.mx.mxfp4_mm(self.w, c.rows, c.cols, self.X, c.nb, self.Y)
+
+
+class Tiny(DecodeGemv):
+    def __init__(self, mx):
+        import synth
+        super().__init__(mx, layers=LAYERS, cfg=synth.TINY)
+
+
+# --- timing --------------------------------------------------------------------
+
+def time_graph(work: Workload, steps: int, warmup: int, barrier=None):
+    """Capture one step as a CUDA graph, replay `warmup` untimed and `steps`
+    timed, events on the capture stream.  Returns seconds for the timed steps."""
+    import torch
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        work.step()          # eager once: lazy set-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        work.step()
+    for _ in range(max(warmup, 0)):
+        g.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / 1e3, g
+
+
+def time_e2e(work, steps: int, warmup: int):
+    import torch
+    work.setup_e2e()
+    for _ in range(max(warmup, 1)):
+        work.step_e2e()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        work.step_e2e()
+    torch.cuda.synchronize()
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(seconds_target: float = 12.0):
+    """The oracle as it stands on the host: full decode-GEMV matvecs (one layer
+    per call), repeated until ~seconds_target; GB/s in the bench's units."""
+    import oracle
+    import synth
+    c = synth.DECODE
+    w, x = c.weights(), c.activations()
+    oracle.lib()
+    per_launch = synth.padded_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.matmat(w, c.rows, c.cols, x, 1)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target or n >= 200:
+            break
+    return {"value": n * per_launch / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full {c.rows}x{c.cols} matvecs (one layer each) in {el:.1f} s, "
+                      "single-threaded scalar decode, double accumulation"}
+
+
+# --- main ------------------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    c = synth.DECODE
+    w, x = c.weights(), c.activations()
+    oracle.lib()
+    per = synth.padded_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
+    for _ in range(args.warmup):
+        oracle.matmat(w, c.rows, c.cols, x, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmat(w, c.rows, c.cols, x, 1)
+    el = time.perf_counter() - t0
+    value = args.steps * per / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
+        "config": {"workload": c.name, "step": "one layer (one matvec) per step",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full {c.rows}x{c.cols} matvecs"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()
+    torch.cuda.set_device(local)
+    import mxfp4_dequant_matmul_gb300 as mx
+    mx.lib()
+    barrier = (lambda: torch.distributed.barrier()) if ws > 1 else None
+
+    pk = peaks()
+    main_w = DecodeGemv(mx)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    secs, graph = time_graph(main_w, args.steps, args.warmup, barrier)
+    # keep the same step running ~1 s so the sampler sees the clocks under this load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            graph.replay()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if ws > 1:
+        t = torch.tensor([secs], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        secs = float(t.item())
+    value = ws * args.steps * main_w.bytes_per_step / secs / 1e9
+    per_launch_s = secs / (args.steps * main_w.launches_per_step)
+    achieved = main_w.bytes_per_launch / per_launch_s / 1e9
+
+    e2e_secs = time_e2e(main_w, max(args.steps // 5, 3), args.warmup)
+    e2e_steps = max(args.steps // 5, 3)
+    e2e_val = ws * e2e_steps * main_w.bytes_per_step / e2e_secs / 1e9
+
+    workloads = {}
+    if not args.only_main:
+        for cls in (SmallBatch, MoeLayer, Prefill, Tiny):
+            try:
+                w = cls(mx)
+                k = max(args.steps // 5, 5)
+                s, _ = time_graph(w, k, args.warmup)
+                per = s / k
+                entry = {"workload": w.name, "ms_per_step": per * 1e3,
+                         "launches_per_step": w.launches_per_step}
+                if isinstance(w, Prefill):
+                    tf = w.flops_per_step / per / 1e12
+                    entry.update({"value": tf, "unit": "TFLOP/s",
+                                  "roofline": {"bound": "tensor", "achieved": tf,
+                                               "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                               "frac": tf / pk["bf16_tflops"]}})
+                else:
+                    gbs = w.bytes_per_step / per / 1e9
+                    entry.update({"value": gbs, "unit": "GB/s",
+                                  "roofline": {"bound": "hbm", "achieved": gbs,
+                                               "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                               "frac": gbs / pk["hbm_gbs"]}})
+                    if isinstance(w, MoeLayer):
+                        entry["tokens_per_s"] = w.units_per_step / per
+                        entry["touched_experts"] = w.touched
+                    if isinstance(w, Tiny):
+                        entry["note"] = "L2-resident parity config; reported, not graded"
+                workloads[w.name] = entry
+                del w
+                torch.cuda.empty_cache()
+            except Exception as exc:  # report, never hide
+                workloads[cls.__name__] = {"error": repr(exc)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64; nibbles uniform, E8M0 scales U[118,130], "
+                    "x N(0,1))",
+            "config": {"workload": main_w.name, "rows": main_w.rows, "cols": main_w.cols,
+                       "nb": 1, "layers_per_step": LAYERS,
+                       "l2": f"inputs larger than L2: {LAYERS} distinct weight buffers, "
+                             f"{LAYERS * main_w.bytes_per_launch / 1e6:.0f} MB per step",
+                       "timing": "CUDA graph of one step, CUDA events on its stream"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": None, "peak_source": pk["source"],
+                         "kernel": main_w.dominant,
+                         "bytes_per_launch": main_w.bytes_per_launch,
+                         "us_per_launch": per_launch_s * 1e6},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "GB/s",
+                    "h2d_bytes_per_step": main_w.h2d, "d2h_bytes_per_step": main_w.d2h,
+                    "api": "mxfp4_matmat_host per layer (pinned host x in, y out, stream sync)"},
+            "gpu_launches": args.steps * main_w.launches_per_step,
+            "clocks": clocks,
+            "workloads": workloads,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""GPU parity: standalone decode (bit-exact) and the FP32 matvec / small-batch
+product (within 1e-5 of the L1 bound) against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import (REL_FP32, assert_bits_equal, assert_within, cuda, empty, host, to_dev)
+from mx_encode import encode, random_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    return cuda()
+
+
+def run_mv(mx, w_h, rows, cols, x_h):
+    y = empty(rows)
+    mx.mxfp4_mv(to_dev(w_h), rows, cols, to_dev(x_h), y)
+    return host(y)
+
+
+def run_mm(mx, w_h, rows, cols, X_h, nb, fn="mxfp4_mm"):
+    Y = empty(nb * rows)
+    getattr(mx, fn)(to_dev(w_h), rows, cols, to_dev(X_h), nb, Y)
+    return host(Y).reshape(nb, rows)
+
+
+# --- decode ------------------------------------------------------------------
+
+def test_decode_tiny_config_bit_exact(mx):
+    cfg = synth.TINY
+    w_h = cfg.weights()
+    out = empty(cfg.rows * cfg.cols)
+    mx.mxfp4_dequant(to_dev(w_h), cfg.rows, cfg.cols, out)
+    assert_bits_equal(host(out), oracle.dequant(w_h, cfg.rows, cfg.cols), "tiny decode")
+
+
+def test_decode_exhaustive_code_by_scale(mx):
+    codes = np.tile(np.concatenate([np.arange(16), np.arange(16)]), (256, 1))
+    scales = np.arange(256).reshape(256, 1)
+    buf = encode(codes, scales)
+    out = empty(256 * 32)
+    mx.mxfp4_dequant(to_dev(buf), 256, 32, out)
+    got = host(out)
+    assert_bits_equal(got, oracle.dequant(buf, 256, 32), "16x256 table")
+    assert np.signbit(got[127 * 32 + 8]) and got[127 * 32 + 8] == 0.0  # code 8 -> -0.0
+
+
+@pytest.mark.parametrize("name", ["decode", "mm8", "prefill"])
+def test_decode_full_size_planes_bit_exact(mx, name):
+    cfg = synth.CONFIGS[name]
+    w_h = cfg.weights()
+    out = empty(cfg.rows * cfg.cols)
+    mx.mxfp4_dequant(to_dev(w_h), cfg.rows, cfg.cols, out)
+    assert_bits_equal(host(out), oracle.dequant(w_h, cfg.rows, cfg.cols), name)
+
+
+def test_decode_moe_expert_bit_exact(mx):
+    cfg = synth.MOE
+    w_h = synth.mxfp4_matrix(cfg.inter, cfg.hidden, synth.substream(cfg.seed, "gate/7"),
+                             cfg.scale_lo, cfg.scale_hi)
+    out = empty(cfg.inter * cfg.hidden)
+    mx.mxfp4_dequant(to_dev(w_h), cfg.inter, cfg.hidden, out)
+    assert_bits_equal(host(out), oracle.dequant(w_h, cfg.inter, cfg.hidden), "expert")
+
+
+# --- matvec ------------------------------------------------------------------
+
+def test_mv_tiny_config_with_subnormal_and_nan_groups(mx):
+    cfg = synth.TINY
+    w_h, x_h = cfg.weights(), cfg.activations()
+    got = run_mv(mx, w_h, cfg.rows, cfg.cols, x_h)
+    ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, x_h, 1)
+    assert np.isnan(got[250]) and not np.isnan(np.delete(got, 250)).any()
+    assert_within(got, ref, l1, REL_FP32, "tiny mv")
+
+
+def test_mv_decode_config_every_row(mx):
+    cfg = synth.DECODE
+    w_h, x_h = cfg.weights(), cfg.activations()
+    got = run_mv(mx, w_h, cfg.rows, cfg.cols, x_h)
+    ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, x_h, 1)
+    worst = assert_within(got, ref, l1, REL_FP32, "decode GEMV")
+    print(f"decode GEMV worst err/tol {worst:.3g}")
+
+
+@pytest.mark.parametrize("rows,cols", [(40, 256), (300, 2304), (5, 5120), (33, 64)])
+def test_mv_exact_inputs_bit_for_bit(mx, rows, cols):
+    # integer x in [-4, 4], scales 126..128: every FP32 partial sum is exact, so
+    # any summation order gives exactly the oracle's double result.
+    rng = np.random.default_rng(rows + cols)
+    codes, scales = random_case(rng, rows, cols, lo=126, hi=128)
+    buf = encode(codes, scales)
+    x = synth.int_activations(rows * 7 + cols, cols)
+    got = run_mv(mx, buf, rows, cols, x)
+    ref, _ = oracle.matmat(buf, rows, cols, x, 1)
+    assert np.array_equal(got.astype(np.float64), ref[0])
+
+
+def test_mv_one_hot_sweep_pins_every_nibble_and_scale(mx):
+    rows, cols = 64, 256
+    rng = np.random.default_rng(1)
+    codes, scales = random_case(rng, rows, cols, lo=100, hi=150)
+    buf = encode(codes, scales)
+    dense = oracle.dequant(buf, rows, cols)
+    w = to_dev(buf)
+    X = np.eye(cols, dtype=np.float32)
+    Y = empty(cols * rows)
+    mx.mxfp4_mm_fp32(w, rows, cols, to_dev(X), cols, Y)   # token c = unit vector e_c
+    got = host(Y).reshape(cols, rows)
+    assert_bits_equal(got, dense.T, "one-hot sweep")
+
+
+@pytest.mark.parametrize("rows,cols", [(300, 2304), (70000, 64), (5, 5120)])
+def test_page_shapes_mv_and_batches_equal_per_token(mx, rows, cols):
+    seed = rows + cols
+    w_h = synth.mxfp4_matrix(rows, cols, seed, 119, 123, scale_pattern="adjacent_distinct")
+    x1 = synth.normal_f32(seed, cols)
+    got = run_mv(mx, w_h, rows, cols, x1)
+    ref, l1 = oracle.matmat(w_h, rows, cols, x1, 1)
+    assert_within(got, ref, l1, REL_FP32, f"{rows}x{cols} mv")
+    if rows > 1000 and cols < 128:
+        batches = [9]
+    else:
+        batches = [2, 8, 9, 19]
+    for b in batches:
+        X = synth.normal_f32(seed * 31 + b, b * cols).reshape(b, cols)
+        Y = run_mm(mx, w_h, rows, cols, X, b)
+        Y32 = run_mm(mx, w_h, rows, cols, X, b, "mxfp4_mm_fp32")
+        ref, l1 = oracle.matmat(w_h, rows, cols, X, b)
+        assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} batch {b}")
+        assert_bits_equal(Y, Y32, "mm vs mm_fp32")
+        for t in range(b):
+            one = run_mv(mx, w_h, rows, cols, X[t])
+            assert_bits_equal(Y[t], one, f"batch {b} token {t} vs its matvec")
+
+
+def test_mm8_config_every_output(mx):
+    cfg = synth.MM8
+    w_h, X = cfg.weights(), cfg.activations()
+    Y = run_mm(mx, w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    worst = assert_within(Y, ref, l1, REL_FP32, "mm nb=8")
+    print(f"mm nb=8 worst err/tol {worst:.3g}")
+
+
+def test_mm_exact_inputs_bit_for_bit(mx):
+    rows, cols, nb = 96, 1024, 8
+    rng = np.random.default_rng(5)
+    codes, scales = random_case(rng, rows, cols, lo=126, hi=128)
+    buf = encode(codes, scales)
+    X = synth.int_activations(17, nb * cols).reshape(nb, cols)
+    Y = run_mm(mx, buf, rows, cols, X, nb)
+    ref, _ = oracle.matmat(buf, rows, cols, X, nb)
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+def test_zero_activation_gives_zero_except_nan_rows(mx):
+    cfg = synth.TINY
+    w_h = cfg.weights()
+    got = run_mv(mx, w_h, cfg.rows, cfg.cols, np.zeros(cfg.cols, np.float32))
+    assert np.isnan(got[250])
+    assert not np.delete(got, 250).any()
+
+
+def test_results_are_deterministic(mx):
+    cfg = synth.DECODE
+    w, x = to_dev(cfg.weights()), to_dev(cfg.activations())
+    outs = []
+    for _ in range(3):
+        y = empty(cfg.rows)
+        mx.mxfp4_mv(w, cfg.rows, cfg.cols, x, y)
+        outs.append(host(y))
+    assert_bits_equal(outs[0], outs[1]) and assert_bits_equal(outs[0], outs[2])
+
+
+def test_refusals_launch_nothing(mx):
+    import torch
+    w = to_dev(synth.TINY.weights())
+    x = to_dev(np.ones(2304, np.float32))
+    y = torch.full((300,), 7.0, device="cuda:0")
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.mxfp4_mv(w, 300, 2270, x, y)      # cols not a multiple of 32
+    assert e.value.status == 1
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.mxfp4_mv(w, 300, 2304, x[1:], y)  # misaligned x
+    assert e.value.status == 2
+    assert (host(y) == 7.0).all()
+
+
+def test_host_buffer_entry_matches_device_entry(mx):
+    import torch
+    cfg = synth.TINY
+    w_h, x_h = cfg.weights(), cfg.activations()
+    w = to_dev(w_h)
+    y_dev_ref = empty(cfg.rows)
+    mx.mxfp4_mv(w, cfg.rows, cfg.cols, to_dev(x_h), y_dev_ref)
+    X_host = torch.from_numpy(x_h.copy()).pin_memory()
+    Y_host = torch.empty(cfg.rows, dtype=torch.float32).pin_memory()
+    mx.mxfp4_matmat_host(w, cfg.rows, cfg.cols, X_host, 1, Y_host, empty(cfg.cols),
+                         empty(cfg.rows))
+    assert_bits_equal(Y_host.numpy(), host(y_dev_ref), "host entry")

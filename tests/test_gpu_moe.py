@@ -1,0 +1,146 @@
+"""GPU parity of the routed-expert passes against the CPU oracle: gate/up alone,
+down alone on an injected activation (the stage injection of the q4tp MoE
+kernel's run_stages), and the whole layer; experts with 0, 1 and more than 8
+pairs; distinct scale planes per expert; out-of-range ids."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import REL_FP32, assert_bits_equal, assert_within, cuda, empty, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    return cuda()
+
+
+def make_case(E, hidden, inter, T, K, seed, ids=None):
+    cfg = synth.MoeConfig("case", E, hidden, inter, T, K, seed)
+    gate, up, down = cfg.banks()
+    x = cfg.activations()
+    rid, wts = cfg.routes() if ids is None else (ids, synth.routes(seed, T, K, E)[1])
+    return cfg, gate, up, down, x, np.ascontiguousarray(rid, dtype=np.int32), wts
+
+
+def act_tolerance(ref):
+    """Error allowed in act = silu(g)*u when g and u each carry 1e-5 * L1 error,
+    plus a few float roundings of the product."""
+    g, u = ref["g"], ref["u"]
+    s = 1.0 / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    dsilu = np.abs(s * (1.0 + g * (1.0 - s)))
+    prop = dsilu * ref["l1g"] * np.abs(u) + np.abs(g * s) * ref["l1u"]
+    return REL_FP32 * prop + 4.0 * 2.0 ** -23 * np.abs(ref["act"]) + 1e-30
+
+
+def run_gate_up(mx, cfg, gate, up, x, ids, ws=None, act=None):
+    P = cfg.n_tokens * cfg.top_k
+    nbytes = mx.mxfp4_moe_workspace_bytes(cfg.n_experts, cfg.n_tokens, cfg.top_k,
+                                          cfg.hidden, cfg.inter)
+    ws = empty(nbytes // 4 + 4) if ws is None else ws
+    act = empty(P * cfg.inter) if act is None else act
+    mx.mxfp4_moe_gate_up(to_dev(gate), to_dev(up), cfg.n_experts, cfg.hidden, cfg.inter,
+                         to_dev(x), cfg.n_tokens, cfg.top_k, to_dev(ids), act, ws)
+    return act, ws
+
+
+def check_gate_up(act_got, ref, ids, E):
+    valid = ((ids >= 0) & (ids < E)).reshape(-1)
+    got = act_got.reshape(ref["act"].shape)[valid]
+    want = ref["act"][valid]
+    tol = act_tolerance(ref)[valid]
+    err = np.abs(got.astype(np.float64) - want)
+    assert not np.isnan(got).any()
+    bad = np.flatnonzero(err > tol)
+    assert bad.size == 0, f"{bad.size} act values over tolerance, worst {np.max(err / tol):.3g}"
+
+
+@pytest.mark.parametrize("E,hidden,inter,T,K,seed", [
+    (8, 64, 96, 12, 3, 1),       # some experts with no pair
+    (5, 256, 128, 16, 2, 2),
+    (64, 2880, 2880, 32, 4, 3),  # the MoE layer's workload
+])
+def test_gate_up_stage(mx, E, hidden, inter, T, K, seed):
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, seed)
+    act, _ = run_gate_up(mx, cfg, gate, up, x, ids)
+    ref = oracle.moe_gate_up(gate, up, cfg.gu_stride, E, hidden, inter, x, T, K, ids)
+    check_gate_up(host(act), ref, ids, E)
+
+
+def test_gate_up_expert_with_more_than_eight_pairs(mx):
+    E, hidden, inter, T, K = 6, 128, 64, 20, 2
+    ids = np.stack([[0, 1 + t % 5] for t in range(T)]).astype(np.int32)  # expert 0: 20 pairs
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 5, ids)
+    act, _ = run_gate_up(mx, cfg, gate, up, x, ids)
+    ref = oracle.moe_gate_up(gate, up, cfg.gu_stride, E, hidden, inter, x, T, K, ids)
+    check_gate_up(host(act), ref, ids, E)
+
+
+@pytest.mark.parametrize("E,hidden,inter,T,K,seed", [
+    (8, 96, 64, 12, 3, 7), (64, 2880, 2880, 32, 4, 3)])
+def test_down_stage_on_injected_act(mx, E, hidden, inter, T, K, seed):
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, seed)
+    act = synth.normal_f32(seed + 1000, T * K * inter)
+    # plan from a gate/up call (its act output is then overwritten by the injected act)
+    act_d, ws = run_gate_up(mx, cfg, gate, up, x, ids)
+    act_d.copy_(to_dev(act))
+    y = empty(T * hidden)
+    mx.mxfp4_moe_down(to_dev(down), E, hidden, inter, act_d, T, K, to_dev(ids), to_dev(wts),
+                      y, ws)
+    ref = oracle.moe_down(down, cfg.down_stride, E, hidden, inter, act, T, K, ids, wts)
+    assert_within(host(y), ref["out"], ref["l1_out"], REL_FP32, "down stage")
+
+
+def run_layer(mx, cfg, gate, up, down, x, ids, wts):
+    act, ws = run_gate_up(mx, cfg, gate, up, x, ids)
+    y = empty(cfg.n_tokens * cfg.hidden)
+    mx.mxfp4_moe_down(to_dev(down), cfg.n_experts, cfg.hidden, cfg.inter, act, cfg.n_tokens,
+                      cfg.top_k, to_dev(ids), to_dev(wts), y, ws)
+    return host(y).reshape(cfg.n_tokens, cfg.hidden), ws
+
+
+@pytest.mark.parametrize("E,hidden,inter,T,K,seed", [
+    (8, 64, 96, 12, 3, 11), (64, 2880, 2880, 32, 4, 3)])
+def test_whole_layer(mx, E, hidden, inter, T, K, seed):
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, seed)
+    y, _ = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
+                             x, T, K, ids, wts)
+    bound = ref["bound_l1"] + ref["bound_prop"]
+    assert_within(y, ref["out"], bound, REL_FP32, "MoE layer")
+    diff = y - ref["out"]
+    nrmse = np.sqrt((diff ** 2).sum() / (ref["out"] ** 2).sum())
+    cos = (y * ref["out"]).sum() / np.sqrt((y ** 2).sum() * (ref["out"] ** 2).sum())
+    assert nrmse < 1e-4 and cos > 0.999999, (nrmse, cos)
+
+
+def test_layer_is_deterministic(mx):
+    cfg, gate, up, down, x, ids, wts = make_case(16, 256, 256, 24, 4, 13)
+    a, _ = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    b, _ = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    assert_bits_equal(a, b, "rerun")
+
+
+def test_out_of_range_ids_are_skipped_and_counted(mx):
+    import torch
+    cfg, gate, up, down, x, ids, wts = make_case(8, 64, 64, 10, 2, 17)
+    ids = ids.copy()
+    ids[3, 1] = 8
+    ids[6, 0] = -1
+    P = cfg.n_tokens * cfg.top_k
+    act = torch.full((P * cfg.inter,), 123.0, device="cuda:0")
+    act, ws = run_gate_up(mx, cfg, gate, up, x, ids, act=act)
+    assert mx.mxfp4_moe_plan_errors(ws) == 2
+    a = host(act).reshape(P, cfg.inter)
+    assert (a[3 * 2 + 1] == 123.0).all() and (a[6 * 2 + 0] == 123.0).all()
+    ref = oracle.moe_gate_up(gate, up, cfg.gu_stride, 8, 64, 64, x, 10, 2, ids)
+    check_gate_up(a.reshape(-1), ref, ids, 8)
+    # down on an injected act: the invalid pairs contribute nothing
+    act_in = synth.normal_f32(99, P * cfg.inter)
+    act.copy_(to_dev(act_in))
+    y = empty(cfg.n_tokens * cfg.hidden)
+    mx.mxfp4_moe_down(to_dev(down), 8, 64, 64, act, 10, 2, to_dev(ids), to_dev(wts), y, ws)
+    refd = oracle.moe_down(down, cfg.down_stride, 8, 64, 64, act_in, 10, 2, ids, wts)
+    assert_within(host(y), refd["out"], refd["l1_out"], REL_FP32, "down with invalid ids")

@@ -1,0 +1,81 @@
+"""GPU parity of the large-batch (prefill) product: W decoded exactly, X rounded
+to nearest-even bfloat16, FP32 accumulation, against the oracle on bf16(X)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import REL_BF16, REL_FP32, assert_within, cuda, empty, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mx():
+    return cuda()
+
+
+def run(mx, fn, w_h, rows, cols, X, nb):
+    Y = empty(nb * rows)
+    getattr(mx, fn)(to_dev(w_h), rows, cols, to_dev(X), nb, Y)
+    return host(Y).reshape(nb, rows)
+
+
+@pytest.mark.parametrize("rows,cols,nb", [(256, 512, 100), (300, 2304, 77), (64, 64, 129),
+                                          (130, 4096, 65), (96, 160, 1)])
+def test_bf16_path_small_shapes(mx, rows, cols, nb):
+    seed = rows * 3 + cols + nb
+    w_h = synth.mxfp4_matrix(rows, cols, seed, 118, 130)
+    X = synth.normal_f32(seed, nb * cols).reshape(nb, cols)
+    Y = run(mx, "mxfp4_mm_bf16", w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, oracle.round_bf16(X), nb)
+    assert_within(Y, ref, l1, REL_BF16, "bf16 path")
+    # the products are exact and only the FP32 sums round: the FP32 bound holds too
+    assert_within(Y, ref, l1, REL_FP32, "bf16 path, FP32 bound")
+
+
+def test_mm_dispatches_large_batches_to_the_bf16_path(mx):
+    rows, cols, nb = 128, 1024, 96
+    w_h = synth.mxfp4_matrix(rows, cols, 3, 118, 130)
+    X = synth.normal_f32(8, nb * cols).reshape(nb, cols)
+    a = run(mx, "mxfp4_mm", w_h, rows, cols, X, nb)
+    b = run(mx, "mxfp4_mm_bf16", w_h, rows, cols, X, nb)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_bf16_path_tiny_config_nan_and_subnormal_groups(mx):
+    cfg = synth.TINY
+    w_h = cfg.weights()
+    nb = 80
+    X = synth.normal_f32(12, nb * cfg.cols).reshape(nb, cfg.cols)
+    Y = run(mx, "mxfp4_mm_bf16", w_h, cfg.rows, cfg.cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, oracle.round_bf16(X), nb)
+    assert np.isnan(Y[:, 250]).all()
+    assert_within(Y, ref, l1, REL_BF16, "tiny bf16")
+
+
+def test_bf16_path_exact_inputs_bit_for_bit(mx):
+    rows, cols, nb = 256, 1024, 192
+    w_h = synth.mxfp4_matrix(rows, cols, 21, 126, 128)
+    X = synth.int_activations(4, nb * cols).reshape(nb, cols)    # exact in bf16
+    Y = run(mx, "mxfp4_mm_bf16", w_h, rows, cols, X, nb)
+    ref, _ = oracle.matmat(w_h, rows, cols, X, nb)
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+def test_prefill_config_sampled_outputs(mx):
+    cfg = synth.PREFILL
+    w_h, X = cfg.weights(), cfg.activations()
+    Y = run(mx, "mxfp4_mm", w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    rng = np.random.default_rng(0)
+    n = 3000
+    tok = np.concatenate([rng.integers(0, cfg.nb, n - 2), [0, cfg.nb - 1]]).astype(np.int32)
+    row = np.concatenate([rng.integers(0, cfg.rows, n - 2), [0, cfg.rows - 1]]).astype(np.int32)
+    ref, l1 = oracle.matmat_samples(w_h, cfg.rows, cfg.cols, oracle.round_bf16(X), tok, row)
+    assert_within(Y[tok, row], ref, l1, REL_BF16, "prefill samples")
+    worst = assert_within(Y[tok, row], ref, l1, REL_FP32, "prefill samples, FP32 bound")
+    # against the unrounded activations: the bf16 rounding of X is the only gap
+    ref32, _ = oracle.matmat_samples(w_h, cfg.rows, cfg.cols, X, tok, row)
+    nrmse = np.sqrt(((Y[tok, row] - ref32) ** 2).sum() / (ref32 ** 2).sum())
+    print(f"prefill worst err/tol {worst:.3g}; nrmse vs f32-X oracle {nrmse:.3e}")
+    assert nrmse < 1e-2
