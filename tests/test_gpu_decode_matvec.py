@@ -111,7 +111,9 @@ def test_mv_one_hot_sweep_pins_every_nibble_and_scale(mx):
     Y = empty(cols * rows)
     mx.mxfp4_mm_fp32(w, rows, cols, to_dev(X), cols, Y)   # token c = unit vector e_c
     got = host(Y).reshape(cols, rows)
-    assert_bits_equal(got, dense.T, "one-hot sweep")
+    # one non-zero product per output: exact, but a sum that starts at +0
+    # returns +0 for a -0 weight (code 8), so compare values, not sign bits
+    assert np.array_equal(got, dense.T), "one-hot sweep"
 
 
 @pytest.mark.parametrize("rows,cols", [(300, 2304), (70000, 64), (5, 5120)])
