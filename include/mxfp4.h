@@ -65,6 +65,13 @@ const char* mxfp4_status_string(int status);
 /* cudaError_t recorded by the last MXFP4_STATUS_LAUNCH_FAILED on this thread. */
 int mxfp4_last_cuda_error(void);
 
+/* Reads the library's device fault word into *faults (0 = none) and clears it
+ * if `reset` is non-zero.  A kernel that waits on its own asynchronous copies
+ * gives up after a bounded number of polls instead of hanging the GPU; it then
+ * sets this word and returns early, leaving its outputs incomplete.
+ * Synchronises the current device. */
+int mxfp4_device_faults(int* faults, int reset);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int mxfp4_version(void);
 

@@ -59,6 +59,52 @@ __device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
     }
 }
 
+// Group dot products: for each of R rows (its 16 code bytes in code[i]) and
+// each of NB tokens (32 floats of x at xp[t], 16-byte aligned) the sum of the
+// 32 decoded codes times x, in FP32: two FMA chains, one over the even and one
+// over the odd elements (one packed pair FMA feeds both), then even + odd.
+// Every token sees exactly this sequence whatever R and NB are, which is what
+// makes the batched product equal the matvec bit for bit.
+template <int R, int NB>
+__device__ __forceinline__ void group_dots(const uint4 (&code)[R], const float* const (&xp)[NB],
+                                           float (&out)[R][NB]) {
+    float2 d[R][NB];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int t = 0; t < NB; ++t) d[i][t] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 xv[NB][4];
+#pragma unroll
+        for (int t = 0; t < NB; ++t) {
+            const float4 xa = *reinterpret_cast<const float4*>(xp[t] + 8 * k);
+            const float4 xb = *reinterpret_cast<const float4*>(xp[t] + 8 * k + 4);
+            xv[t][0] = make_float2(xa.x, xa.y);
+            xv[t][1] = make_float2(xa.z, xa.w);
+            xv[t][2] = make_float2(xb.x, xb.y);
+            xv[t][3] = make_float2(xb.z, xb.w);
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const uint32_t word = k == 0 ? code[i].x : k == 1 ? code[i].y : k == 2 ? code[i].z
+                                                                                 : code[i].w;
+            uint32_t h[4];
+            e2m1x8_to_f16x2x4(word, h);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float2 v = f16x2_to_f32x2(h[b]);
+#pragma unroll
+                for (int t = 0; t < NB; ++t) d[i][t] = __ffma2_rn(v, xv[t][b], d[i][t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int t = 0; t < NB; ++t) out[i][t] = __fadd_rn(d[i][t].x, d[i][t].y);
+}
+
 // Device pointer arithmetic on the two planes.
 __device__ __forceinline__ const uint4* group_codes(const uint8_t* w, size_t gpr, size_t row,
                                                     size_t g) {
@@ -77,6 +123,66 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// --- shared-memory addresses, mbarriers and 1-D bulk copies -----------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false
+// if it did not complete within `limit` polls (the caller records a fault and
+// gives up instead of hanging the GPU).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    const uint32_t a = smem_u32(bar);
+    for (uint32_t i = 0; i < limit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// Asynchronous global -> shared copy of `bytes` (multiple of 16, both
+// addresses 16-byte aligned) completing on `bar`'s transaction count.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once (weights): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 }  // namespace mxk

@@ -31,6 +31,9 @@ cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden,
                             const float* route_w, float* y, void* ws, cudaStream_t s);
 cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 
+// Device fault words (set when a bounded wait gives up); read and optionally clear.
+cudaError_t read_fault_matvec(int* value, bool reset);
+
 // Bytes of one [rows, cols] buffer, padded to 16.
 inline size_t padded_nbytes(int rows, int cols) {
     const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) / 32 * 17;

@@ -4,8 +4,9 @@
 // It restates the per-lane loop of "cortiq-engine 0.8.40
 // src/gpu_wgpu/mxfp4.rs" PEROP kernels mxfp4_mv / mxfp4_mm: lane l of a warp
 // takes groups g = l, l+32, ...; for each it decodes the 32 codes once, dots
-// them with every token's x over the group in element order (one FP32 FMA
-// chain per token), and adds scale * dot to the token's row partial.  A CTA
+// them with every token's x over the group (group_dots: FP32 FMA chains over
+// the even and the odd elements), and adds scale * dot to the token's row
+// partial.  A CTA
 // of kWarps warps stages the tokens' x in shared memory chunk by chunk and
 // each warp carries R rows of NM matrices, so one x read from shared memory
 // feeds R*NM rows and one decode feeds NB tokens.  The order of operations
@@ -74,63 +75,34 @@ __device__ __forceinline__ void cta_group_walk(const uint8_t* const (&wm)[NM], i
 
         for (int gl = lane; gl < ng; gl += 32) {
             const int g = gc + gl;
-            uint4 code[NM][R];
-            float s[NM][R];
+            uint4 code[NM * R];
+            float s[NM * R];
 #pragma unroll
             for (int m = 0; m < NM; ++m)
 #pragma unroll
                 for (int i = 0; i < R; ++i) {
                     const long row = row_w + i;
                     if (row < rows) {
-                        code[m][i] = ldg_stream(group_codes(wm[m], gpr, row, g));
-                        s[m][i] = e8m0_to_f32(group_scale_byte(wm[m] + code_bytes, gpr, row, g));
+                        code[m * R + i] = ldg_stream(group_codes(wm[m], gpr, row, g));
+                        s[m * R + i] =
+                            e8m0_to_f32(group_scale_byte(wm[m] + code_bytes, gpr, row, g));
                     } else {
-                        code[m][i] = make_uint4(0u, 0u, 0u, 0u);
-                        s[m][i] = 0.0f;
+                        code[m * R + i] = make_uint4(0u, 0u, 0u, 0u);
+                        s[m * R + i] = 0.0f;
                     }
                 }
-            float d[NM][R][NB];
+            const float* xp[NB];
 #pragma unroll
-            for (int m = 0; m < NM; ++m)
-#pragma unroll
-                for (int i = 0; i < R; ++i)
-#pragma unroll
-                    for (int t = 0; t < NB; ++t) d[m][i][t] = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float wv[NM][R][8];
-#pragma unroll
-                for (int m = 0; m < NM; ++m)
-#pragma unroll
-                    for (int i = 0; i < R; ++i) {
-                        const uint32_t word = k == 0   ? code[m][i].x
-                                              : k == 1 ? code[m][i].y
-                                              : k == 2 ? code[m][i].z
-                                                       : code[m][i].w;
-                        e2m1x8_to_f32(word, wv[m][i]);
-                    }
-#pragma unroll
-                for (int t = 0; t < NB; ++t) {
-                    const float* xp = xs + (t * KCG + gl) * kXPad + 8 * k;
-                    const float4 a = *reinterpret_cast<const float4*>(xp);
-                    const float4 b = *reinterpret_cast<const float4*>(xp + 4);
-                    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                    for (int m = 0; m < NM; ++m)
-#pragma unroll
-                        for (int i = 0; i < R; ++i)
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                d[m][i][t] = __fmaf_rn(wv[m][i][j], xv[j], d[m][i][t]);
-                }
-            }
+            for (int t = 0; t < NB; ++t) xp[t] = xs + (t * KCG + gl) * kXPad;
+            float dots[NM * R][NB];
+            group_dots<NM * R, NB>(code, xp, dots);
 #pragma unroll
             for (int m = 0; m < NM; ++m)
 #pragma unroll
                 for (int i = 0; i < R; ++i)
 #pragma unroll
                     for (int t = 0; t < NB; ++t)
-                        acc[m][i][t] = __fmaf_rn(s[m][i], d[m][i][t], acc[m][i][t]);
+                        acc[m][i][t] = __fmaf_rn(s[m * R + i], dots[m * R + i][t], acc[m][i][t]);
         }
     }
 }

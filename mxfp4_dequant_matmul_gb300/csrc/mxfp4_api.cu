@@ -70,6 +70,15 @@ int mxfp4_last_cuda_error(void) { return g_last_cuda_error; }
 
 int mxfp4_version(void) { return 100; }
 
+int mxfp4_device_faults(int* faults, int reset) {
+    if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
+    int v = 0;
+    const cudaError_t e = mxk::read_fault_matvec(&v, reset != 0);
+    if (e != cudaSuccess) return from_cuda(e);
+    *faults = v;
+    return MXFP4_STATUS_OK;
+}
+
 size_t mxfp4_nbytes(int rows, int cols) {
     if (check_shape(rows, cols) != MXFP4_STATUS_OK) return 0;
     return mxk::padded_nbytes(rows, cols);

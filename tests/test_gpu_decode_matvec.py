@@ -205,3 +205,7 @@ def test_host_buffer_entry_matches_device_entry(mx):
     mx.mxfp4_matmat_host(w, cfg.rows, cfg.cols, X_host, 1, Y_host, empty(cfg.cols),
                          empty(cfg.rows))
     assert_bits_equal(Y_host.numpy(), host(y_dev_ref), "host entry")
+
+
+def test_no_device_faults_after_the_suite(mx):
+    assert mx.mxfp4_device_faults(reset=True) == 0
