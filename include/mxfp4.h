@@ -172,6 +172,39 @@ int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter,
                    const float* route_w, float* y, void* workspace, size_t ws_bytes,
                    cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The routed-expert layer without a workspace.  The source pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory when they run the layer -- for example a serving process whose
+ * device memory all belongs to its own pool allocator, or a loop that must not
+ * call cudaMalloc once running because an allocation can block the device and
+ * stall its other streams.
+ *
+ * It runs mxfp4_moe_gate_up and then mxfp4_moe_down (same kernels, same
+ * results) with the routing plan, the activation act and the per-pair down
+ * outputs kept in one file-scope device array of MXFP4_MOE_NOALLOC_SCRATCH_BYTES
+ * bytes, which every GPU that loads the library holds until the process exits.
+ * It allocates nothing.  The caller passes inputs and the output
+ * y [n_tokens, hidden] only.
+ *   - Size limit: mxfp4_moe_workspace_bytes(n_experts, n_tokens, top_k, hidden,
+ *     inter) rounded up to 256, plus n_tokens*top_k*inter*4 bytes for act, must
+ *     not exceed MXFP4_MOE_NOALLOC_SCRATCH_BYTES; larger problems are refused
+ *     with MXFP4_STATUS_WORKSPACE_TOO_SMALL (use the workspace entry points).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array and the array keeps the previous call's
+ *     contents; each call rewrites all of the scratch it reads, so nothing has
+ *     to start at zero.  Calls that overlap on the GPU (other streams, other
+ *     host threads) race on the array: serialise them.
+ *   - Out-of-range expert ids are skipped as in mxfp4_moe_gate_up /
+ *     mxfp4_moe_down; their count is not reported by this entry point. */
+#define MXFP4_MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int mxfp4_moe_layer_noalloc(const void* gate_bank, const void* up_bank, const void* down_bank,
+                            int n_experts, int hidden, int inter, const float* x, int n_tokens,
+                            int top_k, const int32_t* expert_ids, const float* route_w, float* y,
+                            cudaStream_t stream);
+
 /* Copies the plan's count of out-of-range expert ids to *n_invalid (host) and
  * synchronises the stream.  For tests and debugging; the passes themselves
  * never synchronise. */

@@ -15,7 +15,7 @@ __all__ = [
     "Mxfp4Error", "lib", "library_path", "mxfp4_nbytes", "mxfp4_device_faults", "mxfp4_dequant", "mxfp4_mv",
     "mxfp4_mm", "mxfp4_mm_fp32", "mxfp4_mm_bf16", "mxfp4_matmat_host",
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
-    "mxfp4_moe_plan_errors", "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
+    "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +41,7 @@ _SIG = {
     "mxfp4_moe_gate_up": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _P]),
     "mxfp4_moe_down": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "mxfp4_moe_plan_errors": (_I, [_P, _SZ, ctypes.POINTER(_I), _P]),
+    "mxfp4_moe_layer_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIG)
 _lib = None
@@ -178,3 +179,15 @@ def mxfp4_moe_plan_errors(workspace, ws_bytes=None, stream=None) -> int:
     _check("mxfp4_moe_plan_errors", lib().mxfp4_moe_plan_errors(
         _addr(workspace), ws_bytes, ctypes.byref(n), _stream(stream)))
     return n.value
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def mxfp4_moe_layer_noalloc(gate_bank, up_bank, down_bank, n_experts, hidden, inter, x,
+                            n_tokens, top_k, expert_ids, route_w, y, stream=None):
+    """The whole routed-expert layer with its scratch in the library's own
+    fixed device array (no workspace argument, nothing allocated)."""
+    _check("mxfp4_moe_layer_noalloc", lib().mxfp4_moe_layer_noalloc(
+        _addr(gate_bank), _addr(up_bank), _addr(down_bank), n_experts, hidden, inter, _addr(x),
+        n_tokens, top_k, _addr(expert_ids), _addr(route_w), _addr(y), _stream(stream)))

@@ -34,6 +34,9 @@ cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 // Device fault words (set when a bounded wait gives up); read and optionally clear.
 cudaError_t read_fault_matvec(int* value, bool reset);
 
+// Records a CUDA error for mxfp4_last_cuda_error() (this thread).
+void record_cuda_error(int err);
+
 // Bytes of one [rows, cols] buffer, padded to 16.
 inline size_t padded_nbytes(int rows, int cols) {
     const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols) / 32 * 17;

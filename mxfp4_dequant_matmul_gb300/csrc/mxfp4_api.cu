@@ -53,6 +53,8 @@ const uint8_t* u8(const void* p) { return static_cast<const uint8_t*>(p); }
 
 }  // namespace
 
+void mxk::record_cuda_error(int err) { g_last_cuda_error = err; }
+
 extern "C" {
 
 const char* mxfp4_status_string(int status) {
