@@ -17,7 +17,17 @@ cudaError_t launch_dequant(const uint8_t* w, int rows, int cols, float* out, cud
 cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float* X, int nb,
                                float* Y, cudaStream_t s);
 
-// Tensor-core product with X rounded to bfloat16.
+// Tensor-core small-batch product (split-f16 activations, FP32 accumulate);
+// cudaErrorNotSupported, with nothing launched, for shapes it cannot take.
+cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                         cudaStream_t s);
+
+// tcgen05 product with X rounded to bfloat16 (prefill.cu).
+cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                              float* Y, cudaStream_t s);
+
+// CUDA-core product with X rounded to bfloat16 (same numerics as the tcgen05
+// path; kept as a cross-check).
 cudaError_t launch_mm_bf16(const uint8_t* w, int rows, int cols, const float* X, int nb,
                            float* Y, cudaStream_t s);
 
@@ -33,6 +43,8 @@ cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 
 // Device fault words (set when a bounded wait gives up); read and optionally clear.
 cudaError_t read_fault_matvec(int* value, bool reset);
+cudaError_t read_fault_mma(int* value, bool reset);
+cudaError_t read_fault_prefill(int* value, bool reset);
 
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);

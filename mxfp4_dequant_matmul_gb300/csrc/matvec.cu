@@ -258,11 +258,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_mv_bulk(const uint8_t* __restri
         for (int st = 0; st < S; ++st)
             if (rb0 + st * stride < n_rb) issue(rb0 + st * stride, st);
     }
-    // x into shared memory while the first stages are in flight
-    for (int i = threadIdx.x; i < gpr * 8; i += kThreads) {
-        const int g = i >> 3, q = i & 7;
-        *reinterpret_cast<float4*>(xs + g * kXPad + q * 4) =
-            __ldg(reinterpret_cast<const float4*>(x + static_cast<size_t>(g) * kGroup) + q);
+    // x into shared memory while the first stages are in flight (eight loads in
+    // flight per thread before their stores)
+    for (int base = threadIdx.x; base < gpr * 8; base += 8 * kThreads) {
+        float4 v[8];
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {
+            const int i = base + k8 * kThreads;
+            if (i < gpr * 8)
+                v[k8] = __ldg(reinterpret_cast<const float4*>(x) + i);
+        }
+#pragma unroll
+        for (int k8 = 0; k8 < 8; ++k8) {
+            const int i = base + k8 * kThreads;
+            if (i < gpr * 8) *reinterpret_cast<float4*>(xs + (i >> 3) * kXPad + (i & 7) * 4) = v[k8];
+        }
     }
     __syncthreads();
 

@@ -74,10 +74,12 @@ int mxfp4_version(void) { return 100; }
 
 int mxfp4_device_faults(int* faults, int reset) {
     if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
-    int v = 0;
-    const cudaError_t e = mxk::read_fault_matvec(&v, reset != 0);
+    int a = 0, b = 0, c = 0;
+    cudaError_t e = mxk::read_fault_matvec(&a, reset != 0);
+    if (e == cudaSuccess) e = mxk::read_fault_mma(&b, reset != 0);
+    if (e == cudaSuccess) e = mxk::read_fault_prefill(&c, reset != 0);
     if (e != cudaSuccess) return from_cuda(e);
-    *faults = v;
+    *faults = a | (b << 1) | (c << 2);
     return MXFP4_STATUS_OK;
 }
 
@@ -107,15 +109,19 @@ int mxfp4_mm_fp32(const void* w, int rows, int cols, const float* X, int nb, flo
 int mxfp4_mm_bf16(const void* w, int rows, int cols, const float* X, int nb, float* Y,
                   cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
-    return from_cuda(mxk::launch_mm_bf16(u8(w), rows, cols, X, nb, Y, stream));
+    return from_cuda(mxk::launch_mm_tcgen05(u8(w), rows, cols, X, nb, Y, stream));
 }
 
 int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
              cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
-    if (nb <= MXFP4_MM_SMALL_MAX)
+    if (nb <= MXFP4_MM_SMALL_MAX) {
+        const cudaError_t e = mxk::launch_mm_tc(u8(w), rows, cols, X, nb, Y, stream);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        (void)cudaGetLastError();
         return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, X, nb, Y, stream));
-    return from_cuda(mxk::launch_mm_bf16(u8(w), rows, cols, X, nb, Y, stream));
+    }
+    return from_cuda(mxk::launch_mm_tcgen05(u8(w), rows, cols, X, nb, Y, stream));
 }
 
 int mxfp4_matmat_host(const void* w, int rows, int cols, const float* X_host, int nb,

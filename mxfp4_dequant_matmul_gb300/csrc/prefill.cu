@@ -1,0 +1,322 @@
+// prefill.cu -- large-batch MXFP4 product on the 5th-generation tensor cores
+// (tcgen05 + TMEM, sm_103a).
+//
+// Y[t*rows + r] = sum_c W[r][c] * bf16(X[t][c]): the weights decoded exactly to
+// bfloat16 (an E2M1 value times a power of two always fits), the activations
+// rounded to nearest-even bfloat16 ("cortiq-engine 0.8.40
+// src/gpu_wgpu/mxfp4.rs", GLOBAL fn mxg_bf16), products accumulated in FP32.
+// This is the dense contraction of the prefill (many tokens share each weight;
+// "rlx-cpu 0.2.17 src/gguf_matmul.rs" gguf_matmul_bt_cached: dequantise once,
+// then a dense GEMM).
+//
+// One CTA computes a tile of 128 tokens (the MMA's M, operand A = bf16(X)) by
+// 256 weight rows (N, operand B = decoded W), stepping K by 64 (one 128-byte
+// swizzle atom of bf16).  All 16 warps produce: each k-step they load X (f32)
+// and W (codes + scale bytes) for the next step into registers, convert the
+// current step into bfloat16 tiles in shared memory (K-major, 128-byte
+// swizzle), and thread 0 issues four tcgen05.mma (K = 16 each) into a 128 x 256
+// FP32 accumulator in tensor memory; tcgen05.commit frees the stage when the
+// MMAs have read it.  The epilogue reads the accumulator with tcgen05.ld and
+// writes Y.  Every wait is bounded; a CTA that gives up sets the fault word,
+// still frees its tensor memory and returns.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxk {
+namespace {
+
+constexpr int kPM = 128;            // tokens per tile (MMA M)
+constexpr int kPN = 256;            // weight rows per tile (MMA N)
+constexpr int kPK = 64;             // K per step (one 128-byte bf16 swizzle atom)
+constexpr int kPStages = 3;
+constexpr int kPThreads = 512;
+constexpr int kAChunks = kPM * kPK / 8 / kPThreads;   // 16-byte bf16 chunks of A per thread
+constexpr int kBChunks = kPN * kPK / 8 / kPThreads;   // and of B
+constexpr uint32_t kATileBytes = kPM * kPK * 2;   // 16 KB
+constexpr uint32_t kBTileBytes = kPN * kPK * 2;   // 32 KB
+constexpr uint32_t kPStageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kPWaitLimit = 1u << 24;
+
+__device__ int g_fault_prefill;
+
+// --- tcgen05 helpers ----------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                   // leading offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride offset: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: dense, D = F32, A = B = BF16, both K-major, N, M.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two floats -> bf16x2, round to nearest even, `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Raw inputs of one k-step held by one thread: kAChunks chunks of 8
+// activations and kBChunks code words (8 weights each) with their scale bytes.
+struct Raw {
+    float4 x[kAChunks][2];
+    uint32_t code[kBChunks];
+    uint32_t sc[kBChunks];
+};
+
+__global__ void __launch_bounds__(kPThreads, 1) k_prefill(const uint8_t* __restrict__ w, int rows,
+                                                          int cols, const float* __restrict__ X,
+                                                          int nb, float* __restrict__ Y) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment of the tiles (the swizzle pattern repeats every 1024 B)
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bars[kPStages + 1];   // stage free, + accumulator done
+    __shared__ uint32_t tmem_base;
+    __shared__ int ok_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * kPN;      // weight rows of this tile
+    const int t0 = blockIdx.y * kPM;      // tokens of this tile
+    const int gpr = cols / kGroup;
+    const int n_steps = (cols + kPK - 1) / kPK;
+    const uint8_t* scales = w + static_cast<size_t>(rows) * cols / 2;
+
+    if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+    if (tid == 0) {
+        for (int i = 0; i <= kPStages; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    auto load = [&](int s, Raw& raw) {
+        const int k0 = s * kPK;
+#pragma unroll
+        for (int i = 0; i < kAChunks; ++i) {
+            const int c = tid + kPThreads * i;
+            const int m = c >> 3, j = c & 7;
+            const int t = t0 + m, k = k0 + 8 * j;
+            if (t < nb && k < cols) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(X + static_cast<size_t>(t) * cols + k);
+                raw.x[i][0] = __ldg(src);
+                raw.x[i][1] = __ldg(src + 1);
+            } else {
+                raw.x[i][0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                raw.x[i][1] = raw.x[i][0];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBChunks; ++i) {
+            const int c = tid + kPThreads * i;
+            const int n = c >> 3, j = c & 7;
+            const int r = r0 + n, g = 2 * s + (j >> 2);
+            if (r < rows && g < gpr) {
+                raw.code[i] = __ldg(reinterpret_cast<const uint32_t*>(
+                                        w + (static_cast<size_t>(r) * gpr + g) * kGroupBytes) +
+                                    (j & 3));
+                raw.sc[i] = __ldg(scales + static_cast<size_t>(r) * gpr + g);
+            } else {
+                raw.code[i] = 0u;
+                raw.sc[i] = 127u;   // 1.0 times code 0: an exact zero
+            }
+        }
+    };
+    auto store = [&](const Raw& raw, int st) {
+        const uint32_t a_base = smem_u32(smem + st * kPStageBytes);
+        const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+        for (int i = 0; i < kAChunks; ++i) {
+            const int c = tid + kPThreads * i;
+            const int m = c >> 3, j = c & 7;
+            const float4 a = raw.x[i][0], b = raw.x[i][1];
+            sts128(a_base + m * 128 + ((j ^ (m & 7)) << 4), pack_bf16x2(a.x, a.y),
+                   pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+        }
+#pragma unroll
+        for (int i = 0; i < kBChunks; ++i) {
+            const int c = tid + kPThreads * i;
+            const int n = c >> 3, j = c & 7;
+            const float s = e8m0_to_f32(raw.sc[i]);
+            float v[8];
+            e2m1x8_to_f32(raw.code[i], v);
+            // value times a power of two: exact in float and in bfloat16
+            sts128(b_base + n * 128 + ((j ^ (n & 7)) << 4),
+                   pack_bf16x2(__fmul_rn(v[0], s), __fmul_rn(v[1], s)),
+                   pack_bf16x2(__fmul_rn(v[2], s), __fmul_rn(v[3], s)),
+                   pack_bf16x2(__fmul_rn(v[4], s), __fmul_rn(v[5], s)),
+                   pack_bf16x2(__fmul_rn(v[6], s), __fmul_rn(v[7], s)));
+        }
+    };
+
+    constexpr uint32_t idesc = idesc_bf16(kPM, kPN);
+    bool ok = true;
+    Raw A, B;
+    load(0, A);
+    for (int s = 0; s < n_steps; ++s) {
+        Raw& cur = (s & 1) ? B : A;
+        Raw& nxt = (s & 1) ? A : B;
+        const int st = s % kPStages;
+        if (s + 1 < n_steps) load(s + 1, nxt);
+        // the stage is free once the MMAs of step s - kPStages have read it
+        if (tid == 0) {
+            ok_flag = s < kPStages ||
+                      mbar_wait(&bars[st], static_cast<uint32_t>((s / kPStages - 1) & 1),
+                                kPWaitLimit);
+        }
+        __syncthreads();
+        if (!ok_flag) {
+            ok = false;
+            break;
+        }
+        store(cur, st);
+        fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + st * kPStageBytes);
+            const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kPK / 16; ++kk)
+                umma_bf16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc,
+                          (s > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bars[st]);
+            if (s == n_steps - 1) umma_commit(&bars[kPStages]);
+        }
+    }
+
+    // epilogue: wait for the accumulator, then TMEM -> registers -> Y
+    if (tid == 0) ok_flag = ok && mbar_wait(&bars[kPStages], 0u, kPWaitLimit);
+    __syncthreads();
+    if (ok_flag) {
+        tc_fence_after();
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        constexpr int kColsPerWarp = kPN / (kPThreads / 128);
+        const int col0 = (warp >> 2) * kColsPerWarp;
+        const int t = t0 + quarter * 32 + lane;
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0 + cc, v);
+            const int rbase = r0 + col0 + cc;
+            if (t < nb) {
+                float* dst = Y + static_cast<size_t>(t) * rows + rbase;
+                if (rbase + 32 <= rows && (rows & 3) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (rbase + i < rows) dst[i] = __uint_as_float(v[i]);
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicOr(&g_fault_prefill, 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                              float* Y, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(kPStages) * kPStageBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
+    k_prefill<<<grid, kPThreads, smem, s>>>(w, rows, cols, X, nb, Y);
+    return cudaGetLastError();
+}
+
+cudaError_t read_fault_prefill(int* value, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_prefill, sizeof(int));
+    if (e != cudaSuccess || !reset) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_fault_prefill, &zero, sizeof(int));
+}
+
+}  // namespace mxk

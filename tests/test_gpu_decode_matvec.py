@@ -134,10 +134,14 @@ def test_page_shapes_mv_and_batches_equal_per_token(mx, rows, cols):
         Y32 = run_mm(mx, w_h, rows, cols, X, b, "mxfp4_mm_fp32")
         ref, l1 = oracle.matmat(w_h, rows, cols, X, b)
         assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} batch {b}")
-        assert_bits_equal(Y, Y32, "mm vs mm_fp32")
+        assert_within(Y32, ref, l1, REL_FP32, f"{rows}x{cols} batch {b} (FP32 path)")
         for t in range(b):
+            # the FP32 batch path equals the matvec bit for bit, and a token's
+            # result from mxfp4_mm does not depend on the rest of its batch
             one = run_mv(mx, w_h, rows, cols, X[t])
-            assert_bits_equal(Y[t], one, f"batch {b} token {t} vs its matvec")
+            assert_bits_equal(Y32[t], one, f"FP32 batch {b} token {t} vs its matvec")
+            alone = run_mm(mx, w_h, rows, cols, X[t:t + 1], 1)
+            assert_bits_equal(Y[t], alone[0], f"batch {b} token {t} vs the token alone")
 
 
 def test_mm8_config_every_output(mx):
@@ -147,6 +151,34 @@ def test_mm8_config_every_output(mx):
     ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, X, cfg.nb)
     worst = assert_within(Y, ref, l1, REL_FP32, "mm nb=8")
     print(f"mm nb=8 worst err/tol {worst:.3g}")
+
+
+@pytest.mark.parametrize("nb", [1, 3, 5, 8, 13])
+def test_mm_wide_dynamic_range_activations(mx, nb):
+    # activations spanning ~2^-60 .. 2^60 inside every group, plus an all-zero
+    # group: the per-(token, group) prescale of the tensor-core path must keep
+    # every group's small elements
+    rows, cols = 200, 1024
+    w_h = synth.mxfp4_matrix(rows, cols, 40 + nb, 118, 130)
+    base = synth.normal_f32(70 + nb, nb * cols).astype(np.float64)
+    expo = synth.uniform_int(80 + nb, nb * cols, -60, 60)
+    X = (base * np.exp2(expo)).astype(np.float32).reshape(nb, cols)
+    X[:, 64:96] = 0.0
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    assert_within(Y, ref, l1, REL_FP32, f"wide range nb={nb}")
+
+
+@pytest.mark.parametrize("rows,cols,nb", [(50, 544, 3), (33, 32, 8), (17, 160, 2), (131, 2880, 8),
+                                          (64, 96, 1)])
+def test_mm_ragged_shapes(mx, rows, cols, nb):
+    # group counts that do not split evenly over the CTAs of a cluster (or are
+    # fewer than its CTAs), and row counts that are not multiples of 16
+    w_h = synth.mxfp4_matrix(rows, cols, rows + cols + nb, 118, 130)
+    X = synth.normal_f32(rows * 3 + nb, nb * cols).reshape(nb, cols)
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} nb={nb}")
 
 
 def test_mm_exact_inputs_bit_for_bit(mx):
