@@ -14,8 +14,9 @@
 // carries 22 significant bits of x * 2^p and every product with an E2M1 value
 // is exact in the FP32 accumulator.  hi and lo of an element sit in two k-slots
 // of the same MMA facing the same weight, so the tensor core adds them.  A
-// group (32 elements) is four MMAs into a fresh accumulator; each thread then
-// multiplies its four outputs by scale * 2^-p and accumulates in FP32.
+// group (32 elements) is four MMAs into two fresh accumulators (two chains of
+// two, for latency), added; each thread then multiplies its four outputs by
+// scale * 2^-p and accumulates in FP32.
 //
 // K-permutation: lane (q = lane/4, u = lane%4) owns the k-slots 2u, 2u+1,
 // 2u+8, 2u+9 of every MMA; for MMA m of a group it puts elements 8u+2m and
@@ -52,10 +53,10 @@
 namespace mxk {
 namespace {
 
-constexpr int kWarpsT = 8;                 // warps per CTA
+constexpr int kWarpsT = 16;                // warps per CTA
 constexpr int kThreadsT = kWarpsT * 32;
 constexpr int kChunk = 8;                  // groups per unit (128 code bytes per row)
-constexpr int kStages = 4;                 // ring stages per warp
+constexpr int kStages = 2;                 // ring stages per warp
 constexpr int kStageBytes = 16 * 128;      // one TMA tile: 16 rows x 128 bytes
 constexpr uint32_t kWaitLimitT = 1u << 22;
 
@@ -315,11 +316,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 const uint4* xf = reinterpret_cast<const uint4*>(xfrag) +
                                   static_cast<size_t>(gc - g_lo + j) * 64 + lane;
                 const uint4 b01 = xf[0], b23 = xf[32];
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_16816(d, h0[0], h1[0], h0[0], h1[0], b01.x, b01.y);
-                mma_16816(d, h0[1], h1[1], h0[1], h1[1], b01.z, b01.w);
-                mma_16816(d, h0[2], h1[2], h0[2], h1[2], b23.x, b23.y);
-                mma_16816(d, h0[3], h1[3], h0[3], h1[3], b23.z, b23.w);
+                // two independent accumulation chains (elements 8u..8u+3 and
+                // 8u+4..8u+7), added afterwards
+                float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_16816(da, h0[0], h1[0], h0[0], h1[0], b01.x, b01.y);
+                mma_16816(db, h0[2], h1[2], h0[2], h1[2], b23.x, b23.y);
+                mma_16816(da, h0[1], h1[1], h0[1], h1[1], b01.z, b01.w);
+                mma_16816(db, h0[3], h1[3], h0[3], h1[3], b23.z, b23.w);
+                float d[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[e] = __fadd_rn(da[e], db[e]);
                 const float s0 = e8m0_to_f32(sc0[j]), s1 = e8m0_to_f32(sc1[j]);
                 const float p0 = pfac[(gc - g_lo + j) * 8 + 2 * u];
                 const float p1 = pfac[(gc - g_lo + j) * 8 + 2 * u + 1];
