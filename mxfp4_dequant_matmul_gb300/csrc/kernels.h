@@ -17,7 +17,12 @@ cudaError_t launch_dequant(const uint8_t* w, int rows, int cols, float* out, cud
 cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float* X, int nb,
                                float* Y, cudaStream_t s);
 
-// Tensor-core small-batch product (split-f16 activations, FP32 accumulate);
+// tcgen05 small-batch product (decoded weights in tensor memory, split-f16
+// activations, FP32 accumulate); cudaErrorNotSupported when it cannot take the shape.
+cudaError_t launch_mm_tc5(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                          cudaStream_t s);
+
+// mma.sync small-batch product (split-f16 activations, FP32 accumulate);
 // cudaErrorNotSupported, with nothing launched, for shapes it cannot take.
 cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
                          cudaStream_t s);
@@ -45,6 +50,7 @@ cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 cudaError_t read_fault_matvec(int* value, bool reset);
 cudaError_t read_fault_mma(int* value, bool reset);
 cudaError_t read_fault_prefill(int* value, bool reset);
+cudaError_t read_fault_tc5(int* value, bool reset);
 
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);

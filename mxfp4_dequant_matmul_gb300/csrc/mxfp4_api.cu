@@ -74,12 +74,13 @@ int mxfp4_version(void) { return 100; }
 
 int mxfp4_device_faults(int* faults, int reset) {
     if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
-    int a = 0, b = 0, c = 0;
+    int a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = mxk::read_fault_matvec(&a, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_mma(&b, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_prefill(&c, reset != 0);
+    if (e == cudaSuccess) e = mxk::read_fault_tc5(&d, reset != 0);
     if (e != cudaSuccess) return from_cuda(e);
-    *faults = a | (b << 1) | (c << 2);
+    *faults = a | (b << 1) | (c << 2) | (d << 3);
     return MXFP4_STATUS_OK;
 }
 
@@ -116,7 +117,10 @@ int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y
              cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
     if (nb <= MXFP4_MM_SMALL_MAX) {
-        const cudaError_t e = mxk::launch_mm_tc(u8(w), rows, cols, X, nb, Y, stream);
+        cudaError_t e = mxk::launch_mm_tc5(u8(w), rows, cols, X, nb, Y, stream);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        (void)cudaGetLastError();
+        e = mxk::launch_mm_tc(u8(w), rows, cols, X, nb, Y, stream);
         if (e != cudaErrorNotSupported) return from_cuda(e);
         (void)cudaGetLastError();
         return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, X, nb, Y, stream));
