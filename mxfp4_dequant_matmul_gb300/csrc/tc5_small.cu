@@ -7,21 +7,23 @@
 //
 // A CTA takes a tile of 128 weight rows and a slice of the groups (the K
 // dimension; the CTAs of a thread-block cluster split the groups and add their
-// partial sums through distributed shared memory).  Per group (32 elements):
-//   * a decoder warp per 32-row quarter reads its rows' 16 code bytes from a
-//     TMA-filled shared-memory stage, converts the E2M1 codes to f16 (exact,
-//     the hardware pair conversion) and stores them with tcgen05.st as the A
-//     operand (128 rows x K = 32) of the group's slot in tensor memory;
-//   * one thread issues two tcgen05.mma (M = 128, N = 16, K = 16) with that A
-//     and, as B, the activations of the pass from shared memory: column n < 8
-//     is token n's hi half, column 8 + n its lo half (hi = f16(x 2^p),
-//     lo = f16(x 2^p - hi), one power of two p per token for the CTA's slice);
-//     every product is exact and the accumulator is FP32;
-//   * an epilogue warp per quarter reads the 16 accumulator columns back with
-//     tcgen05.ld, and adds scale * (hi + lo) to each token's FP32 row sum.
-// Eight slots (A + accumulator) rotate through tensor memory so that decode,
-// MMA and epilogue of different groups overlap; mbarriers order them, and every
-// wait is bounded.
+// partial sums through distributed shared memory).
+//   * Decoder warps (two per 32-row quarter of tensor memory, taking batches of
+//     four groups in turn) read their rows' code bytes from TMA-filled
+//     shared-memory stages, convert the E2M1 codes to f16 (the hardware pair
+//     conversion, exact), multiply them by 2^(k - kmax) -- k the group's scale
+//     byte, kmax the largest scale byte of the row in the slice, so the product
+//     stays exact in f16 for scale spreads up to 23 binades -- and store them
+//     with tcgen05.st as the A operand (128 rows x K = 32 per group) in a ring
+//     of tensor-memory slots.
+//   * One thread issues two tcgen05.mma (M = 128, N = 16, K = 16) per group,
+//     all accumulating into one FP32 tile in tensor memory; B is the pass's
+//     activations in shared memory: column n < 8 is token n's hi half, column
+//     8 + n its lo half (hi = f16(x 2^p), lo = f16(x 2^p - hi), one power of two
+//     p per token for the slice).  Every product is exact.
+//   * At the end the accumulator is read once (tcgen05.ld), hi + lo added and
+//     scaled by 2^(kmax - 127) 2^-p; a row with a NaN scale byte gives NaN.
+// mbarriers order the stages and slots, and every wait is bounded.
 #include <cstdint>
 #include <mutex>
 
@@ -41,12 +43,17 @@ constexpr int kTok = 8;                     // tokens per pass
 constexpr int kStageGroups = 8;             // groups per code stage (128 bytes per row)
 constexpr int kStages5 = 4;                 // code stages
 constexpr int kStageBytes5 = kRowsT * 128;  // 16 KB
-constexpr int kSlots = 8;                   // (A, accumulator) slots in tensor memory
-constexpr int kSlotCols = 32;               // A: 16 columns (K = 32 f16), D: 16 columns
-constexpr uint32_t kTmemCols5 = kSlots * kSlotCols;   // 256
-constexpr int kWarps5 = 10;                 // 0-3 decode, 4-7 epilogue, 8 TMA, 9 MMA
+constexpr int kBatch = 4;                   // groups per decoder batch
+constexpr int kSlots = 6;                   // A batch slots in tensor memory
+constexpr int kSlotCols = kBatch * 16;      // 16 columns (K = 32 f16) per group
+constexpr uint32_t kDCol = kSlots * kSlotCols;   // accumulator: 16 columns after the slots
+constexpr uint32_t kTmemCols5 = 512;
+constexpr int kWarps5 = 10;                 // 0-7 decode (0-3 also epilogue), 8 TMA, 9 MMA
 constexpr int kThreads5 = kWarps5 * 32;
 constexpr uint32_t kWait5 = 1u << 24;
+constexpr int kMaxGroups5 = 140;            // groups per CTA slice (shared memory bound)
+constexpr int kMaxChunks = (kTok * kMaxGroups5 * 4 + kThreads5 - 1) / kThreads5;
+constexpr int kMaxScChunks = (kRowsT * ((kMaxGroups5 + 30) / 16) + kThreads5 - 1) / kThreads5;
 
 __device__ int g_fault_tc5;
 
@@ -110,7 +117,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -163,7 +169,7 @@ __device__ __forceinline__ uint32_t pack_f16x2_5(float lo, float hi) {
 
 // Shared memory layout (offsets from a 1024-byte aligned base).
 struct T5Layout {
-    uint32_t btile, stages, sc, sc_pitch, part, bars, misc, total;
+    uint32_t btile, stages, sc, sc_pitch, part, kref, bars, misc, total;
 };
 __host__ __device__ inline T5Layout t5_layout(int ng) {
     T5Layout l;
@@ -174,9 +180,10 @@ __host__ __device__ inline T5Layout t5_layout(int ng) {
     l.sc_pitch = (static_cast<uint32_t>(ng) + 15u) & ~15u;
     l.part = l.sc + kRowsT * l.sc_pitch;                           // [128][8] f32
     l.part = (l.part + 15u) & ~15u;
-    l.bars = l.part + kRowsT * kTok * 4;                           // mbarriers
+    l.kref = l.part + kRowsT * kTok * 4;                           // [128] kmax, [128] NaN flag
+    l.bars = l.kref + 2 * kRowsT;                                  // mbarriers
     l.bars = (l.bars + 7u) & ~7u;
-    l.misc = l.bars + (2 * kStages5 + 3 * kSlots) * 8;             // tmem addr, flags, p
+    l.misc = l.bars + (2 * kStages5 + 2 * kSlots + 1) * 8;         // tmem addr, flags, p
     l.total = l.misc + 128 + 1024;                                 // + alignment slack
     return l;
 }
@@ -196,8 +203,10 @@ __global__ void __launch_bounds__(kThreads5, 1)
     uint64_t* code_full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* code_free = code_full + kStages5;
     uint64_t* a_full = code_free + kStages5;
-    uint64_t* d_full = a_full + kSlots;
-    uint64_t* slot_free = d_full + kSlots;
+    uint64_t* a_free = a_full + kSlots;
+    uint64_t* done_bar = a_free + kSlots;
+    uint8_t* kref_s = smem + L.kref;
+    uint8_t* nan_s = kref_s + kRowsT;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
     int* pexp = reinterpret_cast<int*>(smem + L.misc + 8);             // [8] per-token 2^p
@@ -220,13 +229,13 @@ __global__ void __launch_bounds__(kThreads5, 1)
     if (tid == 0) {
         for (int i = 0; i < kStages5; ++i) {
             mbar_init(&code_full[i], 1);
-            mbar_init(&code_free[i], 4);
+            mbar_init(&code_free[i], 8);   // both decoder warps of every quarter
         }
         for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&a_full[i], 4);
-            mbar_init(&d_full[i], 1);
-            mbar_init(&slot_free[i], 4);
+            mbar_init(&a_full[i], 4);      // the batch's decoder warp of every quarter
+            mbar_init(&a_free[i], 1);      // tcgen05.commit
         }
+        mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -252,85 +261,130 @@ __global__ void __launch_bounds__(kThreads5, 1)
     if (warp == 8 && lane == 0)
         for (int s = 0; s < kStages5 && s < n_st; ++s) issue_stage(s);
 
-    // --- scale bytes of the tile's rows and this CTA's groups
+    // --- activations: every thread loads its 8-element chunks of the slice at
+    // once (one round trip), the per-token largest |x| picks the power of two
+    // p, then the chunks become the B tiles.  B tile for group pair g2: rows n
+    // (n < 8: token n hi, else token n - 8 lo), 64 f16 per row (group 2*g2 then
+    // 2*g2 + 1), 128-byte swizzle.
     {
+        // scale bytes of the tile's rows and this CTA's groups: row r's ng bytes,
+        // read as the aligned 16-byte words that cover them (the buffer is padded
+        // to 16 bytes, so no word leaves it); loads issued before the activations'
         const int nrow = min(kRowsT, rows - row0);
-        for (int base = tid; base < nrow * ng; base += 8 * kThreads5) {
-            uint32_t v[8];
+        const int nch_row = (ng + 30) / 16;   // words covering ng bytes at any alignment
+        uint4 sv[kMaxScChunks];
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-                const int i = base + k8 * kThreads5;
-                v[k8] = 0u;
-                if (i < nrow * ng) {
-                    const int r = i / ng, j = i - r * ng;
-                    v[k8] = __ldg(w + plane + static_cast<size_t>(row0 + r) * gpr + g_lo + j);
-                }
+        for (int u = 0; u < kMaxScChunks; ++u) {
+            const int i = tid + u * kThreads5;
+            const int r = i / nch_row, c = i - r * nch_row;
+            sv[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < nrow) {
+                const size_t s0 = plane + static_cast<size_t>(row0 + r) * gpr + g_lo;
+                const size_t addr = (s0 & ~static_cast<size_t>(15)) + 16 * static_cast<size_t>(c);
+                if (addr < s0 + ng) sv[u] = ldg_stream(reinterpret_cast<const uint4*>(w + addr));
             }
+        }
+        // chunk i (8 elements): token t = i % 8, element block e8 = i / 8 of the
+        // slice; kThreads5 is a multiple of 8, so each thread keeps one token
+        const int t = tid & 7;
+        const int n_e8 = ng * 4;
+        const bool t_ok = t < nbt;
+        float xv[kMaxChunks][8];
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {
-                const int i = base + k8 * kThreads5;
-                if (i < nrow * ng) {
-                    const int r = i / ng, j = i - r * ng;
-                    sc_s[r * L.sc_pitch + j] = static_cast<uint8_t>(v[k8]);
+        for (int u = 0; u < kMaxChunks; ++u) {
+            const int e8 = (tid >> 3) + u * (kThreads5 / 8);
+            if (e8 < n_e8 && t_ok) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    X + static_cast<size_t>(t0 + t) * cols + static_cast<size_t>(g_lo) * kGroup +
+                    8 * e8);
+                const float4 a = __ldg(src), b = __ldg(src + 1);
+                xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+                xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) xv[u][k] = 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMaxScChunks; ++u) {
+            const int i = tid + u * kThreads5;
+            const int r = i / nch_row, c = i - r * nch_row;
+            if (r < nrow) {
+                const int mis = static_cast<int>((plane + static_cast<size_t>(row0 + r) * gpr + g_lo) & 15);
+                const int off = 16 * c - mis;   // position of the word's byte 0 in the row
+                const uint32_t wv[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = off + k;
+                    if (j >= 0 && j < ng)
+                        sc_s[r * L.sc_pitch + j] = static_cast<uint8_t>(wv[k >> 2] >> (8 * (k & 3)));
                 }
             }
         }
+        if (tid < nrow)   // bytes past the row's groups read as 0 in the scan below
+            for (int j = ng; j < static_cast<int>(L.sc_pitch); ++j) sc_s[tid * L.sc_pitch + j] = 0;
+        float m = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kMaxChunks; ++u)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(xv[u][k]) <= 3.402823466e38f ? fabsf(xv[u][k]) : 0.0f);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (lane < 8 && m > 0.0f) atomicMax(&tmax[t], __float_as_uint(m));
+        __syncthreads();
+        if (tid < kTok) {
+            const float mt = __uint_as_float(tmax[tid]);
+            // puts the token's largest |x| in [2^14, 2^15); capped so 2^-p stays normal
+            pexp[tid] = mt > 0.0f ? min(14 - ilogbf(mt), 126) : 0;
+        }
+        __syncthreads();
+        const float pmul = exp2i5(pexp[t]);   // 2^p, a normal float for every p above
+#pragma unroll
+        for (int u = 0; u < kMaxChunks; ++u) {
+            const int e8 = (tid >> 3) + u * (kThreads5 / 8);
+            if (e8 < n_e8) {
+                const int g = e8 >> 2, g2 = g >> 1;
+                const int c = ((g & 1) << 2) | (e8 & 3);   // 16-byte chunk within the 128-byte row
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a0 = __fmul_rn(xv[u][2 * k], pmul);
+                    const float a1 = __fmul_rn(xv[u][2 * k + 1], pmul);
+                    hi[k] = pack_f16x2_5(a0, a1);
+                    const float2 h = f16x2_to_f32x2(hi[k]);
+                    lo[k] = pack_f16x2_5(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
+                }
+                uint8_t* tb = btile + g2 * 2048;
+                const int rh = t, rl = t + 8;
+                *reinterpret_cast<uint4*>(tb + rh * 128 + ((c ^ (rh & 7)) << 4)) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(tb + rl * 128 + ((c ^ (rl & 7)) << 4)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        // the odd group of a ragged last pair: zero B columns
+        if (ng & 1) {
+            uint8_t* tb = btile + (ng >> 1) * 2048;
+            for (int i = tid; i < 16 * 4; i += kThreads5) {
+                const int n = i >> 2, c = 4 | (i & 3);
+                *reinterpret_cast<uint4*>(tb + n * 128 + ((c ^ (n & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < kRowsT) {   // largest scale byte below 255 of the row, and any 255
+        unsigned mx = 0u, nanf = 0u;
+        for (int j = 0; j < static_cast<int>(L.sc_pitch) && tid < rows - row0; j += 4) {
+            const unsigned v = *reinterpret_cast<const unsigned*>(sc_s + tid * L.sc_pitch + j);
+            const unsigned is255 = __vcmpeq4(v, 0xFFFFFFFFu);
+            nanf |= is255;
+            mx = __vmaxu4(mx, v & ~is255);
+        }
+        mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
+        kref_s[tid] = static_cast<uint8_t>(mx);
+        nan_s[tid] = nanf ? 1 : 0;
     }
 
-    // --- activations: per-token largest |x| over this CTA's slice, then the B
-    // tiles.  B tile for group pair g2: rows n (n < 8: token n hi, else token
-    // n - 8 lo), 64 f16 per row (group 2*g2 then 2*g2 + 1), 128-byte swizzle.
-    for (int i = tid; i < kTok * ng * 8; i += kThreads5) {
-        const int t = i / (ng * 8), rem = i - t * ng * 8;
-        float m = 0.0f;
-        if (t < nbt) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(
-                X + static_cast<size_t>(t0 + t) * cols + static_cast<size_t>(g_lo) * kGroup) + rem);
-            m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-        }
-        if (m > 0.0f && m <= 3.402823466e38f) atomicMax(&tmax[t], __float_as_uint(m));
-    }
-    __syncthreads();
-    if (tid < kTok) {
-        const float m = __uint_as_float(tmax[tid]);
-        // puts the token's largest |x| in [2^14, 2^15); capped so 2^-p stays normal
-        pexp[tid] = m > 0.0f ? min(14 - ilogbf(m), 126) : 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < ((ng + 1) / 2) * kTok * 8; i += kThreads5) {
-        // one 16-byte chunk c of token t in pair g2: elements 8*(c%4) .. of group 2*g2 + c/4
-        const int g2 = i / (kTok * 8), rem = i - g2 * kTok * 8;
-        const int t = rem >> 3, c = rem & 7;
-        const int g = 2 * g2 + (c >> 2);
-        float v[8];
-        if (t < nbt && g < ng) {
-            const float4* src = reinterpret_cast<const float4*>(
-                X + static_cast<size_t>(t0 + t) * cols + static_cast<size_t>(g_lo + g) * kGroup +
-                8 * (c & 3));
-            const float4 a = __ldg(src), b = __ldg(src + 1);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-        }
-        const int p = pexp[t];
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float a0 = scale2_5(v[2 * k], p), a1 = scale2_5(v[2 * k + 1], p);
-            hi[k] = pack_f16x2_5(a0, a1);
-            const float h0 = __half2float(__ushort_as_half(static_cast<unsigned short>(hi[k] & 0xFFFFu)));
-            const float h1 = __half2float(__ushort_as_half(static_cast<unsigned short>(hi[k] >> 16)));
-            lo[k] = pack_f16x2_5(__fsub_rn(a0, h0), __fsub_rn(a1, h1));
-        }
-        uint8_t* tb = btile + g2 * 2048;
-        const int rh = t, rl = t + 8;
-        *reinterpret_cast<uint4*>(tb + rh * 128 + ((c ^ (rh & 7)) << 4)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(tb + rl * 128 + ((c ^ (rl & 7)) << 4)) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
     fence_proxy_async_smem();   // B tiles (generic stores) -> tensor-core reads
     tcf_before();
     __syncthreads();
@@ -341,100 +395,171 @@ __global__ void __launch_bounds__(kThreads5, 1)
         *abort_flag = 1;
         atomicOr(&g_fault_tc5, 1);
     };
-    if (warp < 4) {
-        // decoder for rows 32*warp .. +31
-        const int q = warp;
-        const int r = q * 32 + lane;
-        for (int j = 0; j < ng && !*abort_flag; ++j) {
-            const int s = j / kStageGroups, st = s % kStages5, jj = j % kStageGroups;
-            if (jj == 0 && !mbar_wait(&code_full[st], static_cast<uint32_t>(s / kStages5) & 1u, kWait5)) {
-                fail();
-                break;
-            }
-            const int slot = j % kSlots;
-            if (j >= kSlots &&
-                !mbar_wait(&slot_free[slot], static_cast<uint32_t>(j / kSlots - 1) & 1u, kWait5)) {
-                fail();
-                break;
-            }
-            const uint4 code = *reinterpret_cast<const uint4*>(stages + st * kStageBytes5 + r * 128 +
-                                                               ((jj ^ (r & 7)) << 4));
-            uint32_t a[16];
-            const uint32_t words[4] = {code.x, code.y, code.z, code.w};
+    const int n_batch = (ng + kBatch - 1) / kBatch;
+    const int nrow = min(kRowsT, rows - row0);
+    float corr[kTok];   // groups too far below the row's largest scale, summed exactly
+    // one such group of row r on the CUDA cores: corr[t] += 2^(k-127) sum_e v_e x_te
+    auto far_group = [&](const uint4 code, int k, int j, float (&c)[kTok]) {
+        const uint32_t words[4] = {code.x, code.y, code.z, code.w};
+        float v[32];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t h[4];
-                e2m1x8_to_f16x2x4(words[k], h);
-                a[4 * k] = h[0];
-                a[4 * k + 1] = h[1];
-                a[4 * k + 2] = h[2];
-                a[4 * k + 3] = h[3];
+        for (int kw = 0; kw < 4; ++kw) {
+            uint32_t hh[4];
+            e2m1x8_to_f16x2x4(words[kw], hh);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = f16x2_to_f32x2(hh[e]);
+                v[8 * kw + 2 * e] = f.x;
+                v[8 * kw + 2 * e + 1] = f.y;
             }
-            tmem_st16(tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kSlotCols, a);
+        }
+        const float sk = exp2i5(k - 127);
+        for (int t = 0; t < nbt; ++t) {
+            const float4* xs = reinterpret_cast<const float4*>(
+                X + static_cast<size_t>(t0 + t) * cols + static_cast<size_t>(g_lo + j) * kGroup);
+            float sum = 0.0f;
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 xv = __ldg(xs + e4);
+                sum = __fmaf_rn(v[4 * e4], xv.x, sum);
+                sum = __fmaf_rn(v[4 * e4 + 1], xv.y, sum);
+                sum = __fmaf_rn(v[4 * e4 + 2], xv.z, sum);
+                sum = __fmaf_rn(v[4 * e4 + 3], xv.w, sum);
+            }
+            c[t] = __fmaf_rn(sum, sk, c[t]);
+        }
+    };
+    if (warp < 8) {
+        // decoder: quarter q (rows 32q .. 32q+31), batches h, h+2, h+4, ...
+        const int q = warp & 3, h = warp >> 2;
+        const int r = q * 32 + lane;
+        const int kmax = kref_s[r];
+        for (int t = 0; t < kTok; ++t) corr[t] = 0.0f;
+        for (int b = h; b < n_batch && !*abort_flag; b += 2) {
+            const int s_idx = b / 2, st = s_idx % kStages5;
+            if (!mbar_wait(&code_full[st], static_cast<uint32_t>(s_idx / kStages5) & 1u, kWait5)) {
+                fail();
+                break;
+            }
+            const int slot = b % kSlots;
+            if (b >= kSlots &&
+                !mbar_wait(&a_free[slot], static_cast<uint32_t>(b / kSlots - 1) & 1u, kWait5)) {
+                fail();
+                break;
+            }
+#pragma unroll
+            for (int gg = 0; gg < kBatch; ++gg) {
+                const int j = b * kBatch + gg;
+                if (j < ng) {
+                    const int jj = j % kStageGroups;
+                    const uint4 code = *reinterpret_cast<const uint4*>(
+                        stages + st * kStageBytes5 + r * 128 + ((jj ^ (r & 7)) << 4));
+                    // 2^(k - kmax) as f16: every E2M1 value times it is exact in
+                    // f16 down to k - kmax = -23; a group further below goes to
+                    // the CUDA-core sum instead (and a NaN scale is flagged)
+                    const int k = sc_s[r * L.sc_pitch + j];
+                    const int dd = k == 255 ? -100 : k - kmax;
+                    const uint32_t fb = dd >= -14 ? static_cast<uint32_t>(dd + 15) << 10
+                                        : dd >= -23 ? 1u << (dd + 24)
+                                                    : 0u;
+                    if (dd < -23 && k != 255 && r < nrow)
+                        far_group(code, k, j, corr);
+                    const __half2 f2 = __halves2half2(__ushort_as_half(static_cast<unsigned short>(fb)),
+                                                      __ushort_as_half(static_cast<unsigned short>(fb)));
+                    uint32_t a[16];
+                    const uint32_t words[4] = {code.x, code.y, code.z, code.w};
+#pragma unroll
+                    for (int kw = 0; kw < 4; ++kw) {
+                        uint32_t hh[4];
+                        e2m1x8_to_f16x2x4(words[kw], hh);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __half2 v = *reinterpret_cast<__half2*>(&hh[e]);
+                            v = __hmul2(v, f2);
+                            a[4 * kw + e] = *reinterpret_cast<uint32_t*>(&v);
+                        }
+                    }
+                    tmem_st16(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                         slot * kSlotCols + gg * 16, a);
+                }
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tcf_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive5(&a_full[slot]);
-                if (jj == kStageGroups - 1 || j == ng - 1) mbar_arrive5(&code_free[st]);
+                mbar_arrive5(&code_free[st]);
             }
         }
-    } else if (warp < 8) {
-        // epilogue for rows 32*(warp-4) .. +31
-        const int q = warp - 4;
-        const int r = q * 32 + lane;
-        float acc[kTok];
-#pragma unroll
-        for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
-        for (int j = 0; j < ng && !*abort_flag; ++j) {
-            const int slot = j % kSlots;
-            if (!mbar_wait(&d_full[slot], static_cast<uint32_t>(j / kSlots) & 1u, kWait5)) {
-                fail();
-                break;
-            }
-            tcf_after();
-            uint32_t d[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + slot * kSlotCols + 16, d);
-            tcf_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive5(&slot_free[slot]);
-            const float s = e8m0_to_f32(sc_s[r * L.sc_pitch + j]);
-#pragma unroll
-            for (int t = 0; t < kTok; ++t)
-                acc[t] = __fmaf_rn(s, __fadd_rn(__uint_as_float(d[t]), __uint_as_float(d[t + 8])),
-                                   acc[t]);
-        }
-#pragma unroll
-        for (int t = 0; t < kTok; ++t) part[r * kTok + t] = __fmul_rn(acc[t], exp2i5(-pexp[t]));
     } else if (warp == 8) {
-        // TMA producer: refill each code stage once its 4 decoders are done
+        // TMA producer: refill each code stage once its 8 decoder warps are done
         if (lane == 0) {
-            for (int s = kStages5; s < n_st && !*abort_flag; ++s) {
-                const int st = s % kStages5;
-                if (!mbar_wait(&code_free[st], static_cast<uint32_t>(s / kStages5 - 1) & 1u, kWait5)) {
+            for (int s2 = kStages5; s2 < n_st && !*abort_flag; ++s2) {
+                const int st = s2 % kStages5;
+                if (!mbar_wait(&code_free[st], static_cast<uint32_t>(s2 / kStages5 - 1) & 1u, kWait5)) {
                     fail();
                     break;
                 }
-                issue_stage(s);
+                issue_stage(s2);
             }
         }
     } else {
-        // MMA issuer
+        // MMA issuer: every group's two MMAs accumulate into one tile
         if (lane == 0) {
-            for (int j = 0; j < ng && !*abort_flag; ++j) {
-                const int slot = j % kSlots;
-                if (!mbar_wait(&a_full[slot], static_cast<uint32_t>(j / kSlots) & 1u, kWait5)) {
+            const uint64_t bdesc0 = sw128_desc5(smem_u32(btile));
+            for (int b = 0; b < n_batch && !*abort_flag; ++b) {
+                const int slot = b % kSlots;
+                if (!mbar_wait(&a_full[slot], static_cast<uint32_t>(b / kSlots) & 1u, kWait5)) {
                     fail();
                     break;
                 }
                 tcf_after();
-                const uint32_t bbase = smem_u32(btile + (j >> 1) * 2048) + (j & 1) * 64;
-                const uint32_t a_col = tmem + slot * kSlotCols;
-                const uint32_t d_col = a_col + 16;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    umma_ts(d_col, a_col + kk * 8, sw128_desc5(bbase + kk * 32), kk);
-                umma_commit5(&d_full[slot]);
+                for (int gg = 0; gg < kBatch; ++gg) {
+                    const int j = b * kBatch + gg;
+                    if (j >= ng) break;
+                    // B: group j's 64 bytes in its pair tile, K halves 32 bytes apart
+                    const uint64_t bd =
+                        bdesc0 + static_cast<uint64_t>(((j >> 1) * 2048 + (j & 1) * 64) >> 4);
+                    const uint32_t a_col = tmem + slot * kSlotCols + gg * 16;
+                    umma_ts(tmem + kDCol, a_col, bd, j > 0 ? 1u : 0u);
+                    umma_ts(tmem + kDCol, a_col + 8, bd + 2, 1u);
+                }
+                umma_commit5(&a_free[slot]);
+                if (b == n_batch - 1) umma_commit5(done_bar);
             }
+        }
+    }
+    if (warp >= 4 && warp < 8) {   // second decoder of each row hands over its sum
+        const int r = (warp & 3) * 32 + lane;
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) part[r * kTok + t] = corr[t];
+    }
+    tcf_before();
+    __syncthreads();
+
+    // --- epilogue: the accumulator, once, scaled back
+    if (warp < 4) {
+        const int q = warp;
+        const int r = q * 32 + lane;
+        bool ok = !*abort_flag && (n_batch == 0 || mbar_wait(done_bar, 0u, kWait5));
+        uint32_t d[16];
+        if (ok) {
+            tcf_after();
+            if (n_batch > 0) tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + kDCol, d);
+        } else {
+            fail();
+        }
+        const int kr = static_cast<int>(kref_s[r]) - 127;
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+            float v = 0.0f;
+            if (n_batch > 0)
+                v = scale2_5(__fadd_rn(__uint_as_float(d[t]), __uint_as_float(d[t + 8])),
+                             kr - pexp[t]);
+            v = __fadd_rn(v, __fadd_rn(corr[t], part[r * kTok + t]));
+            if (nan_s[r]) v = __uint_as_float(0x7FC00000u);
+            part[r * kTok + t] = v;
         }
     }
     tcf_before();
@@ -485,7 +610,7 @@ cudaError_t launch5(const uint8_t* w, int rows, int cols, const float* X, int nb
     const int gpr = cols / kGroup;
     const int max_ng = (gpr + CL - 1) / CL;
     const T5Layout l = t5_layout(max_ng);
-    if (l.total > 227 * 1024) return cudaErrorNotSupported;
+    if (l.total > 227 * 1024 || max_ng > kMaxGroups5) return cudaErrorNotSupported;
     auto fn = encode_fn5();
     if (fn == nullptr) return cudaErrorNotSupported;
     CUtensorMap map;

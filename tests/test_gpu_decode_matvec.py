@@ -169,6 +169,28 @@ def test_mm_wide_dynamic_range_activations(mx, nb):
     assert_within(Y, ref, l1, REL_FP32, f"wide range nb={nb}")
 
 
+@pytest.mark.parametrize("nb", [1, 8, 11])
+def test_mm_wide_weight_scales(mx, nb):
+    # scale bytes over 0..240 inside every row, rows whose largest-scale group
+    # holds only zero codes, and rows with one NaN group: the tensor-core path
+    # folds each group's scale into its f16 weights relative to the row's
+    # largest scale byte, so groups far below it must still count in full
+    rows, cols = 300, 2048
+    rng = np.random.default_rng(500 + nb)
+    codes, scales = random_case(rng, rows, cols, lo=0, hi=240)
+    scales[:60] = rng.integers(90, 110, size=(60, cols // 32))
+    scales[:60, 5] = 240
+    codes[:60, 160:192] = rng.choice([0, 8], size=(60, 32))   # zero codes in group 5
+    scales[100, 17] = 255
+    buf = encode(codes, scales)
+    X = synth.normal_f32(600 + nb, nb * cols).reshape(nb, cols)
+    ref, l1 = oracle.matmat(buf, rows, cols, X, nb)
+    for fn in ("mxfp4_mm", "mxfp4_mm_fp32"):
+        Y = run_mm(mx, buf, rows, cols, X, nb, fn)
+        assert np.isnan(Y[:, 100]).all()
+        assert_within(Y, ref, l1, REL_FP32, f"wide weight scales nb={nb} {fn}")
+
+
 @pytest.mark.parametrize("rows,cols,nb", [(50, 544, 3), (33, 32, 8), (17, 160, 2), (131, 2880, 8),
                                           (64, 96, 1)])
 def test_mm_ragged_shapes(mx, rows, cols, nb):
