@@ -146,7 +146,7 @@ class DecodeGemv(Workload):
         self.bytes_per_launch = mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
         self.bytes_per_step = layers * self.bytes_per_launch
         self.units_per_step = self.bytes_per_step
-        self.dominant = "mxfp4_mv (k_matmat<4,1>)"
+        self.dominant = "mxfp4_mv (k_mv_tc<1,1>: mma.sync, split-f16 activations)"
 
     def step(self):
         for w, y in zip(self.ws, self.ys):

@@ -22,6 +22,12 @@ cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float
 cudaError_t launch_mm_tc5(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
                           cudaStream_t s);
 
+// mma.sync product for up to 4 tokens per pass over the weights (split-f16
+// activations, per-group FP32 scaling); cudaErrorNotSupported, with nothing
+// launched, for shapes it cannot take.  Per token the same arithmetic for any nb.
+cudaError_t launch_mv_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                         cudaStream_t s);
+
 // mma.sync small-batch product (split-f16 activations, FP32 accumulate);
 // cudaErrorNotSupported, with nothing launched, for shapes it cannot take.
 cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
@@ -51,6 +57,7 @@ cudaError_t read_fault_matvec(int* value, bool reset);
 cudaError_t read_fault_mma(int* value, bool reset);
 cudaError_t read_fault_prefill(int* value, bool reset);
 cudaError_t read_fault_tc5(int* value, bool reset);
+cudaError_t read_fault_mvtc(int* value, bool reset);
 
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);

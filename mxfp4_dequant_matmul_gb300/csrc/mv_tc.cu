@@ -1,0 +1,582 @@
+// mv_tc.cu -- MXFP4 matvec and products with up to four tokens per pass, the
+// dot products on the tensor cores through mma.sync (sm_103a).
+//
+// Y[t*rows + r] = sum_c W[r][c] X[t][c]  ("cortiq-engine 0.8.40
+// src/gpu_wgpu/mxfp4.rs", PEROP kernels mxfp4_mv and mxfp4_mm).
+//
+// Why the tensor cores for a matvec: at the HBM rate an SM must take in about
+// 44 weight elements per clock, and decoding to FP32 and multiplying on the
+// FP32 pipe costs about three instructions per element, more than the four
+// issue slots per clock of an SM can give.  Here the E2M1 codes go through the
+// hardware pair conversion to f16 (exact) and straight into the A operand of
+// mma.sync m16n8k16; the activations are the B operand, each token's x split
+// into f16 halves hi = f16(x 2^p) and lo = f16(x 2^p - hi) (p one power of two
+// per token and K-slice, putting the slice's largest |x| in [2^14, 2^15)).
+// Column 2n of B is token n's hi, column 2n + 1 its lo, so one MMA serves four
+// tokens.  Every product of an E2M1 value with an f16 is exact in the FP32
+// accumulator.  Each group (32 elements) is two MMAs per 16 rows into a fresh
+// accumulator; hi + lo is taken back by 2^-p and multiplied by the group's
+// scale in FP32, and the result is added to the row's FP32 sum: any scale byte
+// is handled exactly (255 gives NaN) and no partial sum overflows unless the
+// result does.
+//
+// Register layout: lane (g = lane / 4, t = lane % 4) reads code word t of rows
+// g and g + 8 of a group; the four f16 pairs of that word are the A registers
+// of the group's two MMAs (pairs 0, 1 for the first, 2, 3 for the second), and
+// the B registers of lane (2n + h, t) are the same eight elements of token n's
+// hi (h = 0) or lo (h = 1).  Nothing moves between lanes.
+//
+// Data movement: a unit is 32 rows x 8 groups (32 rows x 128 code bytes), one
+// TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) into a ring of two
+// to four stages per warp (as deep as shared memory allows).  A CTA owns up to 128 rows; its warps split them into 32-row
+// units and the K range into equal chunk ranges, each warp keeping its rows'
+// sums in registers over its chunks.  The partial sums are added in chunk
+// order.  When the activations of a whole row do not fit in shared memory, a
+// cluster of CTAs splits the groups and adds its partial sums in rank order
+// through distributed shared memory.  The order of every sum depends on the
+// shape only, so results are deterministic and a token's result does not
+// depend on the other tokens of its batch.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxk {
+namespace {
+
+constexpr int kWarpsM = 16;
+constexpr int kThreadsM = kWarpsM * 32;
+constexpr int kRowsU = 32;                  // rows per unit (two MMA row blocks)
+constexpr int kChunkM = 8;                  // groups per unit (128 code bytes per row)
+constexpr int kStageM = kRowsU * 128;       // one TMA tile, 4 KB
+constexpr int kMinStagesM = 2;              // ring stages per warp (more when they fit)
+constexpr int kMaxStagesM = 4;
+constexpr uint32_t kSmemMaxM = 227 * 1024;
+constexpr int kMaxRuCta = 4;                // 32-row units per CTA
+constexpr uint32_t kWaitM = 1u << 22;
+
+// Groups per CTA slice (the B fragments take 128 * NT bytes per group).  The
+// same for every NT, so that the split of the groups, hence the order of every
+// sum, does not depend on the number of tokens.
+constexpr int kGMax = 128;
+
+__device__ int g_fault_mvtc;   // set when a bounded wait gives up
+
+__device__ __forceinline__ uint32_t cluster_rank_m() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_m() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_m(const void* p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float exp2i_m(int e) {
+    if (e >= -126 && e <= 127) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    if (e > 127) return __uint_as_float(0x7F800000u);
+    if (e >= -149) return __uint_as_float(1u << (e + 149));
+    return 0.0f;
+}
+
+// Two floats -> f16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2_m(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Shared memory (offsets from a 1024-byte aligned base).
+struct MvLayout {
+    uint32_t lut, xf, sc, sc_pitch, part, fin, misc, bars, ring, total;
+};
+__host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, int stages) {
+    MvLayout l;
+    l.lut = 0;                                                        // [256] f32
+    l.xf = 1024;                                                      // [ng][8 NT] uint4
+    l.sc = l.xf + static_cast<uint32_t>(ng_max) * 128 * NT;           // [rows][pitch] u8
+    l.sc_pitch = (static_cast<uint32_t>(ng_max) + 15u) & ~15u;
+    l.part = l.sc + static_cast<uint32_t>(ru_cta) * kRowsU * l.sc_pitch;   // [warps][32][NT]
+    l.part = (l.part + 15u) & ~15u;
+    l.fin = l.part + kWarpsM * kRowsU * NT * 4;                        // [rows][NT]
+    l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[4], tmax[4]
+    l.bars = (l.misc + 64 + 7u) & ~7u;
+    l.ring = (l.bars + kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
+    l.total = l.ring + static_cast<uint32_t>(kWarpsM * stages) * kStageM + 1024;   // + align slack
+    return l;
+}
+
+template <int NT, int CL>
+__global__ void __launch_bounds__(kThreadsM, 1)
+    k_mv_tc(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ w, int rows,
+            int cols, const float* __restrict__ X, int nb, float* __restrict__ Y, int ru_cta,
+            int ng_max, int stages) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const MvLayout L = mv_layout(NT, ng_max, ru_cta, stages);
+    float* lut = reinterpret_cast<float*>(smem + L.lut);
+    uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
+    uint8_t* sc_s = smem + L.sc;
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* fin = reinterpret_cast<float*>(smem + L.fin);
+    int* pexp = reinterpret_cast<int*>(smem + L.misc);                 // [4]
+    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);  // [4]
+    int* not_plain = reinterpret_cast<int*>(smem + L.misc + 32);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t rank = CL > 1 ? cluster_rank_m() : 0u;
+    const int range = blockIdx.x / CL;
+    const int t0 = blockIdx.y * NT;
+    const int nbt = min(NT, nb - t0);
+    const int gpr = cols / kGroup;
+    const int g_lo = static_cast<int>(static_cast<long>(rank) * gpr / CL);
+    const int g_hi = static_cast<int>(static_cast<long>(rank + 1) * gpr / CL);
+    const int ng = g_hi - g_lo;                          // >= 1 (CL <= gpr)
+    const int n_c = (ng + kChunkM - 1) / kChunkM;
+    const int n_ru_all = (rows + kRowsU - 1) / kRowsU;
+    const int ru0 = range * ru_cta;
+    const int n_ru = min(ru_cta, n_ru_all - ru0);        // >= 1 by the grid size
+    const int row0 = ru0 * kRowsU;
+    const size_t plane = static_cast<size_t>(rows) * cols / 2;
+
+    // warp -> (row unit, chunk range): n_ru x WK warps, each over n_c / WK chunks
+    const int WK = min(n_c, kWarpsM / n_ru);
+    const bool active = warp < n_ru * WK;
+    const int my_ru = warp % n_ru, kk = warp / n_ru;
+    const int c_lo = active ? kk * n_c / WK : 0;
+    const int c_hi = active ? (kk + 1) * n_c / WK : 0;
+    const int n_units = c_hi - c_lo;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * stages;
+    uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * stages * kStageM;
+    const uint64_t policy = l2_evict_first();
+    auto issue = [&](int k, int st) {   // unit k of this warp into stage st (lane 0)
+        const int x = (g_lo + (c_lo + k) * kChunkM) * kGroupBytes;
+        const int y = row0 + my_ru * kRowsU;
+        mbar_arrive_expect_tx(&bars[st], kStageM);
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(ring + st * kStageM)),
+            "l"(&tmap), "r"(x), "r"(y), "r"(smem_u32(&bars[st])), "l"(policy)
+            : "memory");
+    };
+    if (tid < NT) tmax[tid] = 0u;
+    if (tid == 0) *not_plain = 0;
+
+    // --- prologue: E8M0 table, scale bytes, activations
+    const int nrow = min(n_ru * kRowsU, rows - row0);
+    const int nch_row = (ng + 30) / 16;   // 16-byte words covering ng bytes at any alignment
+    constexpr int kScU = (kMaxRuCta * kRowsU * ((kGMax + 30) / 16) + kThreadsM - 1) / kThreadsM;
+    uint4 sv[kScU];
+#pragma unroll
+    for (int u = 0; u < kScU; ++u) {
+        const int i = tid + u * kThreadsM;
+        const int r = i / nch_row, c = i - r * nch_row;
+        sv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nrow) {
+            const size_t s0 = plane + static_cast<size_t>(row0 + r) * gpr + g_lo;
+            const size_t addr = (s0 & ~static_cast<size_t>(15)) + 16 * static_cast<size_t>(c);
+            if (addr < s0 + ng) sv[u] = ldg_stream(reinterpret_cast<const uint4*>(w + addr));
+        }
+    }
+    // activation items: (token, group, word) = 8 elements
+    constexpr int kXU = (NT * kGMax * 4 + kThreadsM - 1) / kThreadsM;
+    const int n_items = NT * ng * 4;
+    float xv[kXU][8];
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+        const int i = tid + u * kThreadsM;
+        const int tok = i / (ng * 4), rem = i - tok * ng * 4;
+        if (i < n_items && tok < nbt) {
+            const float4* src = reinterpret_cast<const float4*>(
+                X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
+                8 * rem);
+            const float4 a = __ldg(src), b = __ldg(src + 1);
+            xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+            xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
+        }
+    }
+    // the weights stream after the prologue's own loads, which would otherwise
+    // wait behind them in the memory system
+    if (lane == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+        for (int k = 0; k < stages && k < n_units; ++k) issue(k, k);
+    }
+    if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
+    __syncthreads();   // tmax is zero before any atomic below
+    // "plain" scales: no byte 0 or 255 and none above kPlainMax, so that 2^(k-127)
+    // is the float with bits k << 23 and the rows' sums can stay in the 2^p
+    // domain without overflow (|sum| < 128*32 * 6 * 2^(kPlainMax-127) * 2^15)
+    constexpr uint32_t kPlainMax = 200u;
+    bool odd = false;
+#pragma unroll
+    for (int u = 0; u < kScU; ++u) {
+        const int i = tid + u * kThreadsM;
+        const int r = i / nch_row, c = i - r * nch_row;
+        if (r < nrow) {
+            const int mis =
+                static_cast<int>((plane + static_cast<size_t>(row0 + r) * gpr + g_lo) & 15);
+            const int off = 16 * c - mis;   // row position of the word's byte 0
+            const uint32_t wv[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+            if (mis == 0 && off + 16 <= ng) {   // the whole word lies in the row: one store
+                *reinterpret_cast<uint4*>(sc_s + r * L.sc_pitch + off) = sv[u];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    odd |= (__vcmpeq4(wv[q], 0u) | __vcmpgtu4(wv[q], kPlainMax * 0x01010101u)) != 0u;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = off + k;
+                    const uint32_t b = (wv[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+                    if (j >= 0 && j < ng) {
+                        sc_s[r * L.sc_pitch + j] = static_cast<uint8_t>(b);
+                        odd |= b == 0u || b > kPlainMax;
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+        const int i = tid + u * kThreadsM;
+        const int tok = min(i / (ng * 4), NT - 1);
+        float m = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float a = fabsf(xv[u][e]);
+            m = fmaxf(m, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
+        }
+        // lanes of a token reduce together; one atomic per token and warp
+        const unsigned same = __match_any_sync(0xffffffffu, tok);
+        const unsigned mb = __reduce_max_sync(same, __float_as_uint(m));
+        if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
+    }
+    if (__any_sync(0xffffffffu, odd) && lane == 0) atomicOr(not_plain, 1);
+    __syncthreads();
+    if (tid < NT) {
+        const float m = __uint_as_float(tmax[tid]);
+        // puts the largest |x| in [2^14, 2^15); capped so 2^-p stays normal
+        pexp[tid] = m > 0.0f ? min(14 - ilogbf(m), 126) : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+        const int i = tid + u * kThreadsM;
+        if (i < n_items) {
+            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
+            const int j = rem >> 2, tw = rem & 3;
+            const float pm = exp2i_m(pexp[tok]);   // 2^p is a normal float
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a0 = __fmul_rn(xv[u][2 * k], pm), a1 = __fmul_rn(xv[u][2 * k + 1], pm);
+                hi[k] = pack_f16x2_m(a0, a1);
+                const float2 h = f16x2_to_f32x2(hi[k]);
+                lo[k] = pack_f16x2_m(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
+            }
+            xf[j * (8 * NT) + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            xf[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    }
+    __syncthreads();
+
+    // --- this warp's units
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24 of the unit, token t
+    // hi + lo of a group carries the factor 2^p: undone before the scale, so
+    // that no partial sum leaves the float range unless the result does
+    const int p_t = pexp[t < NT ? t : 0];
+    const float pinv = exp2i_m(-p_t);
+    // the 2^p domain is kept only when it is not below the true one (p >= 0,
+    // the token's |x| below 2^15), so that it adds no underflow either
+    const bool plain = *not_plain == 0 && p_t >= 0;
+    bool failed = false;
+    int k = 0;
+    const uint8_t* scr = sc_s + static_cast<size_t>(my_ru * kRowsU + g) * L.sc_pitch;
+    for (; k < n_units; ++k) {
+        const int st = k % stages;
+        if (!mbar_wait(&bars[st], static_cast<uint32_t>(k / stages) & 1u, kWaitM)) {
+            failed = true;
+            break;
+        }
+        const uint8_t* stg = ring + st * kStageM;
+        const int gc0 = (c_lo + k) * kChunkM;   // first group of the unit in the slice
+        const int ngc = min(kChunkM, ng - gc0);
+        uint2 sb[4];   // the unit's 8 scale bytes of rows g, g+8, g+16, g+24
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            sb[q] = *reinterpret_cast<const uint2*>(scr + q * 8 * L.sc_pitch + gc0);
+#pragma unroll
+        for (int j = 0; j < kChunkM; ++j) {
+            if (j < ngc) {
+                // 128-byte swizzle: chunk j of row r sits at chunk j ^ (r & 7), r & 7 = g
+                const uint8_t* cw = stg + g * 128 + (((j ^ g) & 7) << 4) + t * 4;
+                uint32_t h0[4], h1[4], h2[4], h3[4];
+                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw), h0);
+                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 1024), h1);
+                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 2048), h2);
+                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 3072), h3);
+                uint4 b = make_uint4(0u, 0u, 0u, 0u);
+                if (lane < 8 * NT) b = xf[(gc0 + j) * (8 * NT) + lane];
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                mma16816(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                mma16816(d0, h0[2], h1[2], h0[3], h1[3], b.z, b.w);
+                mma16816(d1, h2[2], h3[2], h2[3], h3[3], b.z, b.w);
+                const int sh = 8 * (j & 3);
+                const uint32_t w0 = j < 4 ? sb[0].x : sb[0].y, w1 = j < 4 ? sb[1].x : sb[1].y;
+                const uint32_t w2 = j < 4 ? sb[2].x : sb[2].y, w3 = j < 4 ? sb[3].x : sb[3].y;
+                float v0 = __fadd_rn(d0[0], d0[1]), v1 = __fadd_rn(d0[2], d0[3]);
+                float v2 = __fadd_rn(d1[0], d1[1]), v3 = __fadd_rn(d1[2], d1[3]);
+                if (plain) {   // the sums stay in the 2^p domain; 2^(k-127) from its bits
+                    const uint32_t m8 = 0xFFu << 23;
+                    const int s23 = 23 - sh;
+                    acc[0] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w0 << s23 : w0 >> -s23) & m8), v0, acc[0]);
+                    acc[1] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w1 << s23 : w1 >> -s23) & m8), v1, acc[1]);
+                    acc[2] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w2 << s23 : w2 >> -s23) & m8), v2, acc[2]);
+                    acc[3] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w3 << s23 : w3 >> -s23) & m8), v3, acc[3]);
+                } else {       // any byte: the table, and 2^-p applied first
+                    acc[0] = __fmaf_rn(lut[(w0 >> sh) & 0xFFu], __fmul_rn(v0, pinv), acc[0]);
+                    acc[1] = __fmaf_rn(lut[(w1 >> sh) & 0xFFu], __fmul_rn(v1, pinv), acc[1]);
+                    acc[2] = __fmaf_rn(lut[(w2 >> sh) & 0xFFu], __fmul_rn(v2, pinv), acc[2]);
+                    acc[3] = __fmaf_rn(lut[(w3 >> sh) & 0xFFu], __fmul_rn(v3, pinv), acc[3]);
+                }
+            }
+        }
+        __syncwarp();   // every lane is done with the stage
+        if (lane == 0 && k + stages < n_units) {
+            fence_proxy_async_smem();
+            issue(k + stages, st);
+        }
+    }
+    if (failed) {
+        if (lane == 0) atomicOr(&g_fault_mvtc, 1);
+        // let this warp's copies in flight land before the CTA can exit
+        for (int kq = k; kq < k + stages && kq < n_units; ++kq)
+            mbar_wait(&bars[kq % stages], static_cast<uint32_t>(kq / stages) & 1u, kWaitM);
+    }
+    if (plain) {   // back from the 2^p domain (exact: a power of two, no overflow)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = __fmul_rn(acc[q], pinv);
+    }
+    if (active && t < NT) {   // D columns 2t, 2t+1 are token t's hi and lo
+        float* pw = part + static_cast<size_t>(warp) * kRowsU * NT;
+        pw[g * NT + t] = acc[0];
+        pw[(g + 8) * NT + t] = acc[1];
+        pw[(g + 16) * NT + t] = acc[2];
+        pw[(g + 24) * NT + t] = acc[3];
+    }
+    __syncthreads();
+
+    // --- add the chunk ranges in order (warp kk * n_ru + ru)
+    for (int i = tid; i < n_ru * kRowsU * NT; i += kThreadsM) {
+        const int ru = i / (kRowsU * NT), rem = i - ru * kRowsU * NT;
+        float s = part[static_cast<size_t>(ru) * kRowsU * NT + rem];
+        for (int q = 1; q < WK; ++q)
+            s = __fadd_rn(s, part[static_cast<size_t>(q * n_ru + ru) * kRowsU * NT + rem]);
+        const int tok = rem % NT;
+        if (CL == 1) {
+            const int row = row0 + ru * kRowsU + rem / NT;
+            if (row < rows && tok < nbt) Y[static_cast<size_t>(t0 + tok) * rows + row] = s;
+        } else {
+            fin[i] = s;
+        }
+    }
+    if (CL > 1) {
+        // --- add over the cluster's CTAs in rank order; CTA k writes its share of rows
+        cluster_sync_m();
+        const int nr = n_ru * kRowsU;
+        const int r_lo = static_cast<int>(rank) * nr / CL;
+        const int r_hi = static_cast<int>(rank + 1) * nr / CL;
+        for (int i = r_lo * NT + tid; i < r_hi * NT; i += kThreadsM) {
+            float s = ld_cluster_m(fin + i, 0);
+            for (uint32_t q = 1; q < static_cast<uint32_t>(CL); ++q)
+                s = __fadd_rn(s, ld_cluster_m(fin + i, q));
+            const int row = row0 + i / NT, tok = i % NT;
+            if (row < rows && tok < nbt) Y[static_cast<size_t>(t0 + tok) * rows + row] = s;
+        }
+        cluster_sync_m();   // no CTA leaves while another still reads its sums
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_m() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int sm_count_m() {
+    static std::once_flag once;
+    static int n = 0;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    });
+    return n > 0 ? n : 1;
+}
+
+// CTAs (CL = 1) or clusters that one wave holds, probed with the largest
+// layout (four tokens) for every NT, so that the row split does not depend on
+// the number of tokens either.
+template <int CL>
+int resident_mv() {
+    static std::once_flag once;
+    static int resident = 0;
+    std::call_once(once, [] {
+        const MvLayout lmax = mv_layout(4, kGMax, kMaxRuCta, kMinStagesM);
+        auto k4 = k_mv_tc<4, CL>;
+        if (cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemMaxM)) != cudaSuccess)
+            return;
+        if (CL == 1) {
+            resident = sm_count_m();
+            return;
+        }
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(CL * 64, 1);
+        q.blockDim = dim3(kThreadsM);
+        q.dynamicSmemBytes = lmax.total;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = CL;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        q.attrs = a;
+        q.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, k4, &q) == cudaSuccess && nc > 0) resident = nc;
+    });
+    return resident;
+}
+
+template <int NT, int CL>
+cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                      cudaStream_t s) {
+    const int gpr = cols / kGroup;
+    const int ng_max = (gpr + CL - 1) / CL;
+    auto kernel = k_mv_tc<NT, CL>;
+    const int resident = resident_mv<CL>();
+    if (resident < 1) return cudaErrorNotSupported;
+    {
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [&] {
+            attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemMaxM));
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+    }
+    const int n_ru_all = (rows + kRowsU - 1) / kRowsU;
+    int ru_cta = (n_ru_all + resident - 1) / resident;
+    ru_cta = ru_cta < 1 ? 1 : (ru_cta > kMaxRuCta ? kMaxRuCta : ru_cta);
+    const int n_ranges = (n_ru_all + ru_cta - 1) / ru_cta;
+    // as many ring stages as the shared memory holds (deeper rings keep more
+    // weight bytes in flight; the arithmetic does not depend on the depth)
+    const uint32_t fixed = mv_layout(NT, ng_max, ru_cta, 0).total;
+    int stages = fixed < kSmemMaxM
+                     ? static_cast<int>((kSmemMaxM - fixed) / (kWarpsM * kStageM)) : 0;
+    stages = stages > kMaxStagesM ? kMaxStagesM : stages;
+    if (stages < kMinStagesM) return cudaErrorNotSupported;
+    const MvLayout l = mv_layout(NT, ng_max, ru_cta, stages);
+    auto fn = encode_fn_m();
+    if (fn == nullptr) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols) / 2, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) / 2};
+    const cuuint32_t box[2] = {128, kRowsU};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ranges * CL),
+                       static_cast<unsigned>((nb + NT - 1) / NT));
+    cfg.blockDim = dim3(kThreadsM);
+    cfg.dynamicSmemBytes = l.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, kernel, map, w, rows, cols, X, nb, Y, ru_cta, ng_max, stages);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t launch_mv_nt(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                         cudaStream_t s) {
+    const int gpr = cols / kGroup;
+    switch ((gpr + kGMax - 1) / kGMax) {
+        case 1: return launch_mv<NT, 1>(w, rows, cols, X, nb, Y, s);
+        case 2: return launch_mv<NT, 2>(w, rows, cols, X, nb, Y, s);
+        case 3: return launch_mv<NT, 3>(w, rows, cols, X, nb, Y, s);
+        case 4: return launch_mv<NT, 4>(w, rows, cols, X, nb, Y, s);
+        case 5:
+        case 6: return launch_mv<NT, 6>(w, rows, cols, X, nb, Y, s);
+        case 7:
+        case 8: return launch_mv<NT, 8>(w, rows, cols, X, nb, Y, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+// Tensor-core product, up to 4 tokens per pass over the weights (passes along
+// the grid's y); cudaErrorNotSupported, with nothing launched, for shapes it
+// cannot take.  A token's arithmetic is the same whatever nb is.
+cudaError_t launch_mv_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
+                         cudaStream_t s) {
+    if (nb <= 1) return launch_mv_nt<1>(w, rows, cols, X, nb, Y, s);
+    if (nb == 2) return launch_mv_nt<2>(w, rows, cols, X, nb, Y, s);
+    return launch_mv_nt<4>(w, rows, cols, X, nb, Y, s);
+}
+
+cudaError_t read_fault_mvtc(int* value, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_mvtc, sizeof(int));
+    if (e != cudaSuccess || !reset) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_fault_mvtc, &zero, sizeof(int));
+}
+
+}  // namespace mxk

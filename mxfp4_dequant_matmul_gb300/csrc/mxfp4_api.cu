@@ -74,13 +74,14 @@ int mxfp4_version(void) { return 100; }
 
 int mxfp4_device_faults(int* faults, int reset) {
     if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
-    int a = 0, b = 0, c = 0, d = 0;
+    int a = 0, b = 0, c = 0, d = 0, f = 0;
     cudaError_t e = mxk::read_fault_matvec(&a, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_mma(&b, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_prefill(&c, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_tc5(&d, reset != 0);
+    if (e == cudaSuccess) e = mxk::read_fault_mvtc(&f, reset != 0);
     if (e != cudaSuccess) return from_cuda(e);
-    *faults = a | (b << 1) | (c << 2) | (d << 3);
+    *faults = a | (b << 1) | (c << 2) | (d << 3) | (f << 4);
     return MXFP4_STATUS_OK;
 }
 
@@ -98,6 +99,9 @@ int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t st
 
 int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y, cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, x, 1, y));
+    cudaError_t e = mxk::launch_mv_tc(u8(w), rows, cols, x, 1, y, stream);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+    (void)cudaGetLastError();
     return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, x, 1, y, stream));
 }
 
@@ -117,7 +121,7 @@ int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y
              cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
     if (nb <= MXFP4_MM_SMALL_MAX) {
-        cudaError_t e = mxk::launch_mm_tc5(u8(w), rows, cols, X, nb, Y, stream);
+        cudaError_t e = mxk::launch_mv_tc(u8(w), rows, cols, X, nb, Y, stream);
         if (e != cudaErrorNotSupported) return from_cuda(e);
         (void)cudaGetLastError();
         e = mxk::launch_mm_tc(u8(w), rows, cols, X, nb, Y, stream);

@@ -136,12 +136,13 @@ def test_page_shapes_mv_and_batches_equal_per_token(mx, rows, cols):
         assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} batch {b}")
         assert_within(Y32, ref, l1, REL_FP32, f"{rows}x{cols} batch {b} (FP32 path)")
         for t in range(b):
-            # the FP32 batch path equals the matvec bit for bit, and a token's
-            # result from mxfp4_mm does not depend on the rest of its batch
+            # per token, each batch path equals its own matvec bit for bit: the
+            # FP32 path with nb = 1, and mxfp4_mm (whatever the rest of its
+            # batch) equals mxfp4_mv
+            one32 = run_mm(mx, w_h, rows, cols, X[t:t + 1], 1, "mxfp4_mm_fp32")
+            assert_bits_equal(Y32[t], one32[0], f"FP32 batch {b} token {t} vs its matvec")
             one = run_mv(mx, w_h, rows, cols, X[t])
-            assert_bits_equal(Y32[t], one, f"FP32 batch {b} token {t} vs its matvec")
-            alone = run_mm(mx, w_h, rows, cols, X[t:t + 1], 1)
-            assert_bits_equal(Y[t], alone[0], f"batch {b} token {t} vs the token alone")
+            assert_bits_equal(Y[t], one, f"batch {b} token {t} vs its matvec")
 
 
 def test_mm8_config_every_output(mx):
