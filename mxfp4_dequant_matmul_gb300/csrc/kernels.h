@@ -52,12 +52,25 @@ cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden,
                             const float* route_w, float* y, void* ws, cudaStream_t s);
 cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 
+// Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu;
+// cudaErrorNotSupported, with nothing launched, for shapes they cannot take.
+cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
+                                  int n_experts, int inter, int hidden, int top_k, const float* x,
+                                  const int32_t* hdr, const int32_t* offsets,
+                                  const int32_t* touched, const int32_t* pair_of, float* act,
+                                  cudaStream_t s);
+cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
+                               int inter, const float* act, const int32_t* hdr,
+                               const int32_t* offsets, const int32_t* touched,
+                               const int32_t* pair_of, float* o_pairs, cudaStream_t s);
+
 // Device fault words (set when a bounded wait gives up); read and optionally clear.
 cudaError_t read_fault_matvec(int* value, bool reset);
 cudaError_t read_fault_mma(int* value, bool reset);
 cudaError_t read_fault_prefill(int* value, bool reset);
 cudaError_t read_fault_tc5(int* value, bool reset);
 cudaError_t read_fault_mvtc(int* value, bool reset);
+cudaError_t read_fault_moetc(int* value, bool reset);
 
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);

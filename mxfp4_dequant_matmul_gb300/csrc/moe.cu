@@ -16,8 +16,8 @@
 //
 // Pipeline (all stream-ordered, no inter-CTA waits):
 //   k_moe_plan      one CTA: counts, offsets, touched-expert list, pair lists
-//   k_moe_gate_up   persistent CTAs over (touched expert, row block) units
-//   k_moe_down      same units over the down matrices -> per-pair outputs
+//   gate/up pass    k_moe_tc<2> (moe_tc.cu, tensor cores), else k_moe_pass
+//   down pass       k_moe_tc<1>, else k_moe_pass -> per-pair outputs
 //   k_moe_combine   y[t] = sum_j w[t,j] * o[t*top_k + j], slots in order
 #include <mutex>
 
@@ -265,6 +265,10 @@ cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t stride = padded_nbytes(inter, hidden);
+    e = launch_moe_tc_gate_up(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k, x,
+                              plan.hdr, plan.offsets, plan.touched, plan.pair_of, act, s);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
     return launch_pass<Pass::kGateUp>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k,
                                       x, plan, act, s);
 }
@@ -275,8 +279,13 @@ cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden,
     const int n_pairs = n_tokens * top_k;
     const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
     const size_t stride = padded_nbytes(hidden, inter);
-    cudaError_t e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_experts, hidden, inter,
-                                             top_k, act, plan, plan.o_pairs, s);
+    cudaError_t e = launch_moe_tc_down(down_bank, stride, n_experts, hidden, inter, act, plan.hdr,
+                                       plan.offsets, plan.touched, plan.pair_of, plan.o_pairs, s);
+    if (e == cudaErrorNotSupported) {
+        (void)cudaGetLastError();
+        e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_experts, hidden, inter, top_k,
+                                     act, plan, plan.o_pairs, s);
+    }
     if (e != cudaSuccess) return e;
     const size_t n = static_cast<size_t>(n_tokens) * hidden;
     const unsigned blocks = static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);

@@ -1,0 +1,474 @@
+// moe_tc.cu -- routed-expert passes on the tensor cores through mma.sync
+// (sm_103a): act = SiLU(gate_e x) * (up_e x) for every routed pair, and
+// o = down_e act ("cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs" kernels
+// dsv4_global_gate_up_mxfp4 and dsv4_global_down_mxfp4), grouped by expert as
+// "rlx-cpu 0.2.17 src/gguf_matmul.rs" grouped_moe_sort_plan groups them.
+//
+// The arithmetic of a product is the one of mv_tc.cu: E2M1 codes through the
+// hardware pair conversion into the A operand of mma.sync m16n8k16, each
+// pair's vector split into f16 hi and lo (one power of two per pair putting
+// its largest |x| in [2^14, 2^15)) in the B columns 2n and 2n + 1, two MMAs per
+// group and 16 rows into a fresh accumulator, then 2^-p and the group's scale
+// in FP32 and the FP32 row sum.
+//
+// Work: a segment is (touched expert, up to four of its pairs, 128 rows of its
+// matrices); the segments of all touched experts are dealt to persistent CTAs
+// in turn.  For each segment a CTA copies the 128 rows' scale bytes with one
+// bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
+// (matrix, 32-row unit, chunk range) units of 32 rows x 8 groups through
+// per-warp rings of TMA tile loads (a 3-D tensor map over the bank: bytes,
+// rows, experts).  Partial sums are added in chunk order; the gate/up pass
+// applies SiLU(g) * u and writes act[pair][row], the down pass writes
+// o[pair][row].  Every order depends on the shapes and the routing only.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxk {
+namespace {
+
+constexpr int kWarpsE = 16;
+constexpr int kThreadsE = kWarpsE * 32;
+constexpr int kRowsUE = 32;                 // rows per unit (two MMA row blocks)
+constexpr int kChunkE = 8;                  // groups per unit
+constexpr int kStageE = kRowsUE * 128;      // one TMA tile, 4 KB
+constexpr int kStagesE = 2;                 // ring stages per warp
+constexpr int kRuSeg = 4;                   // 32-row units per segment (128 rows)
+constexpr int kTokSeg = 4;                  // pairs per segment
+constexpr int kGMaxE = 128;                 // groups per row (B fragments in shared memory)
+constexpr int kMaxExpertsE = 1024;
+constexpr uint32_t kSmemMaxE = 227 * 1024;
+constexpr uint32_t kWaitE = 1u << 22;
+
+__device__ int g_fault_moetc;   // set when a bounded wait gives up
+
+__device__ __forceinline__ float exp2i_e(int e) {
+    if (e >= -126 && e <= 127) return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    if (e > 127) return __uint_as_float(0x7F800000u);
+    if (e >= -149) return __uint_as_float(1u << (e + 149));
+    return 0.0f;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2_e(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void mma16816_e(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Plan arrays written by the routing plan kernel (moe.cu).
+struct PlanRef {
+    const int32_t* hdr;       // [1] = number of touched experts
+    const int32_t* offsets;   // [E + 1]
+    const int32_t* touched;   // [touched]
+    const int32_t* pair_of;   // pairs grouped by expert
+};
+
+// Shared memory (offsets from a 1024-byte aligned base).
+struct ELayout {
+    uint32_t xf, sc, sc_bytes, part, lut, misc, segst, bars, ring, total;
+};
+__host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
+    ELayout l;
+    l.xf = 0;                                                          // [gpr][32] uint4
+    l.sc = l.xf + static_cast<uint32_t>(gpr) * 512;
+    l.sc_bytes = (static_cast<uint32_t>(kRuSeg * kRowsUE) * gpr + 32u + 15u) & ~15u;
+    l.part = l.sc + NM * l.sc_bytes;                                   // [warps][32][4] f32
+    l.part = (l.part + 15u) & ~15u;
+    l.lut = l.part + kWarpsE * kRowsUE * kTokSeg * 4;                 // [256] f32
+    l.misc = l.lut + 1024;                                            // pexp, tmax, pairs, lead
+    l.segst = l.misc + 64;                                            // [touched + 1] int
+    l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
+    l.ring = (l.bars + (kWarpsE * kStagesE + 1) * 8 + 1023u) & ~1023u;
+    l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
+    return l;
+}
+
+// NM = 2: the gate/up pass (matrices gate, up; vector = the token's x),
+// NM = 1: the down pass (matrix down; vector = the pair's act row).
+template <int NM>
+__global__ void __launch_bounds__(kThreadsE, 1)
+    k_moe_tc(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+             const uint8_t* __restrict__ bank0, const uint8_t* __restrict__ bank1, size_t stride,
+             int rows, int cols, int top_k, int n_experts, const float* __restrict__ vec,
+             PlanRef plan, float* __restrict__ out) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int gpr = cols / kGroup;
+    const ELayout L = e_layout(NM, gpr, n_experts);
+    uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    float* lut = reinterpret_cast<float*>(smem + L.lut);
+    int* pexp = reinterpret_cast<int*>(smem + L.misc);                  // [4]
+    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);   // [4]
+    int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [4]
+    int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2]
+    int* segst = reinterpret_cast<int*>(smem + L.segst);
+    uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* ring_bars = sbar + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const size_t plane = static_cast<size_t>(rows) * cols / 2;
+    const int n_blocks = (rows + kRuSeg * kRowsUE - 1) / (kRuSeg * kRowsUE);
+    const int n_c = (gpr + kChunkE - 1) / kChunkE;
+    const uint64_t policy = l2_evict_first();
+
+    if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
+    if (tid == 0) {
+        mbar_init(sbar, 1);
+        for (int i = 0; i < kWarpsE * kStagesE; ++i) mbar_init(&ring_bars[i], 1);
+        fence_mbar_init();
+        // segments per touched expert: ceil(pairs / 4) x row blocks
+        const int n_touched = plan.hdr[1];
+        segst[0] = 0;
+        for (int u = 0; u < n_touched; ++u) {
+            const int e = plan.touched[u];
+            const int n_e = plan.offsets[e + 1] - plan.offsets[e];
+            segst[u + 1] = segst[u] + (n_e + kTokSeg - 1) / kTokSeg * n_blocks;
+        }
+    }
+    __syncthreads();
+    const int n_touched = plan.hdr[1];
+    const int n_seg = segst[n_touched];
+    uint64_t* bars = ring_bars + warp * kStagesE;
+    uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * kStagesE * kStageE;
+    int kglob = 0;      // units this warp has taken so far (ring phase)
+    int nseg_cta = 0;   // segments this CTA has taken so far (scale barrier phase)
+    bool failed = false;
+
+    for (int s = blockIdx.x; s < n_seg; s += gridDim.x, ++nseg_cta) {
+        int u = 0;
+        while (segst[u + 1] <= s) ++u;
+        const int e = plan.touched[u];
+        const int beg = plan.offsets[e], n_e = plan.offsets[e + 1] - beg;
+        const int rel = s - segst[u];
+        const int ck = rel / n_blocks, b = rel - ck * n_blocks;
+        const int npair = min(kTokSeg, n_e - ck * kTokSeg);
+        const int row0 = b * kRuSeg * kRowsUE;
+        const int nrow = min(kRuSeg * kRowsUE, rows - row0);
+        const int n_ru = (nrow + kRowsUE - 1) / kRowsUE;
+        const int WK = min(n_c, kWarpsE / (NM * n_ru));
+        const bool active = warp < NM * n_ru * WK;
+        const int m = warp % NM, q = warp / NM;
+        const int my_ru = q % n_ru, kk = q / n_ru;
+        const int c_lo = active ? kk * n_c / WK : 0;
+        const int c_hi = active ? (kk + 1) * n_c / WK : 0;
+        const int n_units = c_hi - c_lo;
+
+        // --- prologue: scale bytes (one bulk copy per matrix), the pairs' vectors
+        __syncthreads();   // the last segment is done with every shared array
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            uint32_t total = 0;
+            uint32_t sz[NM];
+            const uint8_t* a0[NM];
+            for (int mm = 0; mm < NM; ++mm) {
+                const uint8_t* bank = mm == 0 ? bank0 : bank1;
+                const uint8_t* src =
+                    bank + static_cast<size_t>(e) * stride + plane + static_cast<size_t>(row0) * gpr;
+                a0[mm] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(src) &
+                                                          ~static_cast<uintptr_t>(15));
+                lead[mm] = static_cast<int>(src - a0[mm]);
+                sz[mm] = (static_cast<uint32_t>(lead[mm] + nrow * gpr) + 15u) & ~15u;
+                total += sz[mm];
+            }
+            mbar_arrive_expect_tx(sbar, total);
+            for (int mm = 0; mm < NM; ++mm)
+                bulk_g2s(smem + L.sc + mm * L.sc_bytes, a0[mm], sz[mm], sbar, policy);
+        }
+        if (tid < kTokSeg) {
+            tmax[tid] = 0u;
+            spair[tid] = tid < npair ? plan.pair_of[beg + ck * kTokSeg + tid] : 0;
+        }
+        __syncthreads();
+        constexpr int kXU = (kTokSeg * kGMaxE * 4 + kThreadsE - 1) / kThreadsE;
+        const int n_items = kTokSeg * gpr * 4;
+        float xv[kXU][8];
+#pragma unroll
+        for (int uu = 0; uu < kXU; ++uu) {
+            const int i = tid + uu * kThreadsE;
+            const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
+            if (i < n_items && tok < npair) {
+                const int pr = spair[tok];
+                const size_t vrow = NM == 2 ? static_cast<size_t>(pr / top_k) : static_cast<size_t>(pr);
+                const float4* src = reinterpret_cast<const float4*>(vec + vrow * cols + 8 * rem);
+                const float4 a = __ldg(src), bb = __ldg(src + 1);
+                xv[uu][0] = a.x; xv[uu][1] = a.y; xv[uu][2] = a.z; xv[uu][3] = a.w;
+                xv[uu][4] = bb.x; xv[uu][5] = bb.y; xv[uu][6] = bb.z; xv[uu][7] = bb.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) xv[uu][k] = 0.0f;
+            }
+        }
+        // the weights stream after the vectors' loads
+        auto issue = [&](int k, int st) {   // this warp's unit k into stage st (lane 0)
+            const int x = (c_lo + k) * kChunkE * kGroupBytes;
+            const int y = row0 + my_ru * kRowsUE;
+            mbar_arrive_expect_tx(&bars[st], kStageE);
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
+                    smem_u32(ring + st * kStageE)),
+                "l"(m == 0 ? &tm0 : &tm1), "r"(x), "r"(y), "r"(e), "r"(smem_u32(&bars[st])),
+                "l"(policy)
+                : "memory");
+        };
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            for (int k = 0; k < kStagesE && k < n_units; ++k) issue(k, (kglob + k) % kStagesE);
+        }
+#pragma unroll
+        for (int uu = 0; uu < kXU; ++uu) {
+            const int i = tid + uu * kThreadsE;
+            const int tok = min(i / (gpr * 4), kTokSeg - 1);
+            float mx = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float a = fabsf(xv[uu][k]);
+                mx = fmaxf(mx, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
+            }
+            const unsigned same = __match_any_sync(0xffffffffu, tok);
+            const unsigned mb = __reduce_max_sync(same, __float_as_uint(mx));
+            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
+        }
+        __syncthreads();
+        if (tid < kTokSeg) {
+            const float mt = __uint_as_float(tmax[tid]);
+            pexp[tid] = mt > 0.0f ? min(14 - ilogbf(mt), 126) : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int uu = 0; uu < kXU; ++uu) {
+            const int i = tid + uu * kThreadsE;
+            if (i < n_items) {
+                const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
+                const int j = rem >> 2, tw = rem & 3;
+                const float pm = exp2i_e(pexp[tok]);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float f0 = __fmul_rn(xv[uu][2 * k], pm), f1 = __fmul_rn(xv[uu][2 * k + 1], pm);
+                    hi[k] = pack_f16x2_e(f0, f1);
+                    const float2 h = f16x2_to_f32x2(hi[k]);
+                    lo[k] = pack_f16x2_e(__fsub_rn(f0, h.x), __fsub_rn(f1, h.y));
+                }
+                xf[j * 32 + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                xf[j * 32 + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        if (!mbar_wait(sbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE)) failed = true;
+        failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
+
+        // --- this warp's units
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24 of the unit, pair t
+        const float pinv = exp2i_e(-pexp[t]);
+        const uint8_t* scm = smem + L.sc + m * L.sc_bytes + lead[m];
+        int k = 0;
+        for (; k < n_units && !failed; ++k) {
+            const int kg = kglob + k, st = kg % kStagesE;
+            if (!mbar_wait(&bars[st], static_cast<uint32_t>(kg / kStagesE) & 1u, kWaitE)) {
+                failed = true;
+                break;
+            }
+            const uint8_t* stg = ring + st * kStageE;
+            const int gc0 = (c_lo + k) * kChunkE;
+            const int ngc = min(kChunkE, gpr - gc0);
+            uint32_t sb[4][2];   // 8 scale bytes of rows g, g+8, g+16, g+24 (any alignment)
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4) {
+                const uint32_t a = static_cast<uint32_t>((my_ru * kRowsUE + g + 8 * r4) * gpr + gc0);
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(
+                    reinterpret_cast<uintptr_t>(scm + a) & ~static_cast<uintptr_t>(3));
+                const uint32_t sh = 8u * (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(scm + a)) & 3u);
+                const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+                sb[r4][0] = __funnelshift_r(w0, w1, sh);
+                sb[r4][1] = __funnelshift_r(w1, w2, sh);
+            }
+#pragma unroll
+            for (int j = 0; j < kChunkE; ++j) {
+                if (j < ngc) {
+                    const uint8_t* cw = stg + g * 128 + (((j ^ g) & 7) << 4) + t * 4;
+                    uint32_t h0[4], h1[4], h2[4], h3[4];
+                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw), h0);
+                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 1024), h1);
+                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 2048), h2);
+                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 3072), h3);
+                    const uint4 bf = xf[(gc0 + j) * 32 + lane];
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma16816_e(d0, h0[0], h1[0], h0[1], h1[1], bf.x, bf.y);
+                    mma16816_e(d1, h2[0], h3[0], h2[1], h3[1], bf.x, bf.y);
+                    mma16816_e(d0, h0[2], h1[2], h0[3], h1[3], bf.z, bf.w);
+                    mma16816_e(d1, h2[2], h3[2], h2[3], h3[3], bf.z, bf.w);
+                    const int sh = 8 * (j & 3), hw = j >> 2;
+                    acc[0] = __fmaf_rn(lut[(sb[0][hw] >> sh) & 0xFFu],
+                                       __fmul_rn(__fadd_rn(d0[0], d0[1]), pinv), acc[0]);
+                    acc[1] = __fmaf_rn(lut[(sb[1][hw] >> sh) & 0xFFu],
+                                       __fmul_rn(__fadd_rn(d0[2], d0[3]), pinv), acc[1]);
+                    acc[2] = __fmaf_rn(lut[(sb[2][hw] >> sh) & 0xFFu],
+                                       __fmul_rn(__fadd_rn(d1[0], d1[1]), pinv), acc[2]);
+                    acc[3] = __fmaf_rn(lut[(sb[3][hw] >> sh) & 0xFFu],
+                                       __fmul_rn(__fadd_rn(d1[2], d1[3]), pinv), acc[3]);
+                }
+            }
+            __syncwarp();   // every lane is done with the stage
+            if (lane == 0 && k + kStagesE < n_units) {
+                fence_proxy_async_smem();
+                issue(k + kStagesE, st);
+            }
+        }
+        if (failed) {
+            // let this warp's copies in flight land before the CTA can exit
+            for (int kq = k; kq < k + kStagesE && kq < n_units; ++kq)
+                mbar_wait(&bars[(kglob + kq) % kStagesE],
+                          static_cast<uint32_t>((kglob + kq) / kStagesE) & 1u, kWaitE);
+        }
+        kglob += n_units;
+        if (active) {   // D columns 2t, 2t+1 are pair t's hi and lo
+            float* pw = part + static_cast<size_t>(warp) * kRowsUE * kTokSeg;
+            pw[g * kTokSeg + t] = acc[0];
+            pw[(g + 8) * kTokSeg + t] = acc[1];
+            pw[(g + 16) * kTokSeg + t] = acc[2];
+            pw[(g + 24) * kTokSeg + t] = acc[3];
+        }
+        failed = __syncthreads_or(failed) != 0;
+        // --- chunk ranges in order (warp (kk * n_ru + ru) * NM + m), then the epilogue
+        for (int i = tid; i < n_ru * kRowsUE * kTokSeg; i += kThreadsE) {
+            const int ru = i / (kRowsUE * kTokSeg), rem = i - ru * kRowsUE * kTokSeg;
+            const int tok = rem % kTokSeg, row = row0 + ru * kRowsUE + rem / kTokSeg;
+            float v[NM];
+#pragma unroll
+            for (int mm = 0; mm < NM; ++mm) {
+                float sacc = part[static_cast<size_t>(ru * NM + mm) * kRowsUE * kTokSeg + rem];
+                for (int qq = 1; qq < WK; ++qq)
+                    sacc = __fadd_rn(sacc, part[static_cast<size_t>((qq * n_ru + ru) * NM + mm) *
+                                                    kRowsUE * kTokSeg + rem]);
+                v[mm] = sacc;
+            }
+            if (row < rows && tok < npair) {
+                const size_t o = static_cast<size_t>(spair[tok]) * rows + row;
+                if constexpr (NM == 2)
+                    out[o] = __fmul_rn(__fdiv_rn(v[0], __fadd_rn(1.0f, expf(-v[0]))), v[1]);
+                else
+                    out[o] = v[0];
+            }
+        }
+        if (failed) break;   // the same in every thread
+    }
+    if (failed && lane == 0) atomicOr(&g_fault_moetc, 1);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_e() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The code planes of a bank as a 3-D byte tensor [experts][rows][cols/2] (the
+// expert stride is the padded matrix size), tiles of 32 rows x 128 bytes.
+bool bank_map(CUtensorMap* map, const uint8_t* bank, size_t stride, int n_experts, int rows,
+              int cols) {
+    auto fn = encode_fn_e();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols) / 2, static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(n_experts)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) / 2,
+                                   static_cast<cuuint64_t>(stride)};
+    const cuuint32_t box[3] = {128, kRowsUE, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(bank), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count_e() {
+    static std::once_flag once;
+    static int n = 0;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    });
+    return n > 0 ? n : 1;
+}
+
+template <int NM>
+cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
+                     int rows, int cols, int top_k, const float* vec, PlanRef plan, float* out,
+                     cudaStream_t s) {
+    const int gpr = cols / kGroup;
+    if (gpr > kGMaxE || n_experts > kMaxExpertsE) return cudaErrorNotSupported;
+    const ELayout l = e_layout(NM, gpr, n_experts);
+    if (l.total > kSmemMaxE) return cudaErrorNotSupported;
+    auto kernel = k_moe_tc<NM>;
+    {
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [&] {
+            attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kSmemMaxE));
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+    }
+    CUtensorMap m0, m1;
+    if (!bank_map(&m0, bank0, stride, n_experts, rows, cols)) return cudaErrorNotSupported;
+    if (NM == 2) {
+        if (!bank_map(&m1, bank1, stride, n_experts, rows, cols)) return cudaErrorNotSupported;
+    } else {
+        m1 = m0;
+    }
+    kernel<<<sm_count_e(), kThreadsE, l.total, s>>>(m0, m1, bank0, bank1, stride, rows, cols, top_k,
+                                                    n_experts, vec, plan, out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
+                                  int n_experts, int inter, int hidden, int top_k, const float* x,
+                                  const int32_t* hdr, const int32_t* offsets,
+                                  const int32_t* touched, const int32_t* pair_of, float* act,
+                                  cudaStream_t s) {
+    return launch_e<2>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k, x,
+                       PlanRef{hdr, offsets, touched, pair_of}, act, s);
+}
+
+cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
+                               int inter, const float* act, const int32_t* hdr,
+                               const int32_t* offsets, const int32_t* touched,
+                               const int32_t* pair_of, float* o_pairs, cudaStream_t s) {
+    return launch_e<1>(down_bank, down_bank, stride, n_experts, hidden, inter, 1, act,
+                       PlanRef{hdr, offsets, touched, pair_of}, o_pairs, s);
+}
+
+cudaError_t read_fault_moetc(int* value, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_moetc, sizeof(int));
+    if (e != cudaSuccess || !reset) return e;
+    const int zero = 0;
+    return cudaMemcpyToSymbol(g_fault_moetc, &zero, sizeof(int));
+}
+
+}  // namespace mxk
