@@ -187,7 +187,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
     // --- prologue: E8M0 table, scale bytes, activations
     const int nrow = min(n_ru * kRowsU, rows - row0);
-    const int nch_row = (ng + 30) / 16;   // 16-byte words covering ng bytes at any alignment
+    // 16-byte words covering a row's ng scale bytes: exactly ng / 16 when the
+    // rows' slices start on 16 bytes and fill whole words, else enough for any
+    // alignment (ragged words are stored byte by byte below)
+    const bool sc_whole = gpr % 16 == 0 && g_lo % 16 == 0 && ng % 16 == 0;
+    const int nch_row = sc_whole ? ng / 16 : (ng + 30) / 16;
     constexpr int kScU = (kMaxRuCta * kRowsU * ((kGMax + 30) / 16) + kThreadsM - 1) / kThreadsM;
     uint4 sv[kScU];
 #pragma unroll
