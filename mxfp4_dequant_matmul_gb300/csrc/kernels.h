@@ -17,11 +17,6 @@ cudaError_t launch_dequant(const uint8_t* w, int rows, int cols, float* out, cud
 cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float* X, int nb,
                                float* Y, cudaStream_t s);
 
-// tcgen05 small-batch product (decoded weights in tensor memory, split-f16
-// activations, FP32 accumulate); cudaErrorNotSupported when it cannot take the shape.
-cudaError_t launch_mm_tc5(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
-                          cudaStream_t s);
-
 // mma.sync product for up to 4 tokens per pass over the weights (split-f16
 // activations, per-group FP32 scaling); cudaErrorNotSupported, with nothing
 // launched, for shapes it cannot take.  Per token the same arithmetic for any nb.
@@ -68,7 +63,6 @@ cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_ex
 cudaError_t read_fault_matvec(int* value, bool reset);
 cudaError_t read_fault_mma(int* value, bool reset);
 cudaError_t read_fault_prefill(int* value, bool reset);
-cudaError_t read_fault_tc5(int* value, bool reset);
 cudaError_t read_fault_mvtc(int* value, bool reset);
 cudaError_t read_fault_moetc(int* value, bool reset);
 

@@ -74,15 +74,14 @@ int mxfp4_version(void) { return 100; }
 
 int mxfp4_device_faults(int* faults, int reset) {
     if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
-    int a = 0, b = 0, c = 0, d = 0, f = 0, h = 0;
+    int a = 0, b = 0, c = 0, f = 0, h = 0;
     cudaError_t e = mxk::read_fault_matvec(&a, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_mma(&b, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_prefill(&c, reset != 0);
-    if (e == cudaSuccess) e = mxk::read_fault_tc5(&d, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_mvtc(&f, reset != 0);
     if (e == cudaSuccess) e = mxk::read_fault_moetc(&h, reset != 0);
     if (e != cudaSuccess) return from_cuda(e);
-    *faults = a | (b << 1) | (c << 2) | (d << 3) | (f << 4) | (h << 5);
+    *faults = a | (b << 1) | (c << 2) | (f << 3) | (h << 4);
     return MXFP4_STATUS_OK;
 }
 
