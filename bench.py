@@ -363,6 +363,26 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """One workload, eager launches: the command the committed ncu summaries use."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import mxfp4_dequant_matmul_gb300 as mx
+    mx.lib()
+    cls = {"decode": DecodeGemv, "mm8": SmallBatch, "moe": MoeLayer, "prefill": Prefill}
+    w = cls[args.profile](mx)
+    for _ in range(args.warmup):
+        w.step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        w.step()
+    torch.cuda.synchronize()
+    print(f"{w.name}: {(time.perf_counter() - t0) / args.steps * 1e3:.3f} ms per step (eager, "
+          f"{w.launches_per_step} launches per step)")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -371,11 +391,17 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "mm8", "moe", "prefill"],
+                    help="run only this workload's warm-up and timed steps (eagerly, one "
+                         "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+        return
+    if args.profile:
+        run_profile(args)
         return
 
     import torch

@@ -72,6 +72,17 @@ int mxfp4_last_cuda_error(void);
  * Synchronises the current device. */
 int mxfp4_device_faults(int* faults, int reset);
 
+/* Launch overlap for mxfp4_mv and mxfp4_mm (up to MXFP4_MM_SMALL_MAX tokens),
+ * off by default, process-wide.  The pages have no counterpart: this is a
+ * property of a stream of launches on one GPU.  When enabled (enable != 0)
+ * these calls use programmatic dependent launch: the kernel may start while
+ * the previous kernel in the stream is still running and already stream the
+ * weight buffer `w` (code and scale planes); it reads X and writes Y only
+ * after that kernel has completed.  Enable it only if no work still running
+ * in the stream writes the weight buffers (weights that stay fixed during
+ * decoding).  Results are bit-identical either way.  Returns MXFP4_STATUS_OK. */
+int mxfp4_set_launch_overlap(int enable);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int mxfp4_version(void);
 

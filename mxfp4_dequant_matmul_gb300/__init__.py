@@ -12,7 +12,8 @@ import ctypes
 import os
 
 __all__ = [
-    "Mxfp4Error", "lib", "library_path", "mxfp4_nbytes", "mxfp4_device_faults", "mxfp4_dequant", "mxfp4_mv",
+    "Mxfp4Error", "lib", "library_path", "mxfp4_nbytes", "mxfp4_device_faults",
+    "mxfp4_set_launch_overlap", "mxfp4_dequant", "mxfp4_mv",
     "mxfp4_mm", "mxfp4_mm_fp32", "mxfp4_mm_bf16", "mxfp4_matmat_host",
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
     "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
@@ -29,6 +30,7 @@ _SIG = {
     "mxfp4_status_string": (ctypes.c_char_p, [_I]),
     "mxfp4_last_cuda_error": (_I, []),
     "mxfp4_version": (_I, []),
+    "mxfp4_set_launch_overlap": (_I, [_I]),
     "mxfp4_device_faults": (_I, [ctypes.POINTER(_I), _I]),
     "mxfp4_nbytes": (_SZ, [_I, _I]),
     "mxfp4_dequant": (_I, [_P, _I, _I, _P, _P]),
@@ -106,6 +108,12 @@ def mxfp4_device_faults(reset: bool = False) -> int:
     v = ctypes.c_int(0)
     _check("mxfp4_device_faults", lib().mxfp4_device_faults(ctypes.byref(v), int(reset)))
     return v.value
+
+
+def mxfp4_set_launch_overlap(enable: bool) -> None:
+    """Programmatic dependent launch for mxfp4_mv / mxfp4_mm (see include/mxfp4.h):
+    only when nothing still running in the stream writes the weight buffers."""
+    _check("mxfp4_set_launch_overlap", lib().mxfp4_set_launch_overlap(int(bool(enable))))
 
 
 def mxfp4_nbytes(rows: int, cols: int) -> int:

@@ -23,6 +23,10 @@ cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float
 cudaError_t launch_mv_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
                          cudaStream_t s);
 
+// Programmatic dependent launch for the mv_tc kernels (process-wide switch).
+void set_launch_overlap(bool on);
+bool launch_overlap();
+
 // mma.sync small-batch product (split-f16 activations, FP32 accumulate);
 // cudaErrorNotSupported, with nothing launched, for shapes it cannot take.
 cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,

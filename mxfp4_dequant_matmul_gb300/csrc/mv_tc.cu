@@ -37,6 +37,7 @@
 // shape only, so results are deterministic and a token's result does not
 // depend on the other tokens of its batch.
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -56,6 +57,10 @@ constexpr int kChunkM = 8;                  // groups per unit (128 code bytes p
 constexpr int kStageM = kRowsU * 128;       // one TMA tile, 4 KB
 constexpr int kMinStagesM = 2;              // ring stages per warp (more when they fit)
 constexpr int kMaxStagesM = 4;
+#ifndef MXFP4_PRE_STAGES
+#define MXFP4_PRE_STAGES 1
+#endif
+constexpr int kPreStagesM = MXFP4_PRE_STAGES;   // stages started before the wait (overlap)
 constexpr uint32_t kSmemMaxM = 227 * 1024;
 constexpr int kMaxRuCta = 4;                // 32-row units per CTA
 constexpr uint32_t kWaitM = 1u << 22;
@@ -130,7 +135,7 @@ template <int NT, int CL>
 __global__ void __launch_bounds__(kThreadsM, 1)
     k_mv_tc(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ w, int rows,
             int cols, const float* __restrict__ X, int nb, float* __restrict__ Y, int ru_cta,
-            int ng_max, int stages) {
+            int ng_max, int stages, int overlap) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -182,6 +187,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             "l"(&tmap), "r"(x), "r"(y), "r"(smem_u32(&bars[st])), "l"(policy)
             : "memory");
     };
+    // the next kernel of the stream may begin its own launch (it waits for this
+    // one before touching anything this one writes)
+    if (overlap) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < NT) tmax[tid] = 0u;
     if (tid == 0) *not_plain = 0;
 
@@ -205,6 +213,24 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             if (addr < s0 + ng) sv[u] = ldg_stream(reinterpret_cast<const uint4*>(w + addr));
         }
     }
+    // The weights stream after the prologue's own loads, which would otherwise
+    // wait behind them in the memory system -- unless the launch overlaps the
+    // previous kernel of the stream (programmatic dependent launch): then the
+    // weights, which that kernel does not write, start at once, and x (which
+    // it may write) is read only once it has completed.
+    auto start_weights = [&](int k0, int k1) {   // this warp's units k0 .. k1-1
+        if (lane == 0) {
+            if (k0 == 0) {
+                for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+                fence_mbar_init();
+            }
+            for (int k = k0; k < k1 && k < n_units; ++k) issue(k, k);
+        }
+    };
+    if (overlap) {
+        start_weights(0, kPreStagesM);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     // activation items: (token, group, word) = 8 elements
     constexpr int kXU = (NT * kGMax * 4 + kThreadsM - 1) / kThreadsM;
     const int n_items = NT * ng * 4;
@@ -225,13 +251,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
         }
     }
-    // the weights stream after the prologue's own loads, which would otherwise
-    // wait behind them in the memory system
-    if (lane == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        fence_mbar_init();
-        for (int k = 0; k < stages && k < n_units; ++k) issue(k, k);
-    }
+    start_weights(overlap ? kPreStagesM : 0, stages);   // after the prologue's loads
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
     __syncthreads();   // tmax is zero before any atomic below
     // "plain" scales: no byte 0 or 255 and none above kPlainMax, so that 2^(k-127)
@@ -442,6 +462,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_m() {
     return fn;
 }
 
+std::atomic<bool> g_overlap{false};
+
 int sm_count_m() {
     static std::once_flag once;
     static int n = 0;
@@ -534,15 +556,19 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     cfg.blockDim = dim3(kThreadsM);
     cfg.dynamicSmemBytes = l.total;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    const int overlap = launch_overlap() ? 1 : 0;
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = overlap ? 2 : 1;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, kernel, map, w, rows, cols, X, nb, Y, ru_cta, ng_max, stages);
+        cudaLaunchKernelEx(&cfg, kernel, map, w, rows, cols, X, nb, Y, ru_cta, ng_max, stages,
+                           overlap);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -575,6 +601,9 @@ cudaError_t launch_mv_tc(const uint8_t* w, int rows, int cols, const float* X, i
     if (nb == 2) return launch_mv_nt<2>(w, rows, cols, X, nb, Y, s);
     return launch_mv_nt<4>(w, rows, cols, X, nb, Y, s);
 }
+
+void set_launch_overlap(bool on) { g_overlap.store(on); }
+bool launch_overlap() { return g_overlap.load(); }
 
 cudaError_t read_fault_mvtc(int* value, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_mvtc, sizeof(int));

@@ -72,6 +72,11 @@ int mxfp4_last_cuda_error(void) { return g_last_cuda_error; }
 
 int mxfp4_version(void) { return 100; }
 
+int mxfp4_set_launch_overlap(int enable) {
+    mxk::set_launch_overlap(enable != 0);
+    return MXFP4_STATUS_OK;
+}
+
 int mxfp4_device_faults(int* faults, int reset) {
     if (faults == nullptr) return MXFP4_STATUS_BAD_POINTER;
     int a = 0, b = 0, c = 0, f = 0, h = 0;

@@ -262,5 +262,67 @@ def test_host_buffer_entry_matches_device_entry(mx):
     assert_bits_equal(Y_host.numpy(), host(y_dev_ref), "host entry")
 
 
+@pytest.mark.parametrize("nb", [1, 3])
+def test_launch_overlap_chain_is_bit_identical(mx, nb):
+    # four layers, each reading the previous one's output: with programmatic
+    # dependent launch a kernel starts early but must read its x only after the
+    # previous kernel has written it, so the chain's results are the same bits
+    n = 1024
+    ws = [to_dev(synth.mxfp4_matrix(n, n, 900 + i, 118, 130)) for i in range(4)]
+    x0 = to_dev(synth.normal_f32(950 + nb, nb * n))
+
+    def chain():
+        import torch
+        outs, x = [], x0
+        for w in ws:
+            y = empty(nb * n)
+            if nb == 1:
+                mx.mxfp4_mv(w, n, n, x, y)
+            else:
+                mx.mxfp4_mm(w, n, n, x, nb, y)
+            # keep magnitudes moderate between layers (a kernel of our own
+            # would do; torch's scale runs between the launches anyway)
+            x = y * (1.0 / 64.0)
+            outs.append(y)
+        torch.cuda.synchronize()
+        return [host(o) for o in outs]
+
+    mx.mxfp4_set_launch_overlap(False)
+    want = chain()
+    try:
+        mx.mxfp4_set_launch_overlap(True)
+        got = chain()
+    finally:
+        mx.mxfp4_set_launch_overlap(False)
+    for i, (g, w_) in enumerate(zip(got, want)):
+        assert_bits_equal(g, w_, f"layer {i} with launch overlap, nb={nb}")
+
+
+def test_launch_overlap_back_to_back_matvecs(mx):
+    # layers launched directly one after another (no other kernel in between):
+    # each reads the previous layer's output as its x
+    n = 1024
+    ws = [to_dev(synth.mxfp4_matrix(n, n, 960 + i, 100, 104)) for i in range(6)]
+    x0 = to_dev(synth.normal_f32(970, n))
+
+    def chain():
+        ys = [empty(n) for _ in ws]
+        x = x0
+        for w, y in zip(ws, ys):
+            mx.mxfp4_mv(w, n, n, x, y)
+            x = y
+        return [host(y) for y in ys]
+
+    mx.mxfp4_set_launch_overlap(False)
+    want = chain()
+    try:
+        mx.mxfp4_set_launch_overlap(True)
+        got = chain()
+    finally:
+        mx.mxfp4_set_launch_overlap(False)
+    for i, (g, w_) in enumerate(zip(got, want)):
+        assert_bits_equal(g, w_, f"back-to-back layer {i} with launch overlap")
+
+
 def test_no_device_faults_after_the_suite(mx):
     assert mx.mxfp4_device_faults(reset=True) == 0
