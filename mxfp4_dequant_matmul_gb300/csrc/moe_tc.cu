@@ -77,22 +77,26 @@ struct PlanRef {
     const int32_t* pair_of;   // pairs grouped by expert
 };
 
-// Shared memory (offsets from a 1024-byte aligned base).
+// Shared memory (offsets from a 1024-byte aligned base).  Two scale buffers
+// (the next segment's rows arrive while this one runs); the partial sums of a
+// segment reuse its scale buffer once every warp is done with the scales.
 struct ELayout {
-    uint32_t xf, sc, sc_bytes, part, lut, misc, segst, bars, ring, total;
+    uint32_t xf, sc, sc_bytes, lut, misc, segst, bars, ring, total;
 };
 __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     ELayout l;
     l.xf = 0;                                                          // [gpr][32] uint4
-    l.sc = l.xf + static_cast<uint32_t>(gpr) * 512;
+    l.sc = l.xf + static_cast<uint32_t>(gpr) * 512;                    // [2][NM][sc_bytes]
     l.sc_bytes = (static_cast<uint32_t>(kRuSeg * kRowsUE) * gpr + 32u + 15u) & ~15u;
-    l.part = l.sc + NM * l.sc_bytes;                                   // [warps][32][4] f32
-    l.part = (l.part + 15u) & ~15u;
-    l.lut = l.part + kWarpsE * kRowsUE * kTokSeg * 4;                 // [256] f32
-    l.misc = l.lut + 1024;                                            // pexp, tmax, pairs, lead
-    l.segst = l.misc + 64;                                            // [touched + 1] int
+    const uint32_t part_bytes = kWarpsE * kRowsUE * kTokSeg * 4;      // [warps][32][4] f32
+    const uint32_t buf = NM * l.sc_bytes > part_bytes ? NM * l.sc_bytes : part_bytes;
+    l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
+    l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
+    l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
+    l.misc = l.lut + 1024;                             // pexp, tmax, pairs, lead
+    l.segst = l.misc + 80;                                            // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
-    l.ring = (l.bars + (kWarpsE * kStagesE + 1) * 8 + 1023u) & ~1023u;
+    l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
     l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
     return l;
 }
@@ -111,15 +115,14 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const int gpr = cols / kGroup;
     const ELayout L = e_layout(NM, gpr, n_experts);
     uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
-    float* part = reinterpret_cast<float*>(smem + L.part);
     float* lut = reinterpret_cast<float*>(smem + L.lut);
     int* pexp = reinterpret_cast<int*>(smem + L.misc);                  // [4]
     unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);   // [4]
     int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [4]
-    int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2]
+    int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2 buffers][2 matrices]
     int* segst = reinterpret_cast<int*>(smem + L.segst);
-    uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* ring_bars = sbar + 1;
+    uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
+    uint64_t* ring_bars = sbar + 2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -130,7 +133,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
 
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
     if (tid == 0) {
-        mbar_init(sbar, 1);
+        mbar_init(&sbar[0], 1);
+        mbar_init(&sbar[1], 1);
         for (int i = 0; i < kWarpsE * kStagesE; ++i) mbar_init(&ring_bars[i], 1);
         fence_mbar_init();
         // segments per touched expert: ceil(pairs / 4) x row blocks
@@ -147,53 +151,101 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const int n_seg = segst[n_touched];
     uint64_t* bars = ring_bars + warp * kStagesE;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * kStagesE * kStageE;
-    int kglob = 0;      // units this warp has taken so far (ring phase)
-    int nseg_cta = 0;   // segments this CTA has taken so far (scale barrier phase)
-    bool failed = false;
 
-    for (int s = blockIdx.x; s < n_seg; s += gridDim.x, ++nseg_cta) {
+    // A segment as this warp sees it.
+    struct Seg {
+        int e, beg, npair, row0, nrow, n_ru, WK, m, my_ru, c_lo, n_units;
+        bool active;
+    };
+    auto seg_of = [&](int s) {
+        Seg q{};
+        if (s >= n_seg) return q;   // none: no units
         int u = 0;
         while (segst[u + 1] <= s) ++u;
-        const int e = plan.touched[u];
-        const int beg = plan.offsets[e], n_e = plan.offsets[e + 1] - beg;
+        q.e = plan.touched[u];
+        const int b0 = plan.offsets[q.e], n_e = plan.offsets[q.e + 1] - b0;
         const int rel = s - segst[u];
         const int ck = rel / n_blocks, b = rel - ck * n_blocks;
-        const int npair = min(kTokSeg, n_e - ck * kTokSeg);
-        const int row0 = b * kRuSeg * kRowsUE;
-        const int nrow = min(kRuSeg * kRowsUE, rows - row0);
-        const int n_ru = (nrow + kRowsUE - 1) / kRowsUE;
-        const int WK = min(n_c, kWarpsE / (NM * n_ru));
-        const bool active = warp < NM * n_ru * WK;
-        const int m = warp % NM, q = warp / NM;
-        const int my_ru = q % n_ru, kk = q / n_ru;
-        const int c_lo = active ? kk * n_c / WK : 0;
-        const int c_hi = active ? (kk + 1) * n_c / WK : 0;
-        const int n_units = c_hi - c_lo;
-
-        // --- prologue: scale bytes (one bulk copy per matrix), the pairs' vectors
-        __syncthreads();   // the last segment is done with every shared array
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            uint32_t total = 0;
-            uint32_t sz[NM];
-            const uint8_t* a0[NM];
-            for (int mm = 0; mm < NM; ++mm) {
-                const uint8_t* bank = mm == 0 ? bank0 : bank1;
-                const uint8_t* src =
-                    bank + static_cast<size_t>(e) * stride + plane + static_cast<size_t>(row0) * gpr;
-                a0[mm] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(src) &
-                                                          ~static_cast<uintptr_t>(15));
-                lead[mm] = static_cast<int>(src - a0[mm]);
-                sz[mm] = (static_cast<uint32_t>(lead[mm] + nrow * gpr) + 15u) & ~15u;
-                total += sz[mm];
-            }
-            mbar_arrive_expect_tx(sbar, total);
-            for (int mm = 0; mm < NM; ++mm)
-                bulk_g2s(smem + L.sc + mm * L.sc_bytes, a0[mm], sz[mm], sbar, policy);
+        q.beg = b0 + ck * kTokSeg;
+        q.npair = min(kTokSeg, n_e - ck * kTokSeg);
+        q.row0 = b * kRuSeg * kRowsUE;
+        q.nrow = min(kRuSeg * kRowsUE, rows - q.row0);
+        q.n_ru = (q.nrow + kRowsUE - 1) / kRowsUE;
+        q.WK = min(n_c, kWarpsE / (NM * q.n_ru));
+        q.active = warp < NM * q.n_ru * q.WK;
+        q.m = warp % NM;
+        const int qq = warp / NM;
+        q.my_ru = qq % q.n_ru;
+        const int kk = qq / q.n_ru;
+        q.c_lo = q.active ? kk * n_c / q.WK : 0;
+        q.n_units = q.active ? (kk + 1) * n_c / q.WK - q.c_lo : 0;
+        return q;
+    };
+    // this warp's unit k of segment q into stage st (lane 0)
+    auto issue = [&](const Seg& q, int k, int st) {
+        const int x = (q.c_lo + k) * kChunkE * kGroupBytes;
+        const int y = q.row0 + q.my_ru * kRowsUE;
+        mbar_arrive_expect_tx(&bars[st], kStageE);
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
+                smem_u32(ring + st * kStageE)),
+            "l"(q.m == 0 ? &tm0 : &tm1), "r"(x), "r"(y), "r"(q.e), "r"(smem_u32(&bars[st])),
+            "l"(policy)
+            : "memory");
+    };
+    // the scale rows of segment q into buffer bi (thread 0): one bulk copy per matrix
+    auto issue_scales = [&](const Seg& q, int bi) {
+        uint32_t total = 0;
+        uint32_t sz[NM];
+        const uint8_t* a0[NM];
+        for (int mm = 0; mm < NM; ++mm) {
+            const uint8_t* bank = mm == 0 ? bank0 : bank1;
+            const uint8_t* src =
+                bank + static_cast<size_t>(q.e) * stride + plane + static_cast<size_t>(q.row0) * gpr;
+            a0[mm] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(src) &
+                                                      ~static_cast<uintptr_t>(15));
+            lead[bi * 2 + mm] = static_cast<int>(src - a0[mm]);
+            sz[mm] = (static_cast<uint32_t>(lead[bi * 2 + mm] + q.nrow * gpr) + 15u) & ~15u;
+            total += sz[mm];
         }
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sbar[bi], total);
+        for (int mm = 0; mm < NM; ++mm)
+            bulk_g2s(smem + L.sc + (bi * NM + mm) * L.sc_bytes, a0[mm], sz[mm], &sbar[bi], policy);
+    };
+
+    int kglob = 0;      // this warp's units consumed so far (ring phase)
+    int issued = 0;     // this warp's units issued so far (lane 0): never more than kglob + stages
+    int nseg_cta = 0;   // segments this CTA has taken so far (scale buffer and phase)
+    bool failed = false;
+    Seg cur = seg_of(blockIdx.x);
+    int sc_pend = -1;   // (thread 0) buffer of a scale copy not yet seen complete
+    uint32_t sc_pend_par = 0;
+    if (tid == 0 && blockIdx.x < n_seg) {
+        issue_scales(cur, 0);
+        sc_pend = 0;
+    }
+
+    for (int s = blockIdx.x; s < n_seg; s += gridDim.x, ++nseg_cta) {
+        const Seg nxt = seg_of(s + gridDim.x);
+        const int bi = nseg_cta & 1;
+        // the next unit of this warp's stream (this segment's, then the next one's)
+        auto issue_next = [&]() {
+            const int j = issued - kglob;
+            if (j < cur.n_units)
+                issue(cur, j, issued % kStagesE);
+            else
+                issue(nxt, j - cur.n_units, issued % kStagesE);
+            ++issued;
+        };
+        const int stream_end = kglob + cur.n_units + nxt.n_units;
+
+        // --- prologue: the pairs' vectors -> B fragments
+        __syncthreads();   // the last segment is done with the fragments and the pairs
         if (tid < kTokSeg) {
             tmax[tid] = 0u;
-            spair[tid] = tid < npair ? plan.pair_of[beg + ck * kTokSeg + tid] : 0;
+            spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
         }
         __syncthreads();
         constexpr int kXU = (kTokSeg * kGMaxE * 4 + kThreadsE - 1) / kThreadsE;
@@ -203,7 +255,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         for (int uu = 0; uu < kXU; ++uu) {
             const int i = tid + uu * kThreadsE;
             const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
-            if (i < n_items && tok < npair) {
+            if (i < n_items && tok < cur.npair) {
                 const int pr = spair[tok];
                 const size_t vrow = NM == 2 ? static_cast<size_t>(pr / top_k) : static_cast<size_t>(pr);
                 const float4* src = reinterpret_cast<const float4*>(vec + vrow * cols + 8 * rem);
@@ -215,22 +267,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 for (int k = 0; k < 8; ++k) xv[uu][k] = 0.0f;
             }
         }
-        // the weights stream after the vectors' loads
-        auto issue = [&](int k, int st) {   // this warp's unit k into stage st (lane 0)
-            const int x = (c_lo + k) * kChunkE * kGroupBytes;
-            const int y = row0 + my_ru * kRowsUE;
-            mbar_arrive_expect_tx(&bars[st], kStageE);
-            asm volatile(
-                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
-                    smem_u32(ring + st * kStageE)),
-                "l"(m == 0 ? &tm0 : &tm1), "r"(x), "r"(y), "r"(e), "r"(smem_u32(&bars[st])),
-                "l"(policy)
-                : "memory");
-        };
+        // weights: fill the ring (some units may have been issued already)
         if (lane == 0) {
             fence_proxy_async_smem();
-            for (int k = 0; k < kStagesE && k < n_units; ++k) issue(k, (kglob + k) % kStagesE);
+            while (issued < kglob + kStagesE && issued < stream_end) issue_next();
         }
 #pragma unroll
         for (int uu = 0; uu < kXU; ++uu) {
@@ -271,27 +311,31 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 xf[j * 32 + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        if (!mbar_wait(sbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE)) failed = true;
+        if (!mbar_wait(&sbar[bi], static_cast<uint32_t>(nseg_cta >> 1) & 1u, kWaitE)) {
+            failed = true;
+        } else {
+            if (tid == 0) sc_pend = -1;
+        }
         failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
 
         // --- this warp's units
         float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24 of the unit, pair t
         const float pinv = exp2i_e(-pexp[t]);
-        const uint8_t* scm = smem + L.sc + m * L.sc_bytes + lead[m];
+        const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
         int k = 0;
-        for (; k < n_units && !failed; ++k) {
+        for (; k < cur.n_units && !failed; ++k) {
             const int kg = kglob + k, st = kg % kStagesE;
             if (!mbar_wait(&bars[st], static_cast<uint32_t>(kg / kStagesE) & 1u, kWaitE)) {
                 failed = true;
                 break;
             }
             const uint8_t* stg = ring + st * kStageE;
-            const int gc0 = (c_lo + k) * kChunkE;
+            const int gc0 = (cur.c_lo + k) * kChunkE;
             const int ngc = min(kChunkE, gpr - gc0);
             uint32_t sb[4][2];   // 8 scale bytes of rows g, g+8, g+16, g+24 (any alignment)
 #pragma unroll
             for (int r4 = 0; r4 < 4; ++r4) {
-                const uint32_t a = static_cast<uint32_t>((my_ru * kRowsUE + g + 8 * r4) * gpr + gc0);
+                const uint32_t a = static_cast<uint32_t>((cur.my_ru * kRowsUE + g + 8 * r4) * gpr + gc0);
                 const uint32_t* wp = reinterpret_cast<const uint32_t*>(
                     reinterpret_cast<uintptr_t>(scm + a) & ~static_cast<uintptr_t>(3));
                 const uint32_t sh = 8u * (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(scm + a)) & 3u);
@@ -326,40 +370,47 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 }
             }
             __syncwarp();   // every lane is done with the stage
-            if (lane == 0 && k + kStagesE < n_units) {
+            if (lane == 0 && issued < stream_end) {   // refill: this segment's or the next one's
                 fence_proxy_async_smem();
-                issue(k + kStagesE, st);
+                issue_next();
             }
         }
         if (failed) {
             // let this warp's copies in flight land before the CTA can exit
-            for (int kq = k; kq < k + kStagesE && kq < n_units; ++kq)
-                mbar_wait(&bars[(kglob + kq) % kStagesE],
-                          static_cast<uint32_t>((kglob + kq) / kStagesE) & 1u, kWaitE);
+            for (int kq = kglob + k; kq < issued; ++kq)
+                mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
         }
-        kglob += n_units;
-        if (active) {   // D columns 2t, 2t+1 are pair t's hi and lo
+        kglob += cur.n_units;
+        failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales
+        // the next segment's scale rows go to the other buffer
+        if (tid == 0 && !failed && s + static_cast<int>(gridDim.x) < n_seg) {
+            issue_scales(nxt, bi ^ 1);
+            sc_pend = bi ^ 1;
+            sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
+        }
+        float* part = reinterpret_cast<float*>(smem + L.sc + bi * NM * L.sc_bytes);
+        if (cur.active) {   // D columns 2t, 2t+1 are pair t's hi and lo
             float* pw = part + static_cast<size_t>(warp) * kRowsUE * kTokSeg;
             pw[g * kTokSeg + t] = acc[0];
             pw[(g + 8) * kTokSeg + t] = acc[1];
             pw[(g + 16) * kTokSeg + t] = acc[2];
             pw[(g + 24) * kTokSeg + t] = acc[3];
         }
-        failed = __syncthreads_or(failed) != 0;
+        __syncthreads();
         // --- chunk ranges in order (warp (kk * n_ru + ru) * NM + m), then the epilogue
-        for (int i = tid; i < n_ru * kRowsUE * kTokSeg; i += kThreadsE) {
+        for (int i = tid; i < cur.n_ru * kRowsUE * kTokSeg; i += kThreadsE) {
             const int ru = i / (kRowsUE * kTokSeg), rem = i - ru * kRowsUE * kTokSeg;
-            const int tok = rem % kTokSeg, row = row0 + ru * kRowsUE + rem / kTokSeg;
+            const int tok = rem % kTokSeg, row = cur.row0 + ru * kRowsUE + rem / kTokSeg;
             float v[NM];
 #pragma unroll
             for (int mm = 0; mm < NM; ++mm) {
                 float sacc = part[static_cast<size_t>(ru * NM + mm) * kRowsUE * kTokSeg + rem];
-                for (int qq = 1; qq < WK; ++qq)
-                    sacc = __fadd_rn(sacc, part[static_cast<size_t>((qq * n_ru + ru) * NM + mm) *
+                for (int qq = 1; qq < cur.WK; ++qq)
+                    sacc = __fadd_rn(sacc, part[static_cast<size_t>((qq * cur.n_ru + ru) * NM + mm) *
                                                     kRowsUE * kTokSeg + rem]);
                 v[mm] = sacc;
             }
-            if (row < rows && tok < npair) {
+            if (row < rows && tok < cur.npair) {
                 const size_t o = static_cast<size_t>(spair[tok]) * rows + row;
                 if constexpr (NM == 2)
                     out[o] = __fmul_rn(__fdiv_rn(v[0], __fadd_rn(1.0f, expf(-v[0]))), v[1]);
@@ -368,6 +419,15 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             }
         }
         if (failed) break;   // the same in every thread
+        cur = nxt;
+    }
+    // a failed CTA may still have copies of a next segment in flight: wait for them
+    if (failed) {
+        __syncthreads();
+        if (lane == 0)
+            for (int kq = kglob; kq < issued; ++kq)
+                mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
+        if (tid == 0 && sc_pend >= 0) mbar_wait(&sbar[sc_pend], sc_pend_par, kWaitE);
     }
     if (failed && lane == 0) atomicOr(&g_fault_moetc, 1);
 }
