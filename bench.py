@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS = 16
+MV_TC_TRAFFIC_BYTES = 31266048   # measured per launch of k_mv_tc<1,1> on the decode GEMV
 METRIC = "MXFP4 fused dequant-matvec weight GB/s (decode GEMV 14336x4096)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -164,6 +165,18 @@ class DecodeGemv(Workload):
     def step_e2e(self):
         for w, yh, y in zip(self.ws, self.yh, self.ys):
             self.mx.mxfp4_matmat_host(w, self.rows, self.cols, self.xh, 1, yh, self.x_stage, y)
+
+
+class DecodeGemvFp32(DecodeGemv):
+    """The decode GEMV through the FP32 CUDA-core path (mxfp4_mm_fp32, nb = 1)."""
+
+    def __init__(self, mx, layers=LAYERS):
+        super().__init__(mx, layers)
+        self.dominant = "mxfp4_mm_fp32 nb=1 (k_mv_bulk)"
+
+    def step(self):
+        for w, y in zip(self.ws, self.ys):
+            self.mx.mxfp4_mm_fp32(w, self.rows, self.cols, self.x, 1, y)
 
 
 class SmallBatch(Workload):
@@ -370,7 +383,8 @@ def run_profile(args):
     __graft_entry__.build()
     import mxfp4_dequant_matmul_gb300 as mx
     mx.lib()
-    cls = {"decode": DecodeGemv, "mm8": SmallBatch, "moe": MoeLayer, "prefill": Prefill}
+    cls = {"decode": DecodeGemv, "decode_fp32": DecodeGemvFp32, "mm8": SmallBatch,
+           "moe": MoeLayer, "prefill": Prefill}
     w = cls[args.profile](mx)
     for _ in range(args.warmup):
         w.step()
@@ -391,7 +405,7 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "mm8", "moe", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "decode_fp32", "mm8", "moe", "prefill"],
                     help="run only this workload's warm-up and timed steps (eagerly, one "
                          "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()
@@ -493,7 +507,10 @@ def main():
                        "timing": "CUDA graph of one step, CUDA events on its stream"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                         "traffic": None, "peak_source": pk["source"],
+                         # dram__bytes_read.sum + dram__bytes_write.sum of one launch of
+                         # the same kernel on the same workload (ncu capture in
+                         # profiles/k_mv_tc_decode_gemv_14336x4096.md)
+                         "traffic": MV_TC_TRAFFIC_BYTES, "peak_source": pk["source"],
                          "kernel": main_w.dominant,
                          "bytes_per_launch": main_w.bytes_per_launch,
                          "us_per_launch": per_launch_s * 1e6},
