@@ -36,11 +36,6 @@ cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, i
 cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
                               float* Y, cudaStream_t s);
 
-// CUDA-core product with X rounded to bfloat16 (same numerics as the tcgen05
-// path; kept as a cross-check).
-cudaError_t launch_mm_bf16(const uint8_t* w, int rows, int cols, const float* X, int nb,
-                           float* Y, cudaStream_t s);
-
 // Routed experts.  The workspace layout is owned by moe.cu.
 size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter);
 cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,

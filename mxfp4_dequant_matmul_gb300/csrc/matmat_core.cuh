@@ -25,21 +25,12 @@ constexpr int kXPad = 36;                   // floats per staged group (32 + 4):
 constexpr int kStageGroups = 256;           // staged groups per chunk * NB
 constexpr size_t kStageBytes = kStageGroups * kXPad * sizeof(float);
 
-// Round to nearest-even bfloat16, kept as float (Inf/NaN pass through): the
-// operand rounding of the tensor-core product.  (GLOBAL fn mxg_bf16.)
-__device__ __forceinline__ float bf16_rne(float v) {
-    uint32_t b = __float_as_uint(v);
-    if ((b & 0x7F800000u) == 0x7F800000u) return v;
-    b = (b + 0x7FFFu + ((b >> 16) & 1u)) & 0xFFFF0000u;
-    return __uint_as_float(b);
-}
-
 // acc[m][i][t] gets the row partial of this lane; call warp_allreduce after.
 // wm[m]: base of matrix m (code plane first, scale plane after it);
 // row_w: first row of this warp (rows >= `rows` are skipped);
 // xt[t]: the token vectors (16-B aligned, `cols` floats), nullptr = zero;
 // xs: kStageBytes of shared memory.  Must be called by all kThreads threads.
-template <int R, int NB, int NM, bool BF16X>
+template <int R, int NB, int NM>
 __device__ __forceinline__ void cta_group_walk(const uint8_t* const (&wm)[NM], int rows,
                                                int cols, long row_w,
                                                const float* const (&xt)[NB], float* xs,
@@ -64,10 +55,6 @@ __device__ __forceinline__ void cta_group_walk(const uint8_t* const (&wm)[NM], i
             if (src != nullptr) {
                 v = __ldg(reinterpret_cast<const float4*>(src + static_cast<size_t>(gc + g) *
                                                                     kGroup) + q);
-                if (BF16X) {
-                    v.x = bf16_rne(v.x); v.y = bf16_rne(v.y);
-                    v.z = bf16_rne(v.z); v.w = bf16_rne(v.w);
-                }
             }
             *reinterpret_cast<float4*>(xs + (t * KCG + g) * kXPad + q * 4) = v;
         }

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) k_dequant(const uint32_t* __restrict__ wo
     }
 }
 
-template <int R, int NB, bool BF16X>
+template <int R, int NB>
 __global__ void __launch_bounds__(kThreads) k_matmat(const uint8_t* __restrict__ w, int rows,
                                                      int cols, const float* __restrict__ X,
                                                      int nb, float* __restrict__ Y) {
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kThreads) k_matmat(const uint8_t* __restrict__
 
     float acc[1][R][NB];
     zero(acc);
-    cta_group_walk<R, NB, 1, BF16X>(wm, rows, cols, row_w, xt, xs, acc);
+    cta_group_walk<R, NB, 1>(wm, rows, cols, row_w, xt, xs, acc);
     warp_allreduce(acc);
 
 #pragma unroll
@@ -386,11 +386,11 @@ cudaError_t launch_mv_bulk(const uint8_t* w, int rows, int cols, const float* x,
     return cudaGetLastError();
 }
 
-template <int R, int NB, bool BF16X>
+template <int R, int NB>
 cudaError_t launch(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
                    cudaStream_t s) {
     const dim3 grid((rows + kWarps * R - 1) / (kWarps * R), (nb + NB - 1) / NB);
-    k_matmat<R, NB, BF16X><<<grid, kThreads, kStageBytes, s>>>(w, rows, cols, X, nb, Y);
+    k_matmat<R, NB><<<grid, kThreads, kStageBytes, s>>>(w, rows, cols, X, nb, Y);
     return cudaGetLastError();
 }
 
@@ -421,25 +421,17 @@ cudaError_t launch_matmat_fp32(const uint8_t* w, int rows, int cols, const float
         if (gpr <= 96) return launch_stream<2, 1, 3>(w, rows, cols, X, nb, Y, s);
         return launch_stream<2, 1, 4>(w, rows, cols, X, nb, Y, s);
     }
-    if (nb == 1) return launch<4, 1, false>(w, rows, cols, X, nb, Y, s);
-    if (nb == 2) return launch<4, 2, false>(w, rows, cols, X, nb, Y, s);
-    if (nb <= 4) return launch<2, 4, false>(w, rows, cols, X, nb, Y, s);
-    return launch<2, 8, false>(w, rows, cols, X, nb, Y, s);
+    if (nb == 1) return launch<4, 1>(w, rows, cols, X, nb, Y, s);
+    if (nb == 2) return launch<4, 2>(w, rows, cols, X, nb, Y, s);
+    if (nb <= 4) return launch<2, 4>(w, rows, cols, X, nb, Y, s);
+    return launch<2, 8>(w, rows, cols, X, nb, Y, s);
 }
 
-// Placeholder for the tensor-core product: the same walk on bf16-rounded x.
-// Every product of a bf16 value and a decoded weight is exact in FP32, so this
-// has the tensor-core path's numerics (exact products, FP32 sums).
 cudaError_t read_fault_matvec(int* value, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_matvec, sizeof(int));
     if (e != cudaSuccess || !reset) return e;
     const int zero = 0;
     return cudaMemcpyToSymbol(g_fault_matvec, &zero, sizeof(int));
-}
-
-cudaError_t launch_mm_bf16(const uint8_t* w, int rows, int cols, const float* X, int nb,
-                           float* Y, cudaStream_t s) {
-    return launch<2, 8, true>(w, rows, cols, X, nb, Y, s);
 }
 
 }  // namespace mxk

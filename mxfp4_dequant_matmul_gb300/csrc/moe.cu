@@ -127,7 +127,7 @@ __device__ __forceinline__ void expert_chunk(const uint8_t* const (&wm)[P == Pas
     }
     float acc[NM][R][NB];
     zero(acc);
-    cta_group_walk<R, NB, NM, false>(wm, rows, cols, row_w, xt, xs, acc);
+    cta_group_walk<R, NB, NM>(wm, rows, cols, row_w, xt, xs, acc);
     warp_allreduce(acc);
 #pragma unroll
     for (int i = 0; i < R; ++i)

@@ -20,6 +20,10 @@
 // writes Y.  Every wait is bounded; a CTA that gives up sets the fault word,
 // still frees its tensor memory and returns.
 #include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -299,10 +303,322 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill(const uint8_t* __restr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Version with the loads off the converting threads: warp 0 streams the raw
+// tiles with TMA -- X as f32 (64 columns x 128 tokens), the codes (32 bytes x
+// 256 rows) and, every 8 k-steps, the scale bytes of 16 groups (16 bytes x 256
+// rows) -- into rings in shared memory; warps 2..15 convert a raw stage into
+// the two bf16 operand tiles (128-byte swizzle) of a converted stage; warp 1
+// issues the four tcgen05.mma of each converted stage and frees it with
+// tcgen05.commit.  Needs cols % 512 == 0 (the scale plane's row stride is a
+// multiple of 16 bytes) and 16-byte aligned X.
+constexpr int kRawStages = 2;
+constexpr int kConvStages = 2;
+constexpr int kConvWarps = 14;
+constexpr uint32_t kRawXBytes = kPM * kPK * 4;      // 32 KB f32
+constexpr uint32_t kRawWBytes = kPN * kPK / 2;      // 8 KB codes
+constexpr uint32_t kRawStageBytes = kRawXBytes + kRawWBytes;
+constexpr uint32_t kScBlockBytes = kPN * 16;        // 16 groups x 256 rows
+constexpr int kStepsPerSc = 8;                      // k-steps per scale block (2 groups each)
+
+struct P2Layout {
+    uint32_t conv, raw, sc, total;
+};
+__host__ __device__ constexpr P2Layout p2_layout() {
+    return P2Layout{0, kConvStages * kPStageBytes,
+                    kConvStages * kPStageBytes + kRawStages * kRawStageBytes,
+                    kConvStages * kPStageBytes + kRawStages * kRawStageBytes + 2 * kScBlockBytes +
+                        1024};
+}
+
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                      uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_p(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_prefill2(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+               const __grid_constant__ CUtensorMap smap, int rows, int cols, int nb,
+               float* __restrict__ Y) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr P2Layout L = p2_layout();
+    // raw_full/raw_free [kRawStages], conv_full/conv_free [kConvStages],
+    // sc_full/sc_free [2], done
+    __shared__ uint64_t bars[2 * kRawStages + 2 * kConvStages + 4 + 1];
+    uint64_t* raw_full = bars;
+    uint64_t* raw_free = raw_full + kRawStages;
+    uint64_t* conv_full = raw_free + kRawStages;
+    uint64_t* conv_free = conv_full + kConvStages;
+    uint64_t* sc_full = conv_free + kConvStages;
+    uint64_t* sc_free = sc_full + 2;
+    uint64_t* done = sc_free + 2;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_word;
+    volatile int* abort_flag = &abort_word;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * kPN;      // weight rows of this tile
+    const int t0 = blockIdx.y * kPM;      // tokens of this tile
+    const int n_steps = (cols + kPK - 1) / kPK;
+    int issued_steps = 0, issued_blocks = 0;   // (producer) copies started
+
+    if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+    if (tid == 0) {
+        for (int i = 0; i < kRawStages; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_free[i], kConvWarps);
+        }
+        for (int i = 0; i < kConvStages; ++i) {
+            mbar_init(&conv_full[i], kConvWarps);
+            mbar_init(&conv_free[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sc_full[i], 1);
+            mbar_init(&sc_free[i], kConvWarps);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicOr(&g_fault_prefill, 1);
+    };
+
+    if (warp == 0) {
+        // --- TMA producer
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first();
+            for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+                const int rs = s % kRawStages;
+                if (s >= kRawStages &&
+                    !mbar_wait(&raw_free[rs], static_cast<uint32_t>(s / kRawStages - 1) & 1u,
+                               kPWaitLimit)) {
+                    fail();
+                    break;
+                }
+                if (s % kStepsPerSc == 0) {   // a new block of scale bytes
+                    const int b = s / kStepsPerSc, sb = b & 1;
+                    if (b >= 2 && !mbar_wait(&sc_free[sb], static_cast<uint32_t>(b / 2 - 1) & 1u,
+                                             kPWaitLimit)) {
+                        fail();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sc_full[sb], kScBlockBytes);
+                    tma2d(smem_u32(smem + L.sc + sb * kScBlockBytes), &smap, b * 16, r0,
+                          &sc_full[sb], policy);
+                    issued_blocks = b + 1;
+                }
+                const uint32_t raw = smem_u32(smem + L.raw + rs * kRawStageBytes);
+                mbar_arrive_expect_tx(&raw_full[rs], kRawStageBytes);
+                tma2d(raw, &xmap, s * kPK, t0, &raw_full[rs], policy);
+                tma2d(raw + kRawXBytes, &wmap, s * (kPK / 2), r0, &raw_full[rs], policy);
+                issued_steps = s + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // --- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kPM, kPN);
+            for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+                const int cs = s % kConvStages;
+                if (!mbar_wait(&conv_full[cs], static_cast<uint32_t>(s / kConvStages) & 1u,
+                               kPWaitLimit)) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + L.conv + cs * kPStageBytes);
+                const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kPK / 16; ++kk)
+                    umma_bf16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32),
+                              idesc, (s > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&conv_free[cs]);
+                if (s == n_steps - 1) umma_commit(done);
+            }
+        }
+    } else {
+        // --- converters: raw stage -> bf16 operand tiles
+        const int ct = tid - 64;   // 0 .. kConvWarps * 32 - 1
+        constexpr int kCT = kConvWarps * 32;
+        for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+            const int rs = s % kRawStages, cs = s % kConvStages, sb = (s / kStepsPerSc) & 1;
+            bool ok = mbar_wait(&raw_full[rs], static_cast<uint32_t>(s / kRawStages) & 1u,
+                                kPWaitLimit);
+            ok = ok && mbar_wait(&sc_full[sb], static_cast<uint32_t>(s / (2 * kStepsPerSc)) & 1u,
+                                 kPWaitLimit);
+            ok = ok && (s < kConvStages ||
+                        mbar_wait(&conv_free[cs], static_cast<uint32_t>(s / kConvStages - 1) & 1u,
+                                  kPWaitLimit));
+            if (!ok) {
+                fail();
+                break;
+            }
+            const uint8_t* raw = smem + L.raw + rs * kRawStageBytes;
+            const uint8_t* scb = smem + L.sc + sb * kScBlockBytes;
+            const uint32_t a_base = smem_u32(smem + L.conv + cs * kPStageBytes);
+            const uint32_t b_base = a_base + kATileBytes;
+            // A: 1024 chunks (token m, 8 columns j) of f32 -> bf16
+            for (int c = ct; c < kPM * kPK / 8; c += kCT) {
+                const int m = c >> 3, j = c & 7;
+                const float4* src = reinterpret_cast<const float4*>(raw + (m * kPK + 8 * j) * 4);
+                const float4 a = src[0], b = src[1];
+                sts128(a_base + m * 128 + ((j ^ (m & 7)) << 4), pack_bf16x2(a.x, a.y),
+                       pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+            }
+            // B: 2048 chunks (row n, code word j) -> 8 decoded weights in bf16
+            for (int c = ct; c < kPN * kPK / 8; c += kCT) {
+                const int n = c >> 3, j = c & 7;
+                const uint32_t code =
+                    *reinterpret_cast<const uint32_t*>(raw + kRawXBytes + n * (kPK / 2) + 4 * j);
+                const float sc = e8m0_to_f32(scb[n * 16 + (s % kStepsPerSc) * 2 + (j >> 2)]);
+                float v[8];
+                e2m1x8_to_f32(code, v);
+                // a value times a power of two: exact in float and in bfloat16
+                sts128(b_base + n * 128 + ((j ^ (n & 7)) << 4),
+                       pack_bf16x2(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc)),
+                       pack_bf16x2(__fmul_rn(v[2], sc), __fmul_rn(v[3], sc)),
+                       pack_bf16x2(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc)),
+                       pack_bf16x2(__fmul_rn(v[6], sc), __fmul_rn(v[7], sc)));
+            }
+            fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_p(&raw_free[rs]);
+                mbar_arrive_p(&conv_full[cs]);
+                if (s % kStepsPerSc == kStepsPerSc - 1 || s == n_steps - 1) mbar_arrive_p(&sc_free[sb]);
+            }
+        }
+    }
+
+    // --- epilogue: wait for the accumulator, then TMEM -> registers -> Y
+    __syncthreads();
+    if (tid == 0 && !*abort_flag && !mbar_wait(done, 0u, kPWaitLimit)) fail();
+    __syncthreads();
+    if (!*abort_flag) {
+        tc_fence_after();
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        constexpr int kColsPerWarp = kPN / (kPThreads / 128);
+        const int col0 = (warp >> 2) * kColsPerWarp;
+        const int t = t0 + quarter * 32 + lane;
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0 + cc, v);
+            const int rbase = r0 + col0 + cc;
+            if (t < nb) {
+                float* dst = Y + static_cast<size_t>(t) * rows + rbase;
+                if (rbase + 32 <= rows && (rows & 3) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (rbase + i < rows) dst[i] = __uint_as_float(v[i]);
+                }
+            }
+        }
+    } else {
+        // a CTA that gave up: let every copy it started land before it exits
+        // (thread 0 is the producer; waits on completed phases return at once)
+        if (tid == 0) {
+            for (int i = issued_steps - kRawStages; i < issued_steps; ++i)
+                if (i >= 0)
+                    mbar_wait(&raw_full[i % kRawStages],
+                              static_cast<uint32_t>(i / kRawStages) & 1u, kPWaitLimit);
+            for (int b = issued_blocks - 2; b < issued_blocks; ++b)
+                if (b >= 0)
+                    mbar_wait(&sc_full[b & 1], static_cast<uint32_t>(b / 2) & 1u, kPWaitLimit);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_p() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool map2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+           uint64_t outer, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn_p();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+cudaError_t launch_prefill2(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                            float* Y, cudaStream_t s) {
+    const int gpr = cols / kGroup;
+    if (gpr % 16 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0) return cudaErrorNotSupported;
+    CUtensorMap xmap, wmap, smap;
+    const uint8_t* scales = w + static_cast<size_t>(rows) * cols / 2;
+    if (!map2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, X, cols, nb,
+               static_cast<uint64_t>(cols) * 4, kPK, kPM) ||
+        !map2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, cols / 2, rows, cols / 2, kPK / 2, kPN) ||
+        !map2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, gpr, rows, gpr, 16, kPN))
+        return cudaErrorNotSupported;
+    constexpr P2Layout l = p2_layout();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(k_prefill2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(p2_layout().total));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
+    k_prefill2<<<grid, kPThreads, l.total, s>>>(xmap, wmap, smap, rows, cols, nb, Y);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
                               float* Y, cudaStream_t s) {
+    {
+        const cudaError_t e2 = launch_prefill2(w, rows, cols, X, nb, Y, s);
+        if (e2 != cudaErrorNotSupported) return e2;
+        (void)cudaGetLastError();
+    }
     const size_t smem = static_cast<size_t>(kPStages) * kPStageBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
