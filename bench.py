@@ -252,8 +252,25 @@ class Prefill(Workload):
         self.flops_per_step = 2.0 * c.rows * c.cols * c.nb
         self.bytes_per_step = (mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.nb * c.cols +
                                4 * c.nb * c.rows)
+        # dense after dequant through the workspace entry point: W and X to bf16,
+        # then the tcgen05 GEMM (three launches per step)
+        self.ws = torch.empty(mx.mxfp4_mm_bf16_workspace_bytes(c.rows, c.cols, c.nb),
+                              dtype=torch.uint8, device="cuda")
+        self.launches_per_step = 3
+        self.dominant = "mxfp4_mm_bf16_ws (k_w_to_bf16, k_x_to_bf16, k_gemm_bf16)"
+
+    def step(self):
+        c = self.c
+        self.mx.mxfp4_mm_bf16_ws(self.w, c.rows, c.cols, self.X, c.nb, self.Y, self.ws)
+
+
+class PrefillNoWorkspace(Prefill):
+    """The same product through mxfp4_mm (no workspace: k_prefill2, in-kernel conversion)."""
+
+    def __init__(self, mx):
+        super().__init__(mx)
         self.launches_per_step = 1
-        self.dominant = "mxfp4_mm bf16 path"
+        self.dominant = "mxfp4_mm nb=2048 (k_prefill2)"
 
     def step(self):
         c = self.c
@@ -384,7 +401,7 @@ def run_profile(args):
     import mxfp4_dequant_matmul_gb300 as mx
     mx.lib()
     cls = {"decode": DecodeGemv, "decode_fp32": DecodeGemvFp32, "mm8": SmallBatch,
-           "moe": MoeLayer, "prefill": Prefill}
+           "moe": MoeLayer, "prefill": Prefill, "prefill_mm": PrefillNoWorkspace}
     w = cls[args.profile](mx)
     for _ in range(args.warmup):
         w.step()
@@ -405,7 +422,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode_fp32", "mm8", "moe", "prefill"],
+    ap.add_argument("--profile",
+                    choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm"],
                     help="run only this workload's warm-up and timed steps (eagerly, one "
                          "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()

@@ -135,6 +135,22 @@ int mxfp4_mm_fp32(const void* w, int rows, int cols, const float* X, int nb, flo
 int mxfp4_mm_bf16(const void* w, int rows, int cols, const float* X, int nb, float* Y,
                   cudaStream_t stream);
 
+/* Bytes of the workspace mxfp4_mm_bf16_ws needs: a bfloat16 copy of W
+ * (rows*cols*2, rounded up to 256) followed by one of X (nb*cols*2).
+ * 0 for an invalid shape or nb < 1. */
+size_t mxfp4_mm_bf16_workspace_bytes(int rows, int cols, int nb);
+
+/* The same product as mxfp4_mm_bf16 computed densely after dequantisation
+ * ("rlx-cpu 0.2.17 src/gguf_matmul.rs" gguf_matmul_bt_cached: dequantise the
+ * weights once, then a dense GEMM): W is decoded exactly to bfloat16 and X
+ * rounded to nearest-even bfloat16 into `workspace` (device, owned by the
+ * caller, 16-byte aligned, >= mxfp4_mm_bf16_workspace_bytes bytes, rewritten
+ * by every call), then a tensor-core GEMM accumulates in FP32.  Same result
+ * contract and error bound as mxfp4_mm_bf16.  MXFP4_STATUS_WORKSPACE_TOO_SMALL
+ * (nothing launched) if workspace_bytes is short. */
+int mxfp4_mm_bf16_ws(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* p2-style host entry (the page's fn matmat): X and Y are HOST buffers, the
  * weight stays resident on the device.  Copies X to x_dev, runs mxfp4_mm
  * (mxfp4_mv when nb == 1), copies the result back to Y and synchronises the

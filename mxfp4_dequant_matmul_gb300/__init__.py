@@ -14,7 +14,8 @@ import os
 __all__ = [
     "Mxfp4Error", "lib", "library_path", "mxfp4_nbytes", "mxfp4_device_faults",
     "mxfp4_set_launch_overlap", "mxfp4_dequant", "mxfp4_mv",
-    "mxfp4_mm", "mxfp4_mm_fp32", "mxfp4_mm_bf16", "mxfp4_matmat_host",
+    "mxfp4_mm", "mxfp4_mm_fp32", "mxfp4_mm_bf16", "mxfp4_mm_bf16_workspace_bytes",
+    "mxfp4_mm_bf16_ws", "mxfp4_matmat_host",
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
     "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
 ]
@@ -38,6 +39,8 @@ _SIG = {
     "mxfp4_mm": (_I, [_P, _I, _I, _P, _I, _P, _P]),
     "mxfp4_mm_fp32": (_I, [_P, _I, _I, _P, _I, _P, _P]),
     "mxfp4_mm_bf16": (_I, [_P, _I, _I, _P, _I, _P, _P]),
+    "mxfp4_mm_bf16_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "mxfp4_mm_bf16_ws": (_I, [_P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "mxfp4_matmat_host": (_I, [_P, _I, _I, _P, _I, _P, _P, _P, _P]),
     "mxfp4_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "mxfp4_moe_gate_up": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _P]),
@@ -143,6 +146,18 @@ def mxfp4_mm_fp32(w, rows, cols, X, nb, Y, stream=None):
 def mxfp4_mm_bf16(w, rows, cols, X, nb, Y, stream=None):
     _check("mxfp4_mm_bf16", lib().mxfp4_mm_bf16(_addr(w), rows, cols, _addr(X), nb,
                                                 _addr(Y), _stream(stream)))
+
+
+def mxfp4_mm_bf16_workspace_bytes(rows, cols, nb) -> int:
+    return int(lib().mxfp4_mm_bf16_workspace_bytes(rows, cols, nb))
+
+
+def mxfp4_mm_bf16_ws(w, rows, cols, X, nb, Y, workspace, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mxfp4_mm_bf16_ws", lib().mxfp4_mm_bf16_ws(_addr(w), rows, cols, _addr(X), nb,
+                                                      _addr(Y), _addr(workspace), ws_bytes,
+                                                      _stream(stream)))
 
 
 def mxfp4_matmat_host(w, rows, cols, X_host, nb, Y_host, x_dev, y_dev, stream=None):

@@ -36,6 +36,12 @@ cudaError_t launch_mm_tc(const uint8_t* w, int rows, int cols, const float* X, i
 cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
                               float* Y, cudaStream_t s);
 
+// Dense after dequant: W and X to bf16 in the workspace, then a TMA-fed tcgen05
+// GEMM (prefill.cu).
+size_t dense_ws_bytes(int rows, int cols, int nb);
+cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                            float* Y, void* ws, cudaStream_t s);
+
 // Routed experts.  The workspace layout is owned by moe.cu.
 size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter);
 cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,

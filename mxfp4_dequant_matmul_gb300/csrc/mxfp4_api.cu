@@ -122,6 +122,20 @@ int mxfp4_mm_bf16(const void* w, int rows, int cols, const float* X, int nb, flo
     return from_cuda(mxk::launch_mm_tcgen05(u8(w), rows, cols, X, nb, Y, stream));
 }
 
+size_t mxfp4_mm_bf16_workspace_bytes(int rows, int cols, int nb) {
+    if (check_shape(rows, cols) != MXFP4_STATUS_OK || nb < 1) return 0;
+    return mxk::dense_ws_bytes(rows, cols, nb);
+}
+
+int mxfp4_mm_bf16_ws(const void* w, int rows, int cols, const float* X, int nb, float* Y,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));
+    MXFP4_TRY(check_ptr(workspace));
+    if (workspace_bytes < mxk::dense_ws_bytes(rows, cols, nb))
+        return MXFP4_STATUS_WORKSPACE_TOO_SMALL;
+    return from_cuda(mxk::launch_mm_dense(u8(w), rows, cols, X, nb, Y, workspace, stream));
+}
+
 int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
              cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, X, nb, Y));

@@ -610,6 +610,210 @@ cudaError_t launch_prefill2(const uint8_t* w, int rows, int cols, const float* X
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Dense after dequant ("rlx-cpu 0.2.17 src/gguf_matmul.rs" gguf_matmul_bt_cached:
+// dequantise once, then a dense GEMM): W is decoded to bfloat16 and X rounded
+// to bfloat16 into a caller's workspace by two elementwise kernels, then a
+// plain tcgen05 GEMM streams both operands with TMA (128-byte swizzle, the
+// layout the MMA descriptors read) through a 4-stage ring; warp 0 issues the
+// copies, warp 1 the MMAs, every warp reads the accumulator back.
+
+// Eight weights per code word: exact bfloat16 (a value times a power of two).
+__global__ void __launch_bounds__(256) k_w_to_bf16(const uint8_t* __restrict__ w, int rows,
+                                                   int cols, uint4* __restrict__ out) {
+    const int wpr = cols / 8;   // code words per row
+    const int gpr = cols / kGroup;
+    const size_t n = static_cast<size_t>(rows) * wpr;
+    const uint8_t* scales = w + static_cast<size_t>(rows) * cols / 2;
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(w);
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const size_t r = i / wpr;
+        const int q = static_cast<int>(i - r * wpr);
+        const float sc = e8m0_to_f32(__ldg(scales + r * gpr + q / 4));
+        float v[8];
+        e2m1x8_to_f32(__ldg(words + i), v);
+        out[i] = make_uint4(pack_bf16x2(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc)),
+                            pack_bf16x2(__fmul_rn(v[2], sc), __fmul_rn(v[3], sc)),
+                            pack_bf16x2(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc)),
+                            pack_bf16x2(__fmul_rn(v[6], sc), __fmul_rn(v[7], sc)));
+    }
+}
+
+// Four activations at a time, rounded to nearest-even bfloat16.
+__global__ void __launch_bounds__(256) k_x_to_bf16(const float4* __restrict__ x, size_t n4,
+                                                   uint2* __restrict__ out) {
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const float4 a = __ldg(x + i);
+        out[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    }
+}
+
+constexpr int kGStages = 4;
+
+__device__ __forceinline__ void tma2d_g(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                        uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_gemm_bf16(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                int rows, int cols, int nb, float* __restrict__ Y) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t full[kGStages], empty[kGStages], done;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_word;
+    volatile int* abort_flag = &abort_word;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * kPN;      // weight rows of this tile
+    const int t0 = blockIdx.y * kPM;      // tokens of this tile
+    const int n_steps = (cols + kPK - 1) / kPK;
+    int issued = 0;   // (producer) stages started
+
+    if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+    if (tid == 0) {
+        for (int i = 0; i < kGStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicOr(&g_fault_prefill, 1);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // --- TMA producer: A tile (128 tokens x 64) and B tile (256 rows x 64)
+        const uint64_t policy = l2_evict_first();
+        for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+            const int st = s % kGStages;
+            if (s >= kGStages &&
+                !mbar_wait(&empty[st], static_cast<uint32_t>(s / kGStages - 1) & 1u, kPWaitLimit)) {
+                fail();
+                break;
+            }
+            const uint32_t a = smem_u32(smem + st * kPStageBytes);
+            mbar_arrive_expect_tx(&full[st], kPStageBytes);
+            tma2d_g(a, &amap, s * kPK, t0, &full[st], policy);
+            tma2d_g(a + kATileBytes, &bmap, s * kPK, r0, &full[st], policy);
+            issued = s + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // --- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16(kPM, kPN);
+        for (int s = 0; s < n_steps && !*abort_flag; ++s) {
+            const int st = s % kGStages;
+            if (!mbar_wait(&full[st], static_cast<uint32_t>(s / kGStages) & 1u, kPWaitLimit)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + st * kPStageBytes);
+            const uint32_t b_base = a_base + kATileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kPK / 16; ++kk)
+                umma_bf16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc,
+                          (s > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&empty[st]);
+            if (s == n_steps - 1) umma_commit(&done);
+        }
+    }
+
+    // --- epilogue: wait for the accumulator, then TMEM -> registers -> Y
+    __syncthreads();
+    if (tid == 0 && !*abort_flag && !mbar_wait(&done, 0u, kPWaitLimit)) fail();
+    __syncthreads();
+    if (!*abort_flag) {
+        tc_fence_after();
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        constexpr int kColsPerWarp = kPN / (kPThreads / 128);
+        const int col0 = (warp >> 2) * kColsPerWarp;
+        const int t = t0 + quarter * 32 + lane;
+#pragma unroll 1
+        for (int cc = 0; cc < kColsPerWarp; cc += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0 + cc, v);
+            const int rbase = r0 + col0 + cc;
+            if (t < nb) {
+                float* dst = Y + static_cast<size_t>(t) * rows + rbase;
+                if (rbase + 32 <= rows && (rows & 3) == 0) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (rbase + i < rows) dst[i] = __uint_as_float(v[i]);
+                }
+            }
+        }
+    } else if (tid == 0) {
+        // a CTA that gave up: let the copies it started land before it exits
+        for (int i = issued - kGStages; i < issued; ++i)
+            if (i >= 0)
+                mbar_wait(&full[i % kGStages], static_cast<uint32_t>(i / kGStages) & 1u,
+                          kPWaitLimit);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A [outer][inner] bf16 matrix as a 2-D tensor map, tiles of 64 x box_outer
+// elements (128-byte rows, 128-byte swizzle).
+bool bf16_map(CUtensorMap* map, const void* base, int inner, int outer, uint32_t box_outer) {
+    auto fn = encode_fn_g();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+    const cuuint32_t box[2] = {kPK, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int grid_for(size_t n, int per_thread_items) {
+    const size_t blocks = (n / per_thread_items + 255) / 256;
+    return static_cast<int>(blocks < 4096 ? (blocks > 0 ? blocks : 1) : 4096);
+}
+
 }  // namespace
 
 cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float* X, int nb,
@@ -625,6 +829,40 @@ cudaError_t launch_mm_tcgen05(const uint8_t* w, int rows, int cols, const float*
     if (e != cudaSuccess) return e;
     const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
     k_prefill<<<grid, kPThreads, smem, s>>>(w, rows, cols, X, nb, Y);
+    return cudaGetLastError();
+}
+
+size_t dense_ws_bytes(int rows, int cols, int nb) {
+    const size_t wb = (static_cast<size_t>(rows) * cols * 2 + 255) / 256 * 256;
+    return wb + static_cast<size_t>(nb) * cols * 2;
+}
+
+cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X, int nb,
+                            float* Y, void* ws, cudaStream_t s) {
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    uint8_t* xb = wb + (static_cast<size_t>(rows) * cols * 2 + 255) / 256 * 256;
+    CUtensorMap amap, bmap;
+    if (!bf16_map(&amap, xb, cols, nb, kPM) || !bf16_map(&bmap, wb, cols, rows, kPN))
+        return cudaErrorNotSupported;
+    const size_t nw = static_cast<size_t>(rows) * cols / 8;
+    k_w_to_bf16<<<grid_for(nw, 4), 256, 0, s>>>(w, rows, cols, reinterpret_cast<uint4*>(wb));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t nx4 = static_cast<size_t>(nb) * cols / 4;
+    k_x_to_bf16<<<grid_for(nx4, 4), 256, 0, s>>>(reinterpret_cast<const float4*>(X), nx4,
+                                                 reinterpret_cast<uint2*>(xb));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    const size_t smem = static_cast<size_t>(kGStages) * kPStageBytes + 1024;
+    std::call_once(once, [smem] {
+        attr_err = cudaFuncSetAttribute(k_gemm_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
+    k_gemm_bf16<<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
     return cudaGetLastError();
 }
 

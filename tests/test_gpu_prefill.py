@@ -79,3 +79,60 @@ def test_prefill_config_sampled_outputs(mx):
     nrmse = np.sqrt(((Y[tok, row] - ref32) ** 2).sum() / (ref32 ** 2).sum())
     print(f"prefill worst err/tol {worst:.3g}; nrmse vs f32-X oracle {nrmse:.3e}")
     assert nrmse < 1e-2
+
+
+def run_ws(mx, w_h, rows, cols, X, nb):
+    import torch
+    Y = empty(nb * rows)
+    nbytes = mx.mxfp4_mm_bf16_workspace_bytes(rows, cols, nb)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    mx.mxfp4_mm_bf16_ws(to_dev(w_h), rows, cols, to_dev(X), nb, Y, ws)
+    return host(Y).reshape(nb, rows)
+
+
+@pytest.mark.parametrize("rows,cols,nb", [(256, 512, 100), (300, 2304, 77), (64, 64, 129),
+                                          (130, 4096, 65), (96, 160, 1)])
+def test_dense_after_dequant_small_shapes(mx, rows, cols, nb):
+    seed = rows * 5 + cols + nb
+    w_h = synth.mxfp4_matrix(rows, cols, seed, 118, 130)
+    X = synth.normal_f32(seed, nb * cols).reshape(nb, cols)
+    Y = run_ws(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, oracle.round_bf16(X), nb)
+    assert_within(Y, ref, l1, REL_BF16, "dense after dequant")
+    assert_within(Y, ref, l1, REL_FP32, "dense after dequant, FP32 bound")
+
+
+def test_dense_after_dequant_nan_subnormal_and_exact_inputs(mx):
+    cfg = synth.TINY
+    w_h = cfg.weights()
+    X = synth.normal_f32(13, 80 * cfg.cols).reshape(80, cfg.cols)
+    Y = run_ws(mx, w_h, cfg.rows, cfg.cols, X, 80)
+    ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, oracle.round_bf16(X), 80)
+    assert np.isnan(Y[:, 250]).all()
+    assert_within(Y, ref, l1, REL_BF16, "tiny dense")
+    rows, cols, nb = 256, 1024, 192
+    w_h = synth.mxfp4_matrix(rows, cols, 22, 126, 128)
+    X = synth.int_activations(5, nb * cols).reshape(nb, cols)    # exact in bf16
+    Y = run_ws(mx, w_h, rows, cols, X, nb)
+    ref, _ = oracle.matmat(w_h, rows, cols, X, nb)
+    assert np.array_equal(Y.astype(np.float64), ref)
+
+
+def test_dense_after_dequant_prefill_config_samples_and_short_workspace(mx):
+    import torch
+    cfg = synth.PREFILL
+    w_h, X = cfg.weights(), cfg.activations()
+    Y = run_ws(mx, w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    rng = np.random.default_rng(1)
+    n = 2000
+    tok = np.concatenate([rng.integers(0, cfg.nb, n - 2), [0, cfg.nb - 1]]).astype(np.int32)
+    row = np.concatenate([rng.integers(0, cfg.rows, n - 2), [0, cfg.rows - 1]]).astype(np.int32)
+    ref, l1 = oracle.matmat_samples(w_h, cfg.rows, cfg.cols, oracle.round_bf16(X), tok, row)
+    assert_within(Y[tok, row], ref, l1, REL_FP32, "prefill dense samples")
+    # a workspace one byte short is refused and nothing runs
+    nbytes = mx.mxfp4_mm_bf16_workspace_bytes(64, 512, 8)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    w_small = to_dev(synth.mxfp4_matrix(64, 512, 3, 118, 130))
+    x_small = to_dev(synth.normal_f32(3, 8 * 512))
+    with pytest.raises(mx.Mxfp4Error):
+        mx.mxfp4_mm_bf16_ws(w_small, 64, 512, x_small, 8, empty(8 * 64), ws, nbytes - 1)
