@@ -699,8 +699,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     };
 
     if (warp == 0 && lane == 0) {
-        // --- TMA producer: A tile (128 tokens x 64) and B tile (256 rows x 64)
-        const uint64_t policy = l2_evict_first();
+        // --- TMA producer: A tile (128 tokens x 64) and B tile (256 rows x 64);
+        // every tile is read by 16 CTAs, so both operands should stay in L2
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
         for (int s = 0; s < n_steps && !*abort_flag; ++s) {
             const int st = s % kGStages;
             if (s >= kGStages &&
