@@ -98,11 +98,14 @@ size_t mxfp4_nbytes(int rows, int cols);
  * with cortiq_core::mxfp4::dequant as their reference.) */
 int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t stream);
 
-/* Matrix-vector product, one token: y[r] = sum_c W[r][c] * x[c], FP32
- * arithmetic on the CUDA cores (per group: the 32 code values dotted with x,
- * then scaled; the row's group partials reduced across a warp).
- * x: [cols] floats, y: [rows] floats.  Error bound: |y - exact| <= 1e-5 *
- * sum_c |W[r][c] x[c]| (a NaN scale makes the row NaN).  (PEROP mxfp4_mv.) */
+/* Matrix-vector product, one token: y[r] = sum_c W[r][c] * x[c].  Each group's
+ * 32 decoded weights (exact in f16) are dotted with x on the tensor cores
+ * (mma.sync; x split into f16 halves hi + lo of x * 2^p, so every product is
+ * exact), the group sum is scaled by its E8M0 factor and 2^-p in FP32 and
+ * added to the row's FP32 sum.  x: [cols] floats, y: [rows] floats.  Error
+ * bound: |y - exact| <= 1e-5 * sum_c |W[r][c] x[c]| (a NaN scale makes the
+ * row NaN).  Deterministic: the order of every sum depends on the shape
+ * only.  (PEROP mxfp4_mv.) */
 int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
              cudaStream_t stream);
 
@@ -110,18 +113,22 @@ int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
  * X: [nb, cols] row-major floats, Y: [nb, rows] (the page's matmat output
  * layout).  Dispatch on nb:
  *   nb <= MXFP4_MM_SMALL_MAX: the small-batch path -- each weight group is
- *     decoded once and applied to up to 8 tokens at a time (PEROP mxfp4_mm);
- *     same error bound as mxfp4_mv.
+ *     decoded once and applied to up to 4 tokens per pass over the weights
+ *     (PEROP mxfp4_mm shares one decode by up to 8); the arithmetic of
+ *     mxfp4_mv, so per token the result equals mxfp4_mv on that token bit
+ *     for bit, whatever the rest of the batch (the page's device test:
+ *     "the batch equal to the matvec per token bit for bit").
  *   nb >  MXFP4_MM_SMALL_MAX: the tensor-core path of mxfp4_mm_bf16 (below):
  *     X is rounded to bfloat16 first. */
 #define MXFP4_MM_SMALL_MAX 64
 int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
              cudaStream_t stream);
 
-/* The small-batch path for any nb >= 1, regardless of MXFP4_MM_SMALL_MAX.  Per
- * token the result is bit-identical to mxfp4_mv on that token (same group walk,
- * same reduction tree), the invariant the page's device test checks
- * ("the batch equal to the matvec per token bit for bit"). */
+/* The same product in plain FP32 on the CUDA cores, any nb >= 1: per group the
+ * decoded values dotted with x in FP32 (two FMA chains), scaled, the row's
+ * group partials reduced across a warp; chunks of 8 tokens share each decode.
+ * Same error bound as mxfp4_mv.  Per token the result is bit-identical to this
+ * function with nb = 1 on that token (same group walk, same reduction tree). */
 int mxfp4_mm_fp32(const void* w, int rows, int cols, const float* X, int nb, float* Y,
                   cudaStream_t stream);
 
