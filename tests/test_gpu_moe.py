@@ -78,6 +78,21 @@ def test_gate_up_expert_with_more_than_eight_pairs(mx):
     check_gate_up(host(act), ref, ids, E)
 
 
+def test_gate_up_and_layer_when_rows_are_too_wide_for_the_tensor_path(mx):
+    # 144 groups per row of gate/up (more than the tensor-core passes stage):
+    # those run the FP32 expert passes; the down pass (64 groups) stays on the
+    # tensor cores
+    E, hidden, inter, T, K = 4, 4608, 64, 6, 2
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 17)
+    act, _ = run_gate_up(mx, cfg, gate, up, x, ids)
+    ref = oracle.moe_gate_up(gate, up, cfg.gu_stride, E, hidden, inter, x, T, K, ids)
+    check_gate_up(host(act), ref, ids, E)
+    y, _ = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
+                             x, T, K, ids, wts)
+    assert_within(y, ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32, "wide MoE layer")
+
+
 @pytest.mark.parametrize("E,hidden,inter,T,K,seed", [
     (8, 96, 64, 12, 3, 7), (64, 2880, 2880, 32, 4, 3)])
 def test_down_stage_on_injected_act(mx, E, hidden, inter, T, K, seed):
