@@ -661,31 +661,57 @@ __device__ __forceinline__ void tma2d_g(uint32_t dst, const CUtensorMap* map, in
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_g(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Persistent: CTA c takes tiles c, c + grid, ... (tile = TN weight rows x 128
+// tokens, token tiles fastest).  Warp 0 streams both operands of every tile
+// through the stage ring, warp 1 issues the MMAs into one of two 256-column
+// TMEM accumulators (tile j into j % 2), and warps 8..15 read a finished
+// accumulator back and store it while the next tile's MMAs run.
+constexpr int kEpiWarp0 = 8;                       // first epilogue warp
+constexpr int kEpiWarps = kPThreads / 32 - kEpiWarp0;   // 8: two per TMEM lane quarter
+
+template <int TN>
 __global__ void __launch_bounds__(kPThreads, 1)
     k_gemm_bf16(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                 int rows, int cols, int nb, float* __restrict__ Y) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t full[kGStages], empty[kGStages], done;
+    __shared__ uint64_t full[kGStages], empty[kGStages], acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_word;
     volatile int* abort_flag = &abort_word;
+    constexpr uint32_t kBBytes = TN * kPK * 2, kStage = kATileBytes + kBBytes;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int r0 = blockIdx.x * kPN;      // weight rows of this tile
-    const int t0 = blockIdx.y * kPM;      // tokens of this tile
     const int n_steps = (cols + kPK - 1) / kPK;
-    int issued = 0;   // (producer) stages started
+    const int n_tt = (nb + kPM - 1) / kPM;
+    const int n_tiles = (rows + TN - 1) / TN * n_tt;
+    int issued = 0;   // (producer) stages started, over all tiles
 
-    if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+    if (warp == 0) tmem_alloc(&tmem_base, 2 * kTmemCols);
     if (tid == 0) {
         for (int i = 0; i < kGStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        mbar_init(&done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kEpiWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -699,75 +725,105 @@ __global__ void __launch_bounds__(kPThreads, 1)
     };
 
     if (warp == 0 && lane == 0) {
-        // --- TMA producer: A tile (128 tokens x 64) and B tile (256 rows x 64);
-        // every tile is read by 16 CTAs, so both operands should stay in L2
-        uint64_t policy;
+        // --- TMA producer: A tile (128 tokens x 64) and B tile (TN rows x 64)
+        uint64_t policy;   // every tile is read by many CTAs: keep both operands in L2
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-        for (int s = 0; s < n_steps && !*abort_flag; ++s) {
-            const int st = s % kGStages;
-            if (s >= kGStages &&
-                !mbar_wait(&empty[st], static_cast<uint32_t>(s / kGStages - 1) & 1u, kPWaitLimit)) {
-                fail();
-                break;
+        for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+            const int r0 = (tile / n_tt) * TN, t0 = (tile % n_tt) * kPM;
+            for (int s = 0; s < n_steps && !*abort_flag; ++s, ++issued) {
+                const int st = issued % kGStages;
+                if (issued >= kGStages &&
+                    !mbar_wait(&empty[st], static_cast<uint32_t>(issued / kGStages - 1) & 1u,
+                               kPWaitLimit)) {
+                    fail();
+                    break;
+                }
+                const uint32_t a = smem_u32(smem + st * kStage);
+                mbar_arrive_expect_tx(&full[st], kStage);
+                tma2d_g(a, &amap, s * kPK, t0, &full[st], policy);
+                tma2d_g(a + kATileBytes, &bmap, s * kPK, r0, &full[st], policy);
             }
-            const uint32_t a = smem_u32(smem + st * kPStageBytes);
-            mbar_arrive_expect_tx(&full[st], kPStageBytes);
-            tma2d_g(a, &amap, s * kPK, t0, &full[st], policy);
-            tma2d_g(a + kATileBytes, &bmap, s * kPK, r0, &full[st], policy);
-            issued = s + 1;
         }
     } else if (warp == 1 && lane == 0) {
         // --- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16(kPM, kPN);
-        for (int s = 0; s < n_steps && !*abort_flag; ++s) {
-            const int st = s % kGStages;
-            if (!mbar_wait(&full[st], static_cast<uint32_t>(s / kGStages) & 1u, kPWaitLimit)) {
+        constexpr uint32_t idesc = idesc_bf16(kPM, TN);
+        int used = 0;   // stages consumed, over all tiles
+        int j = 0;      // this CTA's tile count
+        for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++j) {
+            const int ab = j & 1;
+            if (j >= 2 && !mbar_wait(&acc_empty[ab], static_cast<uint32_t>((j >> 1) - 1) & 1u,
+                                     kPWaitLimit)) {
                 fail();
                 break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + st * kPStageBytes);
-            const uint32_t b_base = a_base + kATileBytes;
+            const uint32_t d = tmem + ab * kTmemCols;
+            for (int s = 0; s < n_steps; ++s, ++used) {
+                const int st = used % kGStages;
+                if (!mbar_wait(&full[st], static_cast<uint32_t>(used / kGStages) & 1u,
+                               kPWaitLimit)) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + st * kStage);
+                const uint32_t b_base = a_base + kATileBytes;
 #pragma unroll
-            for (int kk = 0; kk < kPK / 16; ++kk)
-                umma_bf16(tmem, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc,
-                          (s > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&empty[st]);
-            if (s == n_steps - 1) umma_commit(&done);
+                for (int kk = 0; kk < kPK / 16; ++kk)
+                    umma_bf16(d, sw128_desc(a_base + kk * 32), sw128_desc(b_base + kk * 32), idesc,
+                              (s > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&empty[st]);
+            }
+            if (*abort_flag) break;
+            umma_commit(&acc_full[ab]);
+        }
+    } else if (warp >= kEpiWarp0) {
+        // --- epilogue: accumulator j % 2 -> Y, then hand it back
+        const int ew = warp - kEpiWarp0;
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const int half = ew >> 2;                // columns half*TN/2 ..
+        constexpr int kCols = TN / 2;            // 128 or 112
+        int j = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, ++j) {
+            const int ab = j & 1;
+            if (!mbar_wait(&acc_full[ab], static_cast<uint32_t>(j >> 1) & 1u, kPWaitLimit)) {
+                fail();
+                break;
+            }
+            tc_fence_after();
+            const int r0 = (tile / n_tt) * TN, t0 = (tile % n_tt) * kPM;
+            const int t = t0 + quarter * 32 + lane;
+            const uint32_t src = tmem + ab * kTmemCols + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 half * kCols;
+#pragma unroll 1
+            for (int cc = 0; cc < kCols; cc += 8) {
+                uint32_t v[8];
+                tmem_ld8(src + cc, v);
+                const int rbase = r0 + half * kCols + cc;
+                if (t < nb) {
+                    float* dst = Y + static_cast<size_t>(t) * rows + rbase;
+                    if (rbase + 8 <= rows && (rows & 3) == 0) {
+                        *reinterpret_cast<float4*>(dst) =
+                            make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]),
+                                        __uint_as_float(v[2]), __uint_as_float(v[3]));
+                        *reinterpret_cast<float4*>(dst + 4) =
+                            make_float4(__uint_as_float(v[4]), __uint_as_float(v[5]),
+                                        __uint_as_float(v[6]), __uint_as_float(v[7]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (rbase + i < rows) dst[i] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_g(&acc_empty[ab]);
         }
     }
 
-    // --- epilogue: wait for the accumulator, then TMEM -> registers -> Y
     __syncthreads();
-    if (tid == 0 && !*abort_flag && !mbar_wait(&done, 0u, kPWaitLimit)) fail();
-    __syncthreads();
-    if (!*abort_flag) {
-        tc_fence_after();
-        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-        constexpr int kColsPerWarp = kPN / (kPThreads / 128);
-        const int col0 = (warp >> 2) * kColsPerWarp;
-        const int t = t0 + quarter * 32 + lane;
-#pragma unroll 1
-        for (int cc = 0; cc < kColsPerWarp; cc += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + col0 + cc, v);
-            const int rbase = r0 + col0 + cc;
-            if (t < nb) {
-                float* dst = Y + static_cast<size_t>(t) * rows + rbase;
-                if (rbase + 32 <= rows && (rows & 3) == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + i) =
-                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                        __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (rbase + i < rows) dst[i] = __uint_as_float(v[i]);
-                }
-            }
-        }
-    } else if (tid == 0) {
+    if (*abort_flag && tid == 0) {
         // a CTA that gave up: let the copies it started land before it exits
         for (int i = issued - kGStages; i < issued; ++i)
             if (i >= 0)
@@ -778,7 +834,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, 2 * kTmemCols);
     }
 }
 
@@ -843,8 +899,18 @@ cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X
                             float* Y, void* ws, cudaStream_t s) {
     uint8_t* wb = static_cast<uint8_t*>(ws);
     uint8_t* xb = wb + (static_cast<size_t>(rows) * cols * 2 + 255) / 256 * 256;
+    // weight rows per tile: 256, or 224 when that fills whole waves better
+    // (rounds of tiles over the SMs x rows per tile)
+    const int n_tt = (nb + kPM - 1) / kPM;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        sms = 1;
+    auto tiles_of = [&](int tn) { return static_cast<long>((rows + tn - 1) / tn) * n_tt; };
+    auto cost = [&](int tn) { return (tiles_of(tn) + sms - 1) / sms * tn; };
+    const int tn = cost(224) < cost(256) ? 224 : 256;
     CUtensorMap amap, bmap;
-    if (!bf16_map(&amap, xb, cols, nb, kPM) || !bf16_map(&bmap, wb, cols, rows, kPN))
+    if (!bf16_map(&amap, xb, cols, nb, kPM) || !bf16_map(&bmap, wb, cols, rows, tn))
         return cudaErrorNotSupported;
     const size_t nw = static_cast<size_t>(rows) * cols / 8;
     k_w_to_bf16<<<grid_for(nw, 4), 256, 0, s>>>(w, rows, cols, reinterpret_cast<uint4*>(wb));
@@ -857,14 +923,23 @@ cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X
     if (e != cudaSuccess) return e;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    const size_t smem = static_cast<size_t>(kGStages) * kPStageBytes + 1024;
+    const size_t smem = static_cast<size_t>(kGStages) * kPStageBytes + 1024;   // (tn <= 256)
     std::call_once(once, [smem] {
-        attr_err = cudaFuncSetAttribute(k_gemm_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(k_gemm_bf16<256>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(k_gemm_bf16<224>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
-    k_gemm_bf16<<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
+    const long tiles = tiles_of(tn);
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    if (tn == 224)
+        k_gemm_bf16<224><<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
+    else
+        k_gemm_bf16<256><<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
     return cudaGetLastError();
 }
 
