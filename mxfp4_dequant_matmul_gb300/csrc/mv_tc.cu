@@ -12,25 +12,29 @@
 // mma.sync m16n8k16; the activations are the B operand, each token's x split
 // into f16 halves hi = f16(x 2^p) and lo = f16(x 2^p - hi) (p one power of two
 // per token and K-slice, putting the slice's largest |x| in [2^14, 2^15)).
-// Column 2n of B is token n's hi, column 2n + 1 its lo, so one MMA serves four
-// tokens.  Every product of an E2M1 value with an f16 is exact in the FP32
-// accumulator.  Each group (32 elements) is two MMAs per 16 rows into a fresh
-// accumulator; hi + lo is taken back by 2^-p and multiplied by the group's
-// scale in FP32, and the result is added to the row's FP32 sum: any scale byte
-// is handled exactly (255 gives NaN) and no partial sum overflows unless the
-// result does.
+// Every product of an E2M1 value with an f16 is exact in the FP32 accumulator.
 //
 // Register layout: lane (g = lane / 4, t = lane % 4) reads code word t of rows
-// g and g + 8 of a group; the four f16 pairs of that word are the A registers
-// of the group's two MMAs (pairs 0, 1 for the first, 2, 3 for the second), and
-// the B registers of lane (2n + h, t) are the same eight elements of token n's
-// hi (h = 0) or lo (h = 1).  Nothing moves between lanes.
+// g and g + 8 (and g + 16, g + 24) of a group; the four f16 pairs of that word
+// are its A registers of the group's two MMAs per 16 rows.  B columns 2c, 2c + 1
+// are (hi, lo) of column set c = s NT + n: token n of group slot s.  GP = 4 / NT
+// consecutive groups share one accumulator, group j0 + s putting its x in the
+// columns of slot s only (the other columns are zero, so its MMAs add exact
+// zeros there): after the GP groups, D columns 2t, 2t + 1 of every row hold
+// group j0 + t / NT's hi and lo dot products for token t % NT alone -- for
+// every token count exactly the values a fresh accumulator per group gives.
+// hi + lo is then taken back by 2^-p, multiplied by the group's E8M0 scale and
+// added to one of four FP32 sums per row and token, r = group mod 4 (in group
+// order), and the four are added as ((P0 + P1) + P2) + P3 at the end.  So the
+// arithmetic per token is the same for one, two or four tokens: the batched
+// product equals the matvec bit for bit.  Any scale byte is handled exactly
+// (255 gives NaN) and no partial sum overflows unless the result does.
 //
 // Data movement: a unit is 32 rows x 8 groups (32 rows x 128 code bytes), one
 // TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) into a ring of two
-// to four stages per warp (as deep as shared memory allows).  A CTA owns up to 128 rows; its warps split them into 32-row
-// units and the K range into equal chunk ranges, each warp keeping its rows'
-// sums in registers over its chunks.  The partial sums are added in chunk
+// to four stages per warp (as deep as shared memory allows).  A CTA owns up to
+// 128 rows; its warps split them into 32-row units and the K range into equal
+// chunk ranges, each warp keeping its rows' sums in registers over its chunks.  The partial sums are added in chunk
 // order.  When the activations of a whole row do not fit in shared memory, a
 // cluster of CTAs splits the groups and adds its partial sums in rank order
 // through distributed shared memory.  The order of every sum depends on the
@@ -111,6 +115,33 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator in.
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+__device__ __forceinline__ uint4 lds128_m(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+
+// Four 8 x 16-byte matrices: lane (g, t) gets word t of row g of matrix i in
+// r[i]; lanes 8i .. 8i + 7 give the row addresses of matrix i.
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a)
+                 : "memory");
+}
+
 // Shared memory (offsets from a 1024-byte aligned base).
 struct MvLayout {
     uint32_t lut, xf, sc, sc_pitch, part, fin, misc, bars, ring, total;
@@ -120,10 +151,15 @@ __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, in
     l.lut = 0;                                                        // [256] f32
     l.xf = 1024;                                                      // [ng][8 NT] uint4
     l.sc = l.xf + static_cast<uint32_t>(ng_max) * 128 * NT;           // [rows][pitch] u8
+    // an odd number of 16-byte words per row: eight rows' scale bytes of a unit
+    // fall in eight different bank groups
     l.sc_pitch = (static_cast<uint32_t>(ng_max) + 15u) & ~15u;
+    if ((l.sc_pitch / 16u) % 2u == 0u) l.sc_pitch += 16u;
     l.part = l.sc + static_cast<uint32_t>(ru_cta) * kRowsU * l.sc_pitch;   // [warps][32][NT]
     l.part = (l.part + 15u) & ~15u;
-    l.fin = l.part + kWarpsM * kRowsU * NT * 4;                        // [rows][NT]
+    // [rows][NT]; zero during the units: its bytes 32 .. 47 are the B values of
+    // the lanes that hold none
+    l.fin = l.part + kWarpsM * kRowsU * NT * 4;
     l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[4], tmax[4]
     l.bars = (l.misc + 64 + 7u) & ~7u;
     l.ring = (l.bars + kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
@@ -192,6 +228,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (overlap) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < NT) tmax[tid] = 0u;
     if (tid == 0) *not_plain = 0;
+    for (int i = tid; i < ru_cta * kRowsU * NT / 4; i += kThreadsM)
+        reinterpret_cast<uint4*>(fin)[i] = make_uint4(0u, 0u, 0u, 0u);
 
     // --- prologue: E8M0 table, scale bytes, activations
     const int nrow = min(n_ru * kRowsU, rows - row0);
@@ -331,14 +369,26 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     __syncthreads();
 
     // --- this warp's units
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24 of the unit, token t
+    constexpr int GP = 4 / NT;   // groups sharing one accumulator
+    const int slot = t / NT, tok = t % NT;   // D columns 2t, 2t + 1: group slot, token
+    // acc[q][i]: row g + 8q, token tok, sum r = slot + GP i (groups j, j mod 4 = r)
+    float acc[4][NT];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int i = 0; i < NT; ++i) acc[q][i] = 0.0f;
     // hi + lo of a group carries the factor 2^p: undone before the scale, so
-    // that no partial sum leaves the float range unless the result does
-    const int p_t = pexp[t < NT ? t : 0];
+    // that no partial sum leaves the float range unless the result does; the
+    // 2^p domain is kept only when it is not below the true one (p >= 0, the
+    // token's |x| below 2^15), so that it adds no underflow either
+    const int p_t = pexp[tok];
     const float pinv = exp2i_m(-p_t);
-    // the 2^p domain is kept only when it is not below the true one (p >= 0,
-    // the token's |x| below 2^15), so that it adds no underflow either
     const bool plain = *not_plain == 0 && p_t >= 0;
+    // B: lanes 8 NT s .. 8 NT s + 8 NT - 1 hold the fragment of group slot s
+    const int b_slot = lane / (8 * NT);
+    const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * NT)) * 16;
+    const uint32_t zero_lane = smem_u32(fin) + 32;
+    const uint32_t sel0 = 0x4044u + (static_cast<uint32_t>(slot) << 8);   // byte slot -> byte 2
     bool failed = false;
     int k = 0;
     const uint8_t* scr = sc_s + static_cast<size_t>(my_ru * kRowsU + g) * L.sc_pitch;
@@ -349,6 +399,9 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             break;
         }
         const uint8_t* stg = ring + st * kStageM;
+        // this lane's row (lane) of the tile, chunk 0 after the swizzle; chunk j
+        // is at that address ^ (j << 4) (the tile is 1024-byte aligned)
+        const uint32_t row_addr = smem_u32(stg) + lane * 128 + ((lane & 7) << 4);
         const int gc0 = (c_lo + k) * kChunkM;   // first group of the unit in the slice
         const int ngc = min(kChunkM, ng - gc0);
         uint2 sb[4];   // the unit's 8 scale bytes of rows g, g+8, g+16, g+24
@@ -356,39 +409,55 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         for (int q = 0; q < 4; ++q)
             sb[q] = *reinterpret_cast<const uint2*>(scr + q * 8 * L.sc_pitch + gc0);
 #pragma unroll
-        for (int j = 0; j < kChunkM; ++j) {
-            if (j < ngc) {
-                // 128-byte swizzle: chunk j of row r sits at chunk j ^ (r & 7), r & 7 = g
-                const uint8_t* cw = stg + g * 128 + (((j ^ g) & 7) << 4) + t * 4;
-                uint32_t h0[4], h1[4], h2[4], h3[4];
-                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw), h0);
-                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 1024), h1);
-                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 2048), h2);
-                e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 3072), h3);
-                uint4 b = make_uint4(0u, 0u, 0u, 0u);
-                if (lane < 8 * NT) b = xf[(gc0 + j) * (8 * NT) + lane];
-                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                mma16816(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
-                mma16816(d0, h0[2], h1[2], h0[3], h1[3], b.z, b.w);
-                mma16816(d1, h2[2], h3[2], h2[3], h3[3], b.z, b.w);
-                const int sh = 8 * (j & 3);
-                const uint32_t w0 = j < 4 ? sb[0].x : sb[0].y, w1 = j < 4 ? sb[1].x : sb[1].y;
-                const uint32_t w2 = j < 4 ? sb[2].x : sb[2].y, w3 = j < 4 ? sb[3].x : sb[3].y;
-                float v0 = __fadd_rn(d0[0], d0[1]), v1 = __fadd_rn(d0[2], d0[3]);
-                float v2 = __fadd_rn(d1[0], d1[1]), v3 = __fadd_rn(d1[2], d1[3]);
-                if (plain) {   // the sums stay in the 2^p domain; 2^(k-127) from its bits
-                    const uint32_t m8 = 0xFFu << 23;
-                    const int s23 = 23 - sh;
-                    acc[0] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w0 << s23 : w0 >> -s23) & m8), v0, acc[0]);
-                    acc[1] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w1 << s23 : w1 >> -s23) & m8), v1, acc[1]);
-                    acc[2] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w2 << s23 : w2 >> -s23) & m8), v2, acc[2]);
-                    acc[3] = __fmaf_rn(__uint_as_float((s23 >= 0 ? w3 << s23 : w3 >> -s23) & m8), v3, acc[3]);
-                } else {       // any byte: the table, and 2^-p applied first
-                    acc[0] = __fmaf_rn(lut[(w0 >> sh) & 0xFFu], __fmul_rn(v0, pinv), acc[0]);
-                    acc[1] = __fmaf_rn(lut[(w1 >> sh) & 0xFFu], __fmul_rn(v1, pinv), acc[1]);
-                    acc[2] = __fmaf_rn(lut[(w2 >> sh) & 0xFFu], __fmul_rn(v2, pinv), acc[2]);
-                    acc[3] = __fmaf_rn(lut[(w3 >> sh) & 0xFFu], __fmul_rn(v3, pinv), acc[3]);
+        for (int j0 = 0; j0 < kChunkM; j0 += GP) {
+            if (j0 < ngc) {
+                float d0[4], d1[4];   // rows g, g+8 and g+16, g+24
+#pragma unroll
+                for (int s = 0; s < GP; ++s) {
+                    const int j = j0 + s;
+                    if (j < ngc) {
+                        // code word t of rows g, g+8, g+16, g+24 (128-byte swizzle:
+                        // chunk j of row r sits at chunk j ^ (r & 7))
+                        uint32_t cwd[4];
+                        ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
+                        uint32_t h0[4], h1[4], h2[4], h3[4];
+                        e2m1x8_to_f16x2x4(cwd[0], h0);
+                        e2m1x8_to_f16x2x4(cwd[1], h1);
+                        e2m1x8_to_f16x2x4(cwd[2], h2);
+                        e2m1x8_to_f16x2x4(cwd[3], h3);
+                        const uint4 b = lds128_m(
+                            b_slot == s ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * NT)
+                                        : zero_lane);
+                        if (s == 0) {
+                            mma16816_z(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                            mma16816_z(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                        } else {
+                            mma16816(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                            mma16816(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                        }
+                        mma16816(d0, h0[2], h1[2], h0[3], h1[3], b.z, b.w);
+                        mma16816(d1, h2[2], h3[2], h2[3], h3[3], b.z, b.w);
+                    }
+                }
+                // this lane's group: j0 + slot (its scale byte: byte (j0 & 3) + slot of
+                // word j0 / 4 of the unit's bytes)
+                if (j0 + slot < ngc) {
+                    const uint32_t sel = sel0 + (static_cast<uint32_t>(j0 & 3) << 8);
+                    const uint32_t w0 = j0 < 4 ? sb[0].x : sb[0].y, w1 = j0 < 4 ? sb[1].x : sb[1].y;
+                    const uint32_t w2 = j0 < 4 ? sb[2].x : sb[2].y, w3 = j0 < 4 ? sb[3].x : sb[3].y;
+                    const float v[4] = {__fadd_rn(d0[0], d0[1]), __fadd_rn(d0[2], d0[3]),
+                                        __fadd_rn(d1[0], d1[1]), __fadd_rn(d1[2], d1[3])};
+                    const uint32_t kw[4] = {__byte_perm(w0, 0u, sel), __byte_perm(w1, 0u, sel),
+                                            __byte_perm(w2, 0u, sel), __byte_perm(w3, 0u, sel)};
+                    const int i_acc = (j0 / GP) % NT;   // r = (j0 + slot) mod 4 = slot + GP i
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (plain)   // the sums stay in the 2^p domain; 2^(k-127) from its bits
+                            acc[q][i_acc] = __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[q][i_acc]);
+                        else         // any byte: the table, and 2^-p applied first
+                            acc[q][i_acc] =
+                                __fmaf_rn(lut[kw[q] >> 16], __fmul_rn(v[q], pinv), acc[q][i_acc]);
+                    }
                 }
             }
         }
@@ -404,16 +473,25 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         for (int kq = k; kq < k + stages && kq < n_units; ++kq)
             mbar_wait(&bars[kq % stages], static_cast<uint32_t>(kq / stages) & 1u, kWaitM);
     }
-    if (plain) {   // back from the 2^p domain (exact: a power of two, no overflow)
+    // token n's four sums: P_r in lane (g, (r mod GP) NT + n), entry r / GP; lane
+    // (g, n) adds them in order
+    float out[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = __fmul_rn(acc[q], pinv);
+    for (int q = 0; q < 4; ++q) {
+        float p[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            p[r] = __shfl_sync(0xffffffffu, acc[q][r / GP], (lane & ~3) | ((r % GP) * NT + tok));
+        out[q] = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
+        // back from the 2^p domain (exact: a power of two, no overflow)
+        if (plain) out[q] = __fmul_rn(out[q], pinv);
     }
-    if (active && t < NT) {   // D columns 2t, 2t+1 are token t's hi and lo
+    if (active && t < NT) {   // lane (g, t) has token t
         float* pw = part + static_cast<size_t>(warp) * kRowsU * NT;
-        pw[g * NT + t] = acc[0];
-        pw[(g + 8) * NT + t] = acc[1];
-        pw[(g + 16) * NT + t] = acc[2];
-        pw[(g + 24) * NT + t] = acc[3];
+        pw[g * NT + t] = out[0];
+        pw[(g + 8) * NT + t] = out[1];
+        pw[(g + 16) * NT + t] = out[2];
+        pw[(g + 24) * NT + t] = out[3];
     }
     __syncthreads();
 
