@@ -7,9 +7,14 @@
 // The arithmetic of a product is the one of mv_tc.cu: E2M1 codes through the
 // hardware pair conversion into the A operand of mma.sync m16n8k16, each
 // pair's vector split into f16 hi and lo (one power of two per pair putting
-// its largest |x| in [2^14, 2^15)) in the B columns 2n and 2n + 1, two MMAs per
-// group and 16 rows into a fresh accumulator, then 2^-p and the group's scale
-// in FP32 and the FP32 row sum.
+// its largest |x| in [2^14, 2^15)), two MMAs per group and 16 rows, then 2^-p
+// and the group's scale in FP32 and the FP32 row sum.  A segment with n pairs
+// uses NP = 1, 2 or 4 column sets (NP >= n) and lets GP = 4 / NP consecutive
+// groups share one accumulator: B columns 2c, 2c + 1 are (hi, lo) of pair
+// c % NP for group slot c / NP, group j0 + s putting its x in slot s's columns
+// only, so that the D columns of lane t hold group j0 + t / NP of pair t % NP
+// alone.  Lane t sums its slot's groups; the slots are added in order at the
+// end of the warp's units.
 //
 // Work: a segment is (touched expert, up to four of its pairs, 128 rows of its
 // matrices); the segments of all touched experts are dealt to persistent CTAs
@@ -22,6 +27,7 @@
 // o[pair][row].  Every order depends on the shapes and the routing only.
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -61,14 +67,6 @@ __device__ __forceinline__ uint32_t pack_f16x2_e(float lo, float hi) {
     return r;
 }
 
-__device__ __forceinline__ void mma16816_e(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Plan arrays written by the routing plan kernel (moe.cu).
 struct PlanRef {
     const int32_t* hdr;       // [1] = number of touched experts
@@ -93,7 +91,7 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;                             // pexp, tmax, pairs, lead
+    l.misc = l.lut + 1024;                             // pexp, tmax, pairs, lead, 16 zeros
     l.segst = l.misc + 80;                                            // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
     l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
@@ -120,6 +118,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);   // [4]
     int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [4]
     int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2 buffers][2 matrices]
+    const uint32_t zero16 = smem_u32(smem + L.misc + 64);               // 16 zero bytes
     int* segst = reinterpret_cast<int*>(smem + L.segst);
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
     uint64_t* ring_bars = sbar + 2;
@@ -132,6 +131,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const uint64_t policy = l2_evict_first();
 
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
+    if (tid < 4) reinterpret_cast<uint32_t*>(smem + L.misc + 64)[tid] = 0u;
     if (tid == 0) {
         mbar_init(&sbar[0], 1);
         mbar_init(&sbar[1], 1);
@@ -248,6 +248,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
         }
         __syncthreads();
+        // column sets of this segment: NP >= its pairs
+        const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
         constexpr int kXU = (kTokSeg * kGMaxE * 4 + kThreadsE - 1) / kThreadsE;
         const int n_items = kTokSeg * gpr * 4;
         float xv[kXU][8];
@@ -295,8 +297,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
 #pragma unroll
         for (int uu = 0; uu < kXU; ++uu) {
             const int i = tid + uu * kThreadsE;
-            if (i < n_items) {
-                const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
+            const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
+            if (i < n_items && tok < np) {
                 const int j = rem >> 2, tw = rem & 3;
                 const float pm = exp2i_e(pexp[tok]);
                 uint32_t hi[4], lo[4];
@@ -307,8 +309,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                     const float2 h = f16x2_to_f32x2(hi[k]);
                     lo[k] = pack_f16x2_e(__fsub_rn(f0, h.x), __fsub_rn(f1, h.y));
                 }
-                xf[j * 32 + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                xf[j * 32 + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                xf[j * 8 * np + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                xf[j * 8 * np + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         if (!mbar_wait(&sbar[bi], static_cast<uint32_t>(nseg_cta >> 1) & 1u, kWaitE)) {
@@ -319,9 +321,61 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
 
         // --- this warp's units
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24 of the unit, pair t
-        const float pinv = exp2i_e(-pexp[t]);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24, this lane's groups
+        const int slot = t / np, tok = t % np;   // D columns 2t, 2t + 1: group slot, pair
+        const float pinv = exp2i_e(-pexp[tok]);
+        // B: lanes 8 np s .. 8 np s + 8 np - 1 hold the fragment of group slot s
+        const int b_slot = lane / (8 * np);
+        const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * np)) * 16;
         const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
+        // the groups of a unit, GP to an accumulator
+        auto unit_groups = [&](auto gp_c, uint32_t row_addr, int gc0, int ngc,
+                               const uint32_t (&sb)[4][2]) {
+            constexpr int GP = decltype(gp_c)::value;
+#pragma unroll
+            for (int j0 = 0; j0 < kChunkE; j0 += GP) {
+                if (j0 < ngc) {
+                    float d0[4], d1[4];   // rows g, g+8 and g+16, g+24
+#pragma unroll
+                    for (int sl = 0; sl < GP; ++sl) {
+                        const int j = j0 + sl;
+                        if (j < ngc) {
+                            uint32_t cwd[4];   // code word t of rows g, g+8, g+16, g+24
+                            ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
+                            uint32_t h0[4], h1[4], h2[4], h3[4];
+                            e2m1x8_to_f16x2x4(cwd[0], h0);
+                            e2m1x8_to_f16x2x4(cwd[1], h1);
+                            e2m1x8_to_f16x2x4(cwd[2], h2);
+                            e2m1x8_to_f16x2x4(cwd[3], h3);
+                            const uint4 bf = lds128(
+                                b_slot == sl ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * np)
+                                             : zero16);
+                            if (sl == 0) {
+                                mma16816_z(d0, h0[0], h1[0], h0[1], h1[1], bf.x, bf.y);
+                                mma16816_z(d1, h2[0], h3[0], h2[1], h3[1], bf.x, bf.y);
+                            } else {
+                                mma16816(d0, h0[0], h1[0], h0[1], h1[1], bf.x, bf.y);
+                                mma16816(d1, h2[0], h3[0], h2[1], h3[1], bf.x, bf.y);
+                            }
+                            mma16816(d0, h0[2], h1[2], h0[3], h1[3], bf.z, bf.w);
+                            mma16816(d1, h2[2], h3[2], h2[3], h3[3], bf.z, bf.w);
+                        }
+                    }
+                    if (j0 + slot < ngc) {   // this lane's group j0 + slot
+                        const int hw = j0 >> 2;
+                        const uint32_t sel = 0x4440u + static_cast<uint32_t>((j0 & 3) + slot);
+                        acc[0] = __fmaf_rn(lut[__byte_perm(sb[0][hw], 0u, sel)],
+                                           __fmul_rn(__fadd_rn(d0[0], d0[1]), pinv), acc[0]);
+                        acc[1] = __fmaf_rn(lut[__byte_perm(sb[1][hw], 0u, sel)],
+                                           __fmul_rn(__fadd_rn(d0[2], d0[3]), pinv), acc[1]);
+                        acc[2] = __fmaf_rn(lut[__byte_perm(sb[2][hw], 0u, sel)],
+                                           __fmul_rn(__fadd_rn(d1[0], d1[1]), pinv), acc[2]);
+                        acc[3] = __fmaf_rn(lut[__byte_perm(sb[3][hw], 0u, sel)],
+                                           __fmul_rn(__fadd_rn(d1[2], d1[3]), pinv), acc[3]);
+                    }
+                }
+            }
+        };
         int k = 0;
         for (; k < cur.n_units && !failed; ++k) {
             const int kg = kglob + k, st = kg % kStagesE;
@@ -330,6 +384,9 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 break;
             }
             const uint8_t* stg = ring + st * kStageE;
+            // this lane's row (lane) of the tile, chunk 0 after the 128-byte swizzle;
+            // chunk j is at that address ^ (j << 4) (the tile is 1024-byte aligned)
+            const uint32_t row_addr = smem_u32(stg) + lane * 128 + ((lane & 7) << 4);
             const int gc0 = (cur.c_lo + k) * kChunkE;
             const int ngc = min(kChunkE, gpr - gc0);
             uint32_t sb[4][2];   // 8 scale bytes of rows g, g+8, g+16, g+24 (any alignment)
@@ -343,32 +400,12 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 sb[r4][0] = __funnelshift_r(w0, w1, sh);
                 sb[r4][1] = __funnelshift_r(w1, w2, sh);
             }
-#pragma unroll
-            for (int j = 0; j < kChunkE; ++j) {
-                if (j < ngc) {
-                    const uint8_t* cw = stg + g * 128 + (((j ^ g) & 7) << 4) + t * 4;
-                    uint32_t h0[4], h1[4], h2[4], h3[4];
-                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw), h0);
-                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 1024), h1);
-                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 2048), h2);
-                    e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(cw + 3072), h3);
-                    const uint4 bf = xf[(gc0 + j) * 32 + lane];
-                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816_e(d0, h0[0], h1[0], h0[1], h1[1], bf.x, bf.y);
-                    mma16816_e(d1, h2[0], h3[0], h2[1], h3[1], bf.x, bf.y);
-                    mma16816_e(d0, h0[2], h1[2], h0[3], h1[3], bf.z, bf.w);
-                    mma16816_e(d1, h2[2], h3[2], h2[3], h3[3], bf.z, bf.w);
-                    const int sh = 8 * (j & 3), hw = j >> 2;
-                    acc[0] = __fmaf_rn(lut[(sb[0][hw] >> sh) & 0xFFu],
-                                       __fmul_rn(__fadd_rn(d0[0], d0[1]), pinv), acc[0]);
-                    acc[1] = __fmaf_rn(lut[(sb[1][hw] >> sh) & 0xFFu],
-                                       __fmul_rn(__fadd_rn(d0[2], d0[3]), pinv), acc[1]);
-                    acc[2] = __fmaf_rn(lut[(sb[2][hw] >> sh) & 0xFFu],
-                                       __fmul_rn(__fadd_rn(d1[0], d1[1]), pinv), acc[2]);
-                    acc[3] = __fmaf_rn(lut[(sb[3][hw] >> sh) & 0xFFu],
-                                       __fmul_rn(__fadd_rn(d1[2], d1[3]), pinv), acc[3]);
-                }
-            }
+            if (np == 1)
+                unit_groups(std::integral_constant<int, 4>{}, row_addr, gc0, ngc, sb);
+            else if (np == 2)
+                unit_groups(std::integral_constant<int, 2>{}, row_addr, gc0, ngc, sb);
+            else
+                unit_groups(std::integral_constant<int, 1>{}, row_addr, gc0, ngc, sb);
             __syncwarp();   // every lane is done with the stage
             if (lane == 0 && issued < stream_end) {   // refill: this segment's or the next one's
                 fence_proxy_async_smem();
@@ -389,7 +426,15 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
         }
         float* part = reinterpret_cast<float*>(smem + L.sc + bi * NM * L.sc_bytes);
-        if (cur.active) {   // D columns 2t, 2t+1 are pair t's hi and lo
+        // pair n: the slots' sums in lanes (g, s np + n), added in slot order into lane (g, n)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float v = acc[q];
+            for (int sl = 1; sl < 4 / np; ++sl)
+                v = __fadd_rn(v, __shfl_sync(0xffffffffu, acc[q], (lane & ~3) | (sl * np + tok)));
+            acc[q] = v;
+        }
+        if (cur.active && t < np) {   // lane (g, t) has pair t
             float* pw = part + static_cast<size_t>(warp) * kRowsUE * kTokSeg;
             pw[g * kTokSeg + t] = acc[0];
             pw[(g + 8) * kTokSeg + t] = acc[1];

@@ -107,41 +107,6 @@ __device__ __forceinline__ uint32_t pack_f16x2_m(float lo, float hi) {
     return r;
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// The same with a zero accumulator in.
-__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    const float z = 0.0f;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
-}
-
-__device__ __forceinline__ uint4 lds128_m(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(a));
-    return v;
-}
-
-// Four 8 x 16-byte matrices: lane (g, t) gets word t of row g of matrix i in
-// r[i]; lanes 8i .. 8i + 7 give the row addresses of matrix i.
-__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a)
-                 : "memory");
-}
-
 // Shared memory (offsets from a 1024-byte aligned base).
 struct MvLayout {
     uint32_t lut, xf, sc, sc_pitch, part, fin, misc, bars, ring, total;
@@ -425,7 +390,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                         e2m1x8_to_f16x2x4(cwd[1], h1);
                         e2m1x8_to_f16x2x4(cwd[2], h2);
                         e2m1x8_to_f16x2x4(cwd[3], h3);
-                        const uint4 b = lds128_m(
+                        const uint4 b = lds128(
                             b_slot == s ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * NT)
                                         : zero_lane);
                         if (s == 0) {
