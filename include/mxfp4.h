@@ -102,7 +102,8 @@ int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t st
  * 32 decoded weights (exact in f16) are dotted with x on the tensor cores
  * (mma.sync; x split into f16 halves hi + lo of x * 2^p, so every product is
  * exact), the group sum is scaled by its E8M0 factor and 2^-p in FP32 and
- * added to the row's FP32 sum.  x: [cols] floats, y: [rows] floats.  Error
+ * added to one of the row's four FP32 sums (groups by index mod 4), which are
+ * added in order at the end.  x: [cols] floats, y: [rows] floats.  Error
  * bound: |y - exact| <= 1e-5 * sum_c |W[r][c] x[c]| (a NaN scale makes the
  * row NaN).  Deterministic: the order of every sum depends on the shape
  * only.  (PEROP mxfp4_mv.) */
