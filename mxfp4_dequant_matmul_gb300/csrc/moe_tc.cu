@@ -17,9 +17,9 @@
 // end of the warp's units.
 //
 // Work: a segment is (touched expert, up to four of its pairs, 128 rows of its
-// matrices); the segments of all touched experts are dealt to persistent CTAs
-// in turn.  For each segment a CTA copies the 128 rows' scale bytes with one
-// bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
+// gate and up matrices or 256 rows of its down matrix); the segments of all
+// touched experts are dealt to persistent CTAs in turn.  For each segment a
+// CTA copies the rows' scale bytes with one bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
 // (matrix, 32-row unit, chunk range) units of 32 rows x 8 groups through
 // per-warp rings of TMA tile loads (a 3-D tensor map over the bank: bytes,
 // rows, experts).  Partial sums are added in chunk order; the gate/up pass
@@ -45,7 +45,9 @@ constexpr int kRowsUE = 32;                 // rows per unit (two MMA row blocks
 constexpr int kChunkE = 8;                  // groups per unit
 constexpr int kStageE = kRowsUE * 128;      // one TMA tile, 4 KB
 constexpr int kStagesE = 2;                 // ring stages per warp
-constexpr int kRuSeg = 4;                   // 32-row units per segment (128 rows)
+// 32-row units per segment: 8 / NM (256 rows of one matrix, 128 rows of two), so
+// that every warp has the same number of units per segment in both passes
+__host__ __device__ constexpr int ru_seg(int NM) { return 8 / NM; }
 constexpr int kTokSeg = 4;                  // pairs per segment
 constexpr int kGMaxE = 128;                 // groups per row (B fragments in shared memory)
 constexpr int kMaxExpertsE = 1024;
@@ -85,7 +87,7 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     ELayout l;
     l.xf = 0;                                                          // [gpr][32] uint4
     l.sc = l.xf + static_cast<uint32_t>(gpr) * 512;                    // [2][NM][sc_bytes]
-    l.sc_bytes = (static_cast<uint32_t>(kRuSeg * kRowsUE) * gpr + 32u + 15u) & ~15u;
+    l.sc_bytes = (static_cast<uint32_t>(ru_seg(NM) * kRowsUE) * gpr + 32u + 15u) & ~15u;
     const uint32_t part_bytes = kWarpsE * kRowsUE * kTokSeg * 4;      // [warps][32][4] f32
     const uint32_t buf = NM * l.sc_bytes > part_bytes ? NM * l.sc_bytes : part_bytes;
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
@@ -126,7 +128,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
     const size_t plane = static_cast<size_t>(rows) * cols / 2;
-    const int n_blocks = (rows + kRuSeg * kRowsUE - 1) / (kRuSeg * kRowsUE);
+    constexpr int kSegRows = ru_seg(NM) * kRowsUE;
+    const int n_blocks = (rows + kSegRows - 1) / kSegRows;
     const int n_c = (gpr + kChunkE - 1) / kChunkE;
     const uint64_t policy = l2_evict_first();
 
@@ -168,8 +171,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         const int ck = rel / n_blocks, b = rel - ck * n_blocks;
         q.beg = b0 + ck * kTokSeg;
         q.npair = min(kTokSeg, n_e - ck * kTokSeg);
-        q.row0 = b * kRuSeg * kRowsUE;
-        q.nrow = min(kRuSeg * kRowsUE, rows - q.row0);
+        q.row0 = b * kSegRows;
+        q.nrow = min(kSegRows, rows - q.row0);
         q.n_ru = (q.nrow + kRowsUE - 1) / kRowsUE;
         q.WK = min(n_c, kWarpsE / (NM * q.n_ru));
         q.active = warp < NM * q.n_ru * q.WK;
