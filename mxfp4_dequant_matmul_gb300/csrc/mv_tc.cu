@@ -65,6 +65,7 @@ constexpr int kMaxStagesM = 4;
 #define MXFP4_PRE_STAGES 1
 #endif
 constexpr int kPreStagesM = MXFP4_PRE_STAGES;   // stages started before the wait (overlap)
+static_assert(kPreStagesM >= 1 && kPreStagesM <= kMinStagesM, "early stages must fit every ring");
 constexpr uint32_t kSmemMaxM = 227 * 1024;
 constexpr int kMaxRuCta = 4;                // 32-row units per CTA
 constexpr uint32_t kWaitM = 1u << 22;
@@ -221,13 +222,14 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // previous kernel of the stream (programmatic dependent launch): then the
     // weights, which that kernel does not write, start at once, and x (which
     // it may write) is read only once it has completed.
+    // (unit k goes to stage k: never more units than the ring has stages)
     auto start_weights = [&](int k0, int k1) {   // this warp's units k0 .. k1-1
         if (lane == 0) {
             if (k0 == 0) {
                 for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
                 fence_mbar_init();
             }
-            for (int k = k0; k < k1 && k < n_units; ++k) issue(k, k);
+            for (int k = k0; k < k1 && k < stages && k < n_units; ++k) issue(k, k);
         }
     };
     if (overlap) {
