@@ -15,7 +15,8 @@
 // call, their decode shared by all of the expert's pairs.
 //
 // Pipeline (all stream-ordered, no inter-CTA waits):
-//   k_moe_plan      one CTA: counts, offsets, touched-expert list, pair lists
+//   k_moe_plan_s    one CTA: counts, offsets, touched-expert list, pair lists
+//                   (shared-memory scans; k_moe_plan beyond 4096 experts)
 //   gate/up pass    k_moe_tc<2> (moe_tc.cu, tensor cores), else k_moe_pass
 //   down pass       k_moe_tc<1>, else k_moe_pass -> per-pair outputs
 //   k_moe_combine   y[t] = sum_j w[t,j] * o[t*top_k + j], slots in order
@@ -99,6 +100,95 @@ __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ i
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
         int pos = plan.offsets[e];
         for (int p = 0; p < n_pairs; ++p)
+            if (__ldg(ids + p) == e) plan.pair_of[pos++] = p;
+    }
+}
+
+// The same plan with the counts, offsets and touched flags in shared memory
+// (up to kPlanSmemExperts experts): counts by shared atomics, offsets and the
+// touched list by block-wide exclusive scans, then each touched expert lists
+// its pairs in increasing order.  The arrays it writes are those of k_moe_plan.
+constexpr int kPlanSmemExperts = 4096;
+
+__global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__ ids, int n_pairs,
+                                                     int n_experts, Plan plan) {
+    __shared__ int s_cnt[kPlanSmemExperts];
+    __shared__ int s_wsum[2][32];
+    __shared__ int s_invalid;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    for (int e = tid; e < n_experts; e += nt) s_cnt[e] = 0;
+    if (tid == 0) s_invalid = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = tid; p < n_pairs; p += nt) {
+        const int32_t e = __ldg(ids + p);
+        if (e < 0 || e >= n_experts)
+            ++bad;
+        else
+            atomicAdd(&s_cnt[e], 1);
+    }
+    if (bad) atomicAdd(&s_invalid, bad);
+    __syncthreads();
+    // thread tid takes experts [e0, e1): its count and touched sums, scanned
+    // across the warp, then across the warps
+    const int per = (n_experts + nt - 1) / nt;
+    const int e0 = min(tid * per, n_experts), e1 = min(e0 + per, n_experts);
+    int c_sum = 0, f_sum = 0;
+    for (int e = e0; e < e1; ++e) {
+        c_sum += s_cnt[e];
+        f_sum += s_cnt[e] > 0 ? 1 : 0;
+    }
+    int c_inc = c_sum, f_inc = f_sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int c = __shfl_up_sync(0xffffffffu, c_inc, d);
+        const int f = __shfl_up_sync(0xffffffffu, f_inc, d);
+        if (lane >= d) {
+            c_inc += c;
+            f_inc += f;
+        }
+    }
+    if (lane == 31) {
+        s_wsum[0][w] = c_inc;
+        s_wsum[1][w] = f_inc;
+    }
+    __syncthreads();
+    if (w == 0) {
+        const int nw = nt >> 5;
+        int c = lane < nw ? s_wsum[0][lane] : 0, f = lane < nw ? s_wsum[1][lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int cu = __shfl_up_sync(0xffffffffu, c, d);
+            const int fu = __shfl_up_sync(0xffffffffu, f, d);
+            if (lane >= d) {
+                c += cu;
+                f += fu;
+            }
+        }
+        s_wsum[0][lane] = c;   // inclusive over warps 0 .. lane
+        s_wsum[1][lane] = f;
+    }
+    __syncthreads();
+    int c_run = c_inc - c_sum + (w > 0 ? s_wsum[0][w - 1] : 0);
+    int f_run = f_inc - f_sum + (w > 0 ? s_wsum[1][w - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        const int c = s_cnt[e];
+        plan.offsets[e] = c_run;
+        if (c > 0) plan.touched[f_run++] = e;
+        s_cnt[e] = c_run;   // from here on: the first position of expert e
+        c_run += c;
+    }
+    if (tid == nt - 1) {   // its range ends at n_experts: the totals
+        plan.offsets[n_experts] = c_run;
+        plan.hdr[0] = s_invalid;
+        plan.hdr[1] = f_run;
+    }
+    __syncthreads();
+    const int n_valid = n_pairs - s_invalid;
+    for (int e = tid; e < n_experts; e += nt) {
+        int pos = s_cnt[e];
+        const int end = e + 1 < n_experts ? s_cnt[e + 1] : n_valid;
+        for (int p = 0; p < n_pairs && pos < end; ++p)
             if (__ldg(ids + p) == e) plan.pair_of[pos++] = p;
     }
 }
@@ -261,7 +351,10 @@ cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
                                const int32_t* ids, float* act, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
     const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
-    k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
+    if (n_experts <= kPlanSmemExperts)
+        k_moe_plan_s<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
+    else
+        k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t stride = padded_nbytes(inter, hidden);
