@@ -112,7 +112,7 @@ constexpr int kPlanSmemExperts = 4096;
 
 __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__ ids, int n_pairs,
                                                      int n_experts, Plan plan) {
-    __shared__ int s_cnt[kPlanSmemExperts];
+    extern __shared__ int s_cnt[];   // [n_experts]
     __shared__ int s_wsum[2][32];
     __shared__ int s_invalid;
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
@@ -352,7 +352,8 @@ cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
     const int n_pairs = n_tokens * top_k;
     const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
     if (n_experts <= kPlanSmemExperts)
-        k_moe_plan_s<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
+        k_moe_plan_s<<<1, 1024, 4 * static_cast<size_t>(n_experts), s>>>(ids, n_pairs, n_experts,
+                                                                         plan);
     else
         k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
     cudaError_t e = cudaGetLastError();

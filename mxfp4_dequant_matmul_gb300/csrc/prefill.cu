@@ -618,35 +618,34 @@ cudaError_t launch_prefill2(const uint8_t* w, int rows, int cols, const float* X
 // layout the MMA descriptors read) through a 4-stage ring; warp 0 issues the
 // copies, warp 1 the MMAs, every warp reads the accumulator back.
 
-// Eight weights per code word: exact bfloat16 (a value times a power of two).
-__global__ void __launch_bounds__(256) k_w_to_bf16(const uint8_t* __restrict__ w, int rows,
-                                                   int cols, uint4* __restrict__ out) {
+// Both operands of the dense product in one launch: items [0, nw) are code
+// words of W (8 elements, exact in bfloat16: E2M1 value times E8M0 scale), items
+// [nw, nw + nx4) are four activations of X, rounded to nearest-even bfloat16.
+__global__ void __launch_bounds__(256) k_to_bf16(const uint8_t* __restrict__ w, int rows, int cols,
+                                                 uint4* __restrict__ wout,
+                                                 const float4* __restrict__ x, size_t nx4,
+                                                 uint2* __restrict__ xout) {
     const int wpr = cols / 8;   // code words per row
     const int gpr = cols / kGroup;
-    const size_t n = static_cast<size_t>(rows) * wpr;
+    const size_t nw = static_cast<size_t>(rows) * wpr;
     const uint8_t* scales = w + static_cast<size_t>(rows) * cols / 2;
     const uint32_t* words = reinterpret_cast<const uint32_t*>(w);
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nw + nx4;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const size_t r = i / wpr;
-        const int q = static_cast<int>(i - r * wpr);
-        const float sc = e8m0_to_f32(__ldg(scales + r * gpr + q / 4));
-        float v[8];
-        e2m1x8_to_f32(__ldg(words + i), v);
-        out[i] = make_uint4(pack_bf16x2(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc)),
-                            pack_bf16x2(__fmul_rn(v[2], sc), __fmul_rn(v[3], sc)),
-                            pack_bf16x2(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc)),
-                            pack_bf16x2(__fmul_rn(v[6], sc), __fmul_rn(v[7], sc)));
-    }
-}
-
-// Four activations at a time, rounded to nearest-even bfloat16.
-__global__ void __launch_bounds__(256) k_x_to_bf16(const float4* __restrict__ x, size_t n4,
-                                                   uint2* __restrict__ out) {
-    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        const float4 a = __ldg(x + i);
-        out[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+        if (i < nw) {
+            const size_t r = i / wpr;
+            const int q = static_cast<int>(i - r * wpr);
+            const float sc = e8m0_to_f32(__ldg(scales + r * gpr + q / 4));
+            float v[8];
+            e2m1x8_to_f32(__ldg(words + i), v);
+            wout[i] = make_uint4(pack_bf16x2(__fmul_rn(v[0], sc), __fmul_rn(v[1], sc)),
+                                 pack_bf16x2(__fmul_rn(v[2], sc), __fmul_rn(v[3], sc)),
+                                 pack_bf16x2(__fmul_rn(v[4], sc), __fmul_rn(v[5], sc)),
+                                 pack_bf16x2(__fmul_rn(v[6], sc), __fmul_rn(v[7], sc)));
+        } else {
+            const float4 a = __ldg(x + (i - nw));
+            xout[i - nw] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+        }
     }
 }
 
@@ -913,13 +912,11 @@ cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X
     if (!bf16_map(&amap, xb, cols, nb, kPM) || !bf16_map(&bmap, wb, cols, rows, tn))
         return cudaErrorNotSupported;
     const size_t nw = static_cast<size_t>(rows) * cols / 8;
-    k_w_to_bf16<<<grid_for(nw, 4), 256, 0, s>>>(w, rows, cols, reinterpret_cast<uint4*>(wb));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const size_t nx4 = static_cast<size_t>(nb) * cols / 4;
-    k_x_to_bf16<<<grid_for(nx4, 4), 256, 0, s>>>(reinterpret_cast<const float4*>(X), nx4,
-                                                 reinterpret_cast<uint2*>(xb));
-    e = cudaGetLastError();
+    k_to_bf16<<<grid_for(nw + nx4, 4), 256, 0, s>>>(w, rows, cols, reinterpret_cast<uint4*>(wb),
+                                                    reinterpret_cast<const float4*>(X), nx4,
+                                                    reinterpret_cast<uint2*>(xb));
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;

@@ -159,3 +159,17 @@ def test_out_of_range_ids_are_skipped_and_counted(mx):
     mx.mxfp4_moe_down(to_dev(down), 8, 64, 64, act, 10, 2, to_dev(ids), to_dev(wts), y, ws)
     refd = oracle.moe_down(down, cfg.down_stride, 8, 64, 64, act_in, 10, 2, ids, wts)
     assert_within(host(y), refd["out"], refd["l1_out"], REL_FP32, "down with invalid ids")
+
+
+@pytest.mark.parametrize("E", [300, 2000, 5000])
+def test_layer_with_many_experts(mx, E):
+    # the routing plan's scans over several warps (300), several experts per
+    # thread (2000) and the plan beyond 4096 experts (5000); past 1024 experts
+    # the expert passes are the FP32 ones
+    hidden, inter, T, K = 64, 32, 64, 4
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 23)
+    y, ws = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    assert mx.mxfp4_moe_plan_errors(ws) == 0
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
+                             x, T, K, ids, wts)
+    assert_within(y, ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32, f"{E} experts")
