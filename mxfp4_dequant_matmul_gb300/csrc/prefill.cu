@@ -625,6 +625,9 @@ __global__ void __launch_bounds__(256) k_to_bf16(const uint8_t* __restrict__ w, 
                                                  uint4* __restrict__ wout,
                                                  const float4* __restrict__ x, size_t nx4,
                                                  uint2* __restrict__ xout) {
+    // the GEMM may launch now and set itself up; it reads these outputs only
+    // after this grid has completed (griddepcontrol.wait)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int wpr = cols / 8;   // code words per row
     const int gpr = cols / kGroup;
     const size_t nw = static_cast<size_t>(rows) * wpr;
@@ -718,6 +721,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    // the operands are written by the conversion launch before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     auto fail = [&]() {
         *abort_flag = 1;
         atomicOr(&g_fault_prefill, 1);
@@ -933,10 +938,22 @@ cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X
     if (attr_err != cudaSuccess) return attr_err;
     const long tiles = tiles_of(tn);
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    if (tn == 224)
-        k_gemm_bf16<224><<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
-    else
-        k_gemm_bf16<256><<<grid, kPThreads, smem, s>>>(amap, bmap, rows, cols, nb, Y);
+    // programmatic dependent launch: set-up (barriers, TMEM) under the
+    // conversion's tail, the first copy after it has completed
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t el =
+        tn == 224 ? cudaLaunchKernelEx(&cfg, k_gemm_bf16<224>, amap, bmap, rows, cols, nb, Y)
+                  : cudaLaunchKernelEx(&cfg, k_gemm_bf16<256>, amap, bmap, rows, cols, nb, Y);
+    if (el != cudaSuccess) return el;
     return cudaGetLastError();
 }
 
