@@ -33,9 +33,9 @@
 // Data movement: a unit is 32 rows x 8 groups (32 rows x 128 code bytes), one
 // TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) into a ring of two
 // to four stages per warp (as deep as shared memory allows).  A CTA owns up to
-// 128 rows; its warps split them into 32-row units and the K range into equal
-// chunk ranges, each warp keeping its rows' sums in registers over its chunks.  The partial sums are added in chunk
-// order.  When the activations of a whole row do not fit in shared memory, a
+// 128 rows: its 16 warps take equal contiguous ranges of its (32-row unit,
+// chunk) tasks, keep their sums in registers and store them as their pieces of
+// a row unit; the pieces are added in chunk order.  When the activations of a whole row do not fit in shared memory, a
 // cluster of CTAs splits the groups and adds its partial sums in rank order
 // through distributed shared memory.  The order of every sum depends on the
 // shape only, so results are deterministic and a token's result does not
@@ -121,11 +121,11 @@ __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, in
     // fall in eight different bank groups
     l.sc_pitch = (static_cast<uint32_t>(ng_max) + 15u) & ~15u;
     if ((l.sc_pitch / 16u) % 2u == 0u) l.sc_pitch += 16u;
-    l.part = l.sc + static_cast<uint32_t>(ru_cta) * kRowsU * l.sc_pitch;   // [warps][32][NT]
+    l.part = l.sc + static_cast<uint32_t>(ru_cta) * kRowsU * l.sc_pitch;   // [warp + ru][32][NT]
     l.part = (l.part + 15u) & ~15u;
     // [rows][NT]; zero during the units: its bytes 32 .. 47 are the B values of
     // the lanes that hold none
-    l.fin = l.part + kWarpsM * kRowsU * NT * 4;
+    l.fin = l.part + static_cast<uint32_t>(kWarpsM + ru_cta - 1) * kRowsU * NT * 4;
     l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[4], tmax[4]
     l.bars = (l.misc + 64 + 7u) & ~7u;
     l.ring = (l.bars + kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
@@ -168,20 +168,25 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const int row0 = ru0 * kRowsU;
     const size_t plane = static_cast<size_t>(rows) * cols / 2;
 
-    // warp -> (row unit, chunk range): n_ru x WK warps, each over n_c / WK chunks
-    const int WK = min(n_c, kWarpsM / n_ru);
-    const bool active = warp < n_ru * WK;
-    const int my_ru = warp % n_ru, kk = warp / n_ru;
-    const int c_lo = active ? kk * n_c / WK : 0;
-    const int c_hi = active ? (kk + 1) * n_c / WK : 0;
-    const int n_units = c_hi - c_lo;
+    // The CTA's (row unit, chunk) tasks, row unit major, in 16 contiguous ranges
+    // as equal as the count allows (shape only).  Warp w takes range w when the
+    // count divides evenly (consecutive warps then stream neighbouring rows),
+    // else range (w mod 4) 4 + w / 4, so that each scheduler (the warps
+    // w = s mod 4) holds a contiguous quarter of the tasks.  A warp's sums become
+    // the piece of its range for a row unit (slot range + row unit) whenever its
+    // range leaves the unit.
+    const int n_tasks = n_ru * n_c;
+    const int rg = n_tasks % kWarpsM == 0 ? warp : (warp & 3) * (kWarpsM / 4) + (warp >> 2);
+    const int t_lo = rg * n_tasks / kWarpsM;
+    const int n_units = (rg + 1) * n_tasks / kWarpsM - t_lo;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * stages;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * stages * kStageM;
     const uint64_t policy = l2_evict_first();
-    auto issue = [&](int k, int st) {   // unit k of this warp into stage st (lane 0)
-        const int x = (g_lo + (c_lo + k) * kChunkM) * kGroupBytes;
-        const int y = row0 + my_ru * kRowsU;
+    // the unit of row unit ru, chunk c into stage st (lane 0)
+    auto issue_rc = [&](int ru, int c, int st) {
+        const int x = (g_lo + c * kChunkM) * kGroupBytes;
+        const int y = row0 + ru * kRowsU;
         mbar_arrive_expect_tx(&bars[st], kStageM);
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -229,7 +234,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                 for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
                 fence_mbar_init();
             }
-            for (int k = k0; k < k1 && k < stages && k < n_units; ++k) issue(k, k);
+            for (int k = k0; k < k1 && k < stages && k < n_units; ++k) {
+                const int task = t_lo + k, ru = task / n_c;
+                issue_rc(ru, task - ru * n_c, k);
+            }
         }
     };
     if (overlap) {
@@ -356,12 +364,44 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * NT)) * 16;
     const uint32_t zero_lane = smem_u32(fin) + 32;
     const uint32_t sel0 = 0x4044u + (static_cast<uint32_t>(slot) << 8);   // byte slot -> byte 2
+    // token n's four sums: P_r in lane (g, (r mod GP) NT + n), entry r / GP; lane
+    // (g, n) adds them in order and stores them as this warp's piece of row unit ru
+    auto flush = [&](int ru) {
+        float* pw = part + static_cast<size_t>(rg + ru) * kRowsU * NT;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float p[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                p[r] = __shfl_sync(0xffffffffu, acc[q][r / GP], (lane & ~3) | ((r % GP) * NT + tok));
+            float v = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
+            // back from the 2^p domain (exact: a power of two, no overflow)
+            if (plain) v = __fmul_rn(v, pinv);
+            if (t < NT) pw[(g + 8 * q) * NT + t] = v;   // lane (g, t) has token t
+#pragma unroll
+            for (int i = 0; i < NT; ++i) acc[q][i] = 0.0f;
+        }
+    };
     bool failed = false;
-    int k = 0;
-    const uint8_t* scr = sc_s + static_cast<size_t>(my_ru * kRowsU + g) * L.sc_pitch;
+    int k = 0, cur_ru = -1;
+    // (row unit, chunk) of unit k and of unit k + stages, the next to be issued
+    int u_ru = t_lo / n_c, u_c = t_lo - (t_lo / n_c) * n_c;
+    int i_ru = (t_lo + stages) / n_c, i_c = (t_lo + stages) - ((t_lo + stages) / n_c) * n_c;
+    int st = 0;           // k mod stages
+    uint32_t phase = 0;   // (k / stages) mod 2
+    const uint8_t* scr = sc_s;
     for (; k < n_units; ++k) {
-        const int st = k % stages;
-        if (!mbar_wait(&bars[st], static_cast<uint32_t>(k / stages) & 1u, kWaitM)) {
+        const int ru = u_ru, chunk = u_c;   // this unit's row unit and chunk
+        if (++u_c == n_c) {
+            u_c = 0;
+            ++u_ru;
+        }
+        if (ru != cur_ru) {
+            if (cur_ru >= 0) flush(cur_ru);
+            cur_ru = ru;
+            scr = sc_s + static_cast<size_t>(ru * kRowsU + g) * L.sc_pitch;
+        }
+        if (!mbar_wait(&bars[st], phase, kWaitM)) {
             failed = true;
             break;
         }
@@ -369,7 +409,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         // this lane's row (lane) of the tile, chunk 0 after the swizzle; chunk j
         // is at that address ^ (j << 4) (the tile is 1024-byte aligned)
         const uint32_t row_addr = smem_u32(stg) + lane * 128 + ((lane & 7) << 4);
-        const int gc0 = (c_lo + k) * kChunkM;   // first group of the unit in the slice
+        const int gc0 = chunk * kChunkM;   // first group of the unit in the slice
         const int ngc = min(kChunkM, ng - gc0);
         uint2 sb[4];   // the unit's 8 scale bytes of rows g, g+8, g+16, g+24
 #pragma unroll
@@ -431,7 +471,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         __syncwarp();   // every lane is done with the stage
         if (lane == 0 && k + stages < n_units) {
             fence_proxy_async_smem();
-            issue(k + stages, st);
+            issue_rc(i_ru, i_c, st);
+            if (++i_c == n_c) {
+                i_c = 0;
+                ++i_ru;
+            }
+        }
+        if (++st == stages) {   // unit k + 1: stage (k + 1) mod stages, phase bit of (k + 1) / stages
+            st = 0;
+            phase ^= 1u;
         }
     }
     if (failed) {
@@ -440,34 +488,25 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         for (int kq = k; kq < k + stages && kq < n_units; ++kq)
             mbar_wait(&bars[kq % stages], static_cast<uint32_t>(kq / stages) & 1u, kWaitM);
     }
-    // token n's four sums: P_r in lane (g, (r mod GP) NT + n), entry r / GP; lane
-    // (g, n) adds them in order
-    float out[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float p[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            p[r] = __shfl_sync(0xffffffffu, acc[q][r / GP], (lane & ~3) | ((r % GP) * NT + tok));
-        out[q] = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
-        // back from the 2^p domain (exact: a power of two, no overflow)
-        if (plain) out[q] = __fmul_rn(out[q], pinv);
-    }
-    if (active && t < NT) {   // lane (g, t) has token t
-        float* pw = part + static_cast<size_t>(warp) * kRowsU * NT;
-        pw[g * NT + t] = out[0];
-        pw[(g + 8) * NT + t] = out[1];
-        pw[(g + 16) * NT + t] = out[2];
-        pw[(g + 24) * NT + t] = out[3];
-    }
+    if (cur_ru >= 0) flush(cur_ru);
     __syncthreads();
 
-    // --- add the chunk ranges in order (warp kk * n_ru + ru)
+    // --- add each row unit's pieces in chunk order: the ranges from the one
+    // holding the unit's first task to the one holding its last (the range of
+    // task T is (16 T + 15) / n_tasks), empty ones skipped
     for (int i = tid; i < n_ru * kRowsU * NT; i += kThreadsM) {
         const int ru = i / (kRowsU * NT), rem = i - ru * kRowsU * NT;
-        float s = part[static_cast<size_t>(ru) * kRowsU * NT + rem];
-        for (int q = 1; q < WK; ++q)
-            s = __fadd_rn(s, part[static_cast<size_t>(q * n_ru + ru) * kRowsU * NT + rem]);
+        const int r_a = (kWarpsM * ru * n_c + kWarpsM - 1) / n_tasks;
+        const int r_b = (kWarpsM * ((ru + 1) * n_c - 1) + kWarpsM - 1) / n_tasks;
+        float s = 0.0f;
+        bool first = true;
+        for (int r = r_a; r <= r_b; ++r) {
+            if (r * n_tasks / kWarpsM < (r + 1) * n_tasks / kWarpsM) {
+                const float v = part[static_cast<size_t>(r + ru) * kRowsU * NT + rem];
+                s = first ? v : __fadd_rn(s, v);
+                first = false;
+            }
+        }
         const int tok = rem % NT;
         if (CL == 1) {
             const int row = row0 + ru * kRowsU + rem / NT;
