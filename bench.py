@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 LAYERS = 16
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of k_mv_tc<1,1> on the decode
 # GEMV (profiles/k_mv_tc_decode_gemv_14336x4096.md)
-MV_TC_TRAFFIC_BYTES = None
+MV_TC_TRAFFIC_BYTES = 31266048
 METRIC = "MXFP4 fused dequant-matvec weight GB/s (decode GEMV 14336x4096)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
