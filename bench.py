@@ -352,16 +352,35 @@ def cpu_baseline(seconds_target: float = 12.0):
 
 # --- main ------------------------------------------------------------------------
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """Rank, world size and local rank from the torchrun environment; with more than
+    one rank, the process group (NCCL on the GPUs; gloo runs the same host logic on
+    CPU)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return ws, rank, local
+
+
+def max_over_ranks(secs: float, ws: int) -> float:
+    """The slowest rank's time: every rank's timed region ends at the same barrier,
+    and the whole job's throughput is the work of all ranks over this time."""
+    if ws == 1:
+        return secs
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([secs], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_reference(args, ws, rank):
@@ -468,10 +487,7 @@ def main():
             graph.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop()
-    if ws > 1:
-        t = torch.tensor([secs], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = max_over_ranks(secs, ws)
     value = ws * args.steps * main_w.bytes_per_step / secs / 1e9
     per_launch_s = secs / (args.steps * main_w.launches_per_step)
     achieved = main_w.bytes_per_launch / per_launch_s / 1e9
