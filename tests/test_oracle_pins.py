@@ -245,6 +245,8 @@ def test_moe_gate_up_against_dense_numpy(orc):
             np.testing.assert_allclose(res["u"][p], u, rtol=1e-12, atol=1e-12)
             np.testing.assert_allclose(res["l1g"][p], np.abs(m["mats"]["gate"][e]) @ np.abs(xt),
                                        rtol=1e-12)
+            np.testing.assert_allclose(res["l1u"][p], np.abs(m["mats"]["up"][e]) @ np.abs(xt),
+                                       rtol=1e-12)
             with np.errstate(over="ignore"):
                 act = g / (1.0 + np.exp(-g)) * u
             np.testing.assert_allclose(res["act"][p], act, rtol=1e-11, atol=1e-12)
@@ -266,6 +268,26 @@ def test_moe_down_against_dense_numpy(orc):
         np.testing.assert_allclose(res["out"][t], want, rtol=1e-12, atol=1e-12)
 
 
+def test_moe_down_l1_terms_against_dense_numpy(orc):
+    # l1_pairs[p] = |down_e| |act_p| and l1_out[t] = sum_j |w_tj| l1_pairs[t*K + j]: the
+    # magnitudes the down stage's tolerance is relative to
+    m = _tiny_moe(seed=4)
+    rng = np.random.default_rng(10)
+    act = rng.standard_normal((m["T"] * m["K"], m["inter"])).astype(np.float32)
+    wts = m["wts"].copy()
+    wts[0, 1] = -wts[0, 1]          # a negative route weight still adds |w|
+    res = orc.moe_down(m["banks"]["down"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                       act, m["T"], m["K"], m["ids"], wts, want_pairs=True)
+    for t in range(m["T"]):
+        want = np.zeros(m["hidden"])
+        for j in range(m["K"]):
+            p, e = t * m["K"] + j, m["ids"][t, j]
+            l1p = np.abs(m["mats"]["down"][e]) @ np.abs(act[p].astype(np.float64))
+            np.testing.assert_allclose(res["l1_pairs"][p], l1p, rtol=1e-12)
+            want += abs(np.float64(wts[t, j])) * l1p
+        np.testing.assert_allclose(res["l1_out"][t], want, rtol=1e-12)
+
+
 def test_moe_forward_is_gate_up_then_down_in_double(orc):
     m = _tiny_moe(seed=2)
     fw = orc.moe_forward(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
@@ -284,6 +306,82 @@ def test_moe_forward_is_gate_up_then_down_in_double(orc):
         np.testing.assert_allclose(fw["out"][t], want, rtol=1e-11, atol=1e-11)
     assert (fw["bound_l1"] >= np.abs(fw["out"]) * (1 - 1e-12)).all()
     assert (fw["bound_prop"] > 0).all()
+
+
+def _dense_layer(m, x, wts, dg=None, du=None):
+    """The layer in double from the dense matrices, with optional additive errors
+    dg[p], du[p] on the gate and up dot products of pair p."""
+    out = np.zeros((m["T"], m["hidden"]))
+    acts = {}
+    for t in range(m["T"]):
+        xt = x[t].astype(np.float64)
+        for j in range(m["K"]):
+            p, e = t * m["K"] + j, m["ids"][t, j]
+            g = m["mats"]["gate"][e] @ xt + (0.0 if dg is None else dg[p])
+            u = m["mats"]["up"][e] @ xt + (0.0 if du is None else du[p])
+            with np.errstate(over="ignore"):
+                a = g / (1.0 + np.exp(-g)) * u
+            acts[p] = (g, u, a)
+            out[t] += np.float64(wts[t, j]) * (m["mats"]["down"][e] @ a)
+    return out, acts
+
+
+def test_moe_forward_bound_l1_against_dense_numpy(orc):
+    m = _tiny_moe(seed=5)
+    fw = orc.moe_forward(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
+                         m["stride_gu"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                         m["x"], m["T"], m["K"], m["ids"], m["wts"])
+    _, acts = _dense_layer(m, m["x"], m["wts"])
+    for t in range(m["T"]):
+        want = np.zeros(m["hidden"])
+        for j in range(m["K"]):
+            p, e = t * m["K"] + j, m["ids"][t, j]
+            want += abs(np.float64(m["wts"][t, j])) * (np.abs(m["mats"]["down"][e]) @
+                                                      np.abs(acts[p][2]))
+        np.testing.assert_allclose(fw["bound_l1"][t], want, rtol=1e-12)
+
+
+def test_moe_forward_bound_prop_is_the_worst_first_order_error(orc):
+    # bound_prop's defining property: if every gate dot product g_c may be off by
+    # eps * L1g_c and every up dot product u_c by eps * L1u_c, the largest first-order
+    # change of out[t][r] is eps * bound_prop[t][r].  Attain it: for one output
+    # (t, r), push g_c and u_c of each of t's pairs in the direction that moves
+    # w_tj * down_e[r][c] * act_c upward (signs of w down silu'(g) u and w down
+    # silu(g)), run the perturbed layer densely in numpy, and compare the change
+    # over eps with the oracle's bound.  A bound that dropped |u|, the route
+    # weight, |down| or either term would miss.
+    m = _tiny_moe(seed=6, E=6, hidden=96, inter=64, T=3, K=3)
+    wts = m["wts"].copy()
+    wts[1, 2] = -0.6                  # signs of the route weights matter too
+    fw = orc.moe_forward(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
+                         m["stride_gu"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                         m["x"], m["T"], m["K"], m["ids"], wts)
+    base, acts = _dense_layer(m, m["x"], wts)
+    eps = 1e-7
+    checked = 0
+    for t in range(m["T"]):
+        xt = np.abs(m["x"][t].astype(np.float64))
+        for r in (0, 7, m["hidden"] - 1):
+            dg, du = {}, {}
+            for j in range(m["K"]):
+                p, e = t * m["K"] + j, m["ids"][t, j]
+                g, u, _ = acts[p]
+                s = 1.0 / (1.0 + np.exp(-g))
+                dsilu = s * (1.0 + g * (1.0 - s))
+                coef = np.float64(wts[t, j]) * m["mats"]["down"][e][r]
+                l1g = np.abs(m["mats"]["gate"][e]) @ xt
+                l1u = np.abs(m["mats"]["up"][e]) @ xt
+                dg[p] = eps * l1g * np.sign(coef * dsilu * u)
+                du[p] = eps * l1u * np.sign(coef * g * s)
+            for tt in range(m["T"]):
+                for j in range(m["K"]):
+                    dg.setdefault(tt * m["K"] + j, 0.0)
+                    du.setdefault(tt * m["K"] + j, 0.0)
+            moved, _ = _dense_layer(m, m["x"], wts, dg, du)
+            rate = (moved[t, r] - base[t, r]) / eps
+            assert rate == pytest.approx(fw["bound_prop"][t, r], rel=1e-4), (t, r)
+            checked += 1
+    assert checked == 3 * m["T"]
 
 
 def test_moe_plan_is_a_stable_counting_sort(orc):
