@@ -32,8 +32,9 @@ sys.path.insert(0, ROOT)
 
 LAYERS = 16
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of k_mv_tc<1,1> on the decode
-# GEMV (profiles/k_mv_tc_decode_gemv_14336x4096.md)
+# GEMV, from one ncu capture of `bench.py --profile decode` (cold L2, one launch)
 MV_TC_TRAFFIC_BYTES = 31266048
+REPEATS = 5          # timed regions per workload; the median is reported
 METRIC = "MXFP4 fused dequant-matvec weight GB/s (decode GEMV 14336x4096)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -231,7 +232,7 @@ class MoeLayer(Workload):
                                4 * P * c.inter * 2 + 8 * P)
         self.units_per_step = c.n_tokens
         self.launches_per_step = 4   # plan, gate/up, down, combine
-        self.dominant = "k_moe_pass (gate/up + down)"
+        self.dominant = "k_moe_tc<2> (gate/up) + k_moe_tc<1> (down)"
 
     def step(self):
         c, mx = self.c, self.mx
@@ -287,9 +288,10 @@ class Tiny(DecodeGemv):
 
 # --- timing --------------------------------------------------------------------
 
-def time_graph(work: Workload, steps: int, warmup: int, barrier=None):
-    """Capture one step as a CUDA graph, replay `warmup` untimed and `steps`
-    timed, events on the capture stream.  Returns seconds for the timed steps."""
+def time_graph(work: Workload, steps: int, warmup: int, barrier=None, repeats: int = REPEATS):
+    """Capture one step as a CUDA graph, replay `warmup` untimed, then `repeats`
+    timed regions of `steps` replays each, events on the capture stream.
+    Returns (median seconds of a timed region, all regions' seconds, graph)."""
     import torch
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -302,18 +304,22 @@ def time_graph(work: Workload, steps: int, warmup: int, barrier=None):
     for _ in range(max(warmup, 0)):
         g.replay()
     torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(steps):
-            g.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    return start.elapsed_time(end) / 1e3, g
+    regions = []
+    for _ in range(max(repeats, 1)):
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps):
+                g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        regions.append(start.elapsed_time(end) / 1e3)
+    return statistics.median(regions), regions, g
 
 
 def time_e2e(work, steps: int, warmup: int):
@@ -329,9 +335,27 @@ def time_e2e(work, steps: int, warmup: int):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(seconds_target: float = 12.0):
-    """The oracle as it stands on the host: full decode-GEMV matvecs (one layer
-    per call), repeated until ~seconds_target; GB/s in the bench's units."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rows(fn, rows: int, threads: int):
+    """Run fn(r0, r1) over `threads` contiguous row ranges at once.  The oracle's
+    C functions release the GIL (ctypes), so the ranges run on separate cores:
+    the oracle parallel over output rows, its code unchanged."""
+    if threads <= 1:
+        return [fn(0, rows)]
+    from concurrent.futures import ThreadPoolExecutor
+    cuts = [rows * i // threads for i in range(threads + 1)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda i: fn(cuts[i], cuts[i + 1]), range(threads)))
+
+
+def time_oracle_decode(threads: int, seconds_target: float):
+    """Full decode-GEMV matvecs (one layer per call) until ~seconds_target: GB/s."""
     import oracle
     import synth
     c = synth.DECODE
@@ -340,14 +364,66 @@ def cpu_baseline(seconds_target: float = 12.0):
     per_launch = synth.padded_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.matmat(w, c.rows, c.cols, x, 1)
+        oracle_rows(lambda r0, r1: oracle.matmat(w, c.rows, c.cols, x, 1, r0, r1), c.rows,
+                    threads)
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds_target or n >= 200:
+        if el >= seconds_target or n >= 400:
             break
-    return {"value": n * per_launch / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full {c.rows}x{c.cols} matvecs (one layer each) in {el:.1f} s, "
-                      "single-threaded scalar decode, double accumulation"}
+    return n * per_launch / el / 1e9, n, el
+
+
+def time_oracle_mm8(threads: int, rows_sample: int = 512):
+    """The small-batch product (8 tokens) on a window of rows: weight GB/s, in the
+    bench's byte units scaled to the rows computed."""
+    import oracle
+    import synth
+    c = synth.MM8
+    w, X = c.weights(), c.activations()
+    t0 = time.perf_counter()
+    oracle_rows(lambda r0, r1: oracle.matmat(w, c.rows, c.cols, X, c.nb, r0, r1),
+                rows_sample, threads)
+    el = time.perf_counter() - t0
+    full = synth.padded_nbytes(c.rows, c.cols) + 4 * c.nb * c.cols + 4 * c.nb * c.rows
+    return full * rows_sample / c.rows / el / 1e9, el
+
+
+def time_oracle_moe(n_tokens: int = 2):
+    """The routed-expert layer for the first n_tokens tokens of the MoE workload
+    (their routes and weights), whole layer in the oracle: tokens/s."""
+    import oracle
+    import synth
+    c = synth.MOE
+    gate, up, down = c.banks()
+    x = c.activations()
+    ids, wts = c.routes()
+    t0 = time.perf_counter()
+    oracle.moe_forward(gate, up, down, c.gu_stride, c.down_stride, c.n_experts, c.hidden,
+                       c.inter, x[:n_tokens], n_tokens, c.top_k, ids[:n_tokens],
+                       wts[:n_tokens])
+    el = time.perf_counter() - t0
+    return n_tokens / el, el
+
+
+def cpu_baseline(seconds_target: float = 8.0):
+    """The oracle as it stands on the host cores: the decode GEMV single-threaded
+    and over all cores (row ranges in parallel), plus the small-batch and MoE
+    workloads on bounded samples.  `value` is the all-cores decode-GEMV GB/s."""
+    cores = host_cores()
+    one, n1, el1 = time_oracle_decode(1, seconds_target)
+    allc, na, ela = time_oracle_decode(cores, seconds_target)
+    mm8_gbs, el_mm = time_oracle_mm8(cores)
+    moe_tps, el_moe = time_oracle_moe()
+    return {"value": allc, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"decode GEMV 14336x4096: {na} full matvecs over {cores} threads (row "
+                      f"ranges) in {ela:.1f} s; scalar decode, double accumulation",
+            "single_thread": {"value": one, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} full matvecs in {el1:.1f} s"},
+            "per_workload": {
+                "mm8": {"value": mm8_gbs, "unit": "GB/s", "cores": cores,
+                        "sample": f"512 of 4096 rows x 8 tokens in {el_mm:.1f} s"},
+                "moe": {"value": moe_tps, "unit": "tokens/s", "cores": 1,
+                        "sample": f"2 of 32 tokens, whole layer, in {el_moe:.1f} s"}}}
 
 
 # --- main ------------------------------------------------------------------------
@@ -392,11 +468,17 @@ def run_reference(args, ws, rank):
     w, x = c.weights(), c.activations()
     oracle.lib()
     per = synth.padded_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
+    cores = host_cores()
+
+    def one_layer():
+        oracle_rows(lambda r0, r1: oracle.matmat(w, c.rows, c.cols, x, 1, r0, r1), c.rows,
+                    cores)
+
     for _ in range(args.warmup):
-        oracle.matmat(w, c.rows, c.cols, x, 1)
+        one_layer()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.matmat(w, c.rows, c.cols, x, 1)
+        one_layer()
     el = time.perf_counter() - t0
     value = args.steps * per / el / 1e9
     line = {
@@ -406,8 +488,9 @@ def run_reference(args, ws, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
         "config": {"workload": c.name, "step": "one layer (one matvec) per step",
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} full {c.rows}x{c.cols} matvecs"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full {c.rows}x{c.cols} matvecs, row ranges "
+                                   f"over {cores} threads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -479,7 +562,7 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    secs, graph = time_graph(main_w, args.steps, args.warmup, barrier)
+    secs, regions, graph = time_graph(main_w, args.steps, args.warmup, barrier)
     # keep the same step running ~1 s so the sampler sees the clocks under this load
     t_end = time.perf_counter() + 1.0
     while time.perf_counter() < t_end:
@@ -491,6 +574,12 @@ def main():
     value = ws * args.steps * main_w.bytes_per_step / secs / 1e9
     per_launch_s = secs / (args.steps * main_w.launches_per_step)
     achieved = main_w.bytes_per_launch / per_launch_s / 1e9
+    # the same step with launch overlap off: every launch waits for the previous one
+    mx.mxfp4_set_launch_overlap(False)
+    secs_off, _, g_off = time_graph(main_w, args.steps, args.warmup, barrier)
+    del g_off
+    mx.mxfp4_set_launch_overlap(True)
+    us_off = secs_off / (args.steps * main_w.launches_per_step) * 1e6
 
     e2e_secs = time_e2e(main_w, max(args.steps // 5, 3), args.warmup)
     e2e_steps = max(args.steps // 5, 3)
@@ -501,8 +590,9 @@ def main():
         for cls in (SmallBatch, MoeLayer, Prefill, Tiny):
             try:
                 w = cls(mx)
-                k = max(args.steps // 5, 5)
-                s, _ = time_graph(w, k, args.warmup)
+                k = max(args.steps, 20)
+                s, _, g_w = time_graph(w, k, args.warmup)
+                del g_w
                 per = s / k
                 entry = {"workload": w.name, "ms_per_step": per * 1e3,
                          "launches_per_step": w.launches_per_step}
@@ -545,13 +635,15 @@ def main():
                        "nb": 1, "layers_per_step": LAYERS,
                        "l2": f"inputs larger than L2: {LAYERS} distinct weight buffers, "
                              f"{LAYERS * main_w.bytes_per_launch / 1e6:.0f} MB per step",
-                       "timing": "CUDA graph of one step, CUDA events on its stream",
-                       "launch_overlap": "on (mxfp4_set_launch_overlap)"},
+                       "timing": f"CUDA graph of one step, CUDA events on its stream; median "
+                                 f"of {len(regions)} timed regions of {args.steps} steps each",
+                       "regions_ms_per_step": [r / args.steps * 1e3 for r in regions],
+                       "launch_overlap": "on (mxfp4_set_launch_overlap)",
+                       "us_per_launch_overlap_off": us_off},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                          # dram__bytes_read.sum + dram__bytes_write.sum of one launch of
-                         # the same kernel on the same workload (ncu capture in
-                         # profiles/k_mv_tc_decode_gemv_14336x4096.md)
+                         # the same kernel on the same workload (one ncu capture)
                          "traffic": MV_TC_TRAFFIC_BYTES, "peak_source": pk["source"],
                          "kernel": main_w.dominant,
                          "bytes_per_launch": main_w.bytes_per_launch,

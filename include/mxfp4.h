@@ -227,7 +227,10 @@ int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter,
  *     with MXFP4_STATUS_WORKSPACE_TOO_SMALL (use the workspace entry points).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per device together
+ *     with the id of the context it belongs to; after the device's context is
+ *     destroyed and created again (cudaDeviceReset), the next call looks it up
+ *     again, so make that call outside stream capture as well.
  *   - Every call uses the same array and the array keeps the previous call's
  *     contents; each call rewrites all of the scratch it reads, so nothing has
  *     to start at zero.  Calls that overlap on the GPU (other streams, other

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -73,6 +74,31 @@ cudaError_t read_fault_moetc(int* value, bool reset);
 
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);
+
+// A value computed once per device and then reused: kernel attributes (the
+// dynamic shared-memory limit), SM counts and occupancies belong to a device,
+// so a value obtained with one device current is never reused on another.
+// `compute` runs with the device current, under the memo's lock.
+class PerDevice {
+  public:
+    template <class F>
+    int get(F&& compute) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) return compute();
+        std::lock_guard<std::mutex> lock(mu_);
+        if (!done_[dev]) {
+            val_[dev] = compute();
+            done_[dev] = true;
+        }
+        return val_[dev];
+    }
+
+  private:
+    static constexpr int kMax = 64;
+    std::mutex mu_;
+    bool done_[kMax] = {};
+    int val_[kMax] = {};
+};
 
 // Bytes of one [rows, cols] buffer, padded to 16.
 inline size_t padded_nbytes(int rows, int cols) {

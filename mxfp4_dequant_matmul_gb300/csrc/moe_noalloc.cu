@@ -14,7 +14,13 @@
 // The array's name in host code is a host-side stand-in, not a device
 // address, so the device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and passed to the kernels.
+// The address belongs to the context that loaded the library's module: if the
+// device's context is destroyed and made again (cudaDeviceReset), the next
+// call sees a new context id and looks the address up again.
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "../../include/mxfp4.h"
 #include "kernels.h"
@@ -28,20 +34,50 @@ __device__ __align__(256) unsigned char g_moe_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mu;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_addr_ctx[kMaxDevices] = {};
 
-// Device address of g_moe_scratch on the current device (looked up on first
-// use per device, then cached).
+// Unique id of the calling thread's current context (0 if the driver cannot
+// say): an address cached under one context is not used under another.
+unsigned long long current_context_id() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_moe_scratch on the current device: looked up on the
+// first call per device (and again after the device's context was replaced),
+// then cached.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // 0 before the runtime has made a context current: then the lookup below
+    // runs (and makes it current), and the next call caches under its id
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_addr_mu);
-    if (g_addr[dev] == nullptr) {
+    if (g_addr[dev] == nullptr || ctx == 0 || ctx != g_addr_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_moe_scratch);
         if (e != cudaSuccess) return e;
         g_addr[dev] = p;
+        g_addr_ctx[dev] = ctx;
     }
     *out = g_addr[dev];
     return cudaSuccess;

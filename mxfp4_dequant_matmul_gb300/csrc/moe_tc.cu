@@ -512,13 +512,13 @@ bool bank_map(CUtensorMap* map, const uint8_t* bank, size_t stride, int n_expert
 }
 
 int sm_count_e() {
-    static std::once_flag once;
-    static int n = 0;
-    std::call_once(once, [] {
-        int dev = 0;
+    static PerDevice memo;
+    const int n = memo.get([] {
+        int dev = 0, v = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 0;
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            v = 0;
+        return v;
     });
     return n > 0 ? n : 1;
 }
@@ -533,12 +533,11 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
     if (l.total > kSmemMaxE) return cudaErrorNotSupported;
     auto kernel = k_moe_tc<NM>;
     {
-        static std::once_flag once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(once, [&] {
-            attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kSmemMaxE));
-        });
+        static PerDevice memo;
+        const cudaError_t attr_err = static_cast<cudaError_t>(memo.get([&] {
+            return static_cast<int>(cudaFuncSetAttribute(
+                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemMaxE)));
+        }));
         if (attr_err != cudaSuccess) return attr_err;
     }
     CUtensorMap m0, m1;

@@ -549,13 +549,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_m() {
 std::atomic<bool> g_overlap{false};
 
 int sm_count_m() {
-    static std::once_flag once;
-    static int n = 0;
-    std::call_once(once, [] {
-        int dev = 0;
+    static PerDevice memo;
+    const int n = memo.get([] {
+        int dev = 0, v = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 0;
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            v = 0;
+        return v;
     });
     return n > 0 ? n : 1;
 }
@@ -565,18 +565,15 @@ int sm_count_m() {
 // the number of tokens either.
 template <int CL>
 int resident_mv() {
-    static std::once_flag once;
-    static int resident = 0;
-    std::call_once(once, [] {
+    static PerDevice memo;
+    return memo.get([] {
+        int resident = 0;
         const MvLayout lmax = mv_layout(4, kGMax, kMaxRuCta, kMinStagesM);
         auto k4 = k_mv_tc<4, CL>;
         if (cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemMaxM)) != cudaSuccess)
-            return;
-        if (CL == 1) {
-            resident = sm_count_m();
-            return;
-        }
+            return 0;
+        if (CL == 1) return sm_count_m();
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(CL * 64, 1);
         q.blockDim = dim3(kThreadsM);
@@ -590,8 +587,8 @@ int resident_mv() {
         q.numAttrs = 1;
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, k4, &q) == cudaSuccess && nc > 0) resident = nc;
+        return resident;
     });
-    return resident;
 }
 
 template <int NT, int CL>
@@ -603,12 +600,11 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     const int resident = resident_mv<CL>();
     if (resident < 1) return cudaErrorNotSupported;
     {
-        static std::once_flag once;
-        static cudaError_t attr_err = cudaSuccess;
-        std::call_once(once, [&] {
-            attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kSmemMaxM));
-        });
+        static PerDevice memo;
+        const cudaError_t attr_err = static_cast<cudaError_t>(memo.get([&] {
+            return static_cast<int>(cudaFuncSetAttribute(
+                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemMaxM)));
+        }));
         if (attr_err != cudaSuccess) return attr_err;
     }
     const int n_ru_all = (rows + kRowsU - 1) / kRowsU;

@@ -104,7 +104,11 @@ int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t st
 
 int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y, cudaStream_t stream) {
     MXFP4_TRY(check_product(w, rows, cols, x, 1, y));
+    // the same kernel order as mxfp4_mm, so that a batch equals its matvecs
     cudaError_t e = mxk::launch_mv_tc(u8(w), rows, cols, x, 1, y, stream);
+    if (e != cudaErrorNotSupported) return from_cuda(e);
+    (void)cudaGetLastError();
+    e = mxk::launch_mm_tc(u8(w), rows, cols, x, 1, y, stream);
     if (e != cudaErrorNotSupported) return from_cuda(e);
     (void)cudaGetLastError();
     return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, x, 1, y, stream));

@@ -598,12 +598,12 @@ cudaError_t launch_prefill2(const uint8_t* w, int rows, int cols, const float* X
         !map2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, gpr, rows, gpr, 16, kPN))
         return cudaErrorNotSupported;
     constexpr P2Layout l = p2_layout();
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(k_prefill2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(p2_layout().total));
-    });
+    static PerDevice memo;
+    const cudaError_t attr_err = static_cast<cudaError_t>(memo.get([] {
+        return static_cast<int>(cudaFuncSetAttribute(
+            k_prefill2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            static_cast<int>(p2_layout().total)));
+    }));
     if (attr_err != cudaSuccess) return attr_err;
     const dim3 grid((rows + kPN - 1) / kPN, (nb + kPM - 1) / kPM);
     k_prefill2<<<grid, kPThreads, l.total, s>>>(xmap, wmap, smap, rows, cols, nb, Y);
@@ -923,18 +923,18 @@ cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X
                                                     reinterpret_cast<uint2*>(xb));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
+    static PerDevice memo;
     const size_t smem = static_cast<size_t>(kGStages) * kPStageBytes + 1024;   // (tn <= 256)
-    std::call_once(once, [smem] {
-        attr_err = cudaFuncSetAttribute(k_gemm_bf16<256>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(k_gemm_bf16<224>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(smem));
-    });
+    const cudaError_t attr_err = static_cast<cudaError_t>(memo.get([smem] {
+        cudaError_t a = cudaFuncSetAttribute(k_gemm_bf16<256>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (a == cudaSuccess)
+            a = cudaFuncSetAttribute(k_gemm_bf16<224>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+        return static_cast<int>(a);
+    }));
     if (attr_err != cudaSuccess) return attr_err;
     const long tiles = tiles_of(tn);
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);

@@ -324,5 +324,30 @@ def test_launch_overlap_back_to_back_matvecs(mx):
         assert_bits_equal(g, w_, f"back-to-back layer {i} with launch overlap")
 
 
-def test_no_device_faults_after_the_suite(mx):
-    assert mx.mxfp4_device_faults(reset=True) == 0
+@pytest.mark.parametrize("nb", [1, 2, 8])
+def test_rows_too_wide_for_the_matvec_kernel(mx, nb):
+    # 1152 groups per row: more than a cluster of eight k_mv_tc CTAs stages, so
+    # mxfp4_mv and mxfp4_mm run the cluster split-K kernel k_mma_small
+    rows, cols = 64, 36864
+    w_h = synth.mxfp4_matrix(rows, cols, 700 + nb, 118, 130)
+    X = synth.normal_f32(710 + nb, nb * cols).reshape(nb, cols)
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} nb={nb}")
+    for t in range(nb):
+        assert_bits_equal(Y[t], run_mv(mx, w_h, rows, cols, X[t]), f"token {t} vs its matvec")
+
+
+def test_rows_too_wide_for_both_tensor_kernels(mx):
+    # 1728 groups per row: neither tensor-core kernel stages the row's
+    # activations, so mxfp4_mv and mxfp4_mm take the FP32 path
+    rows, cols, nb = 40, 55296, 3
+    w_h = synth.mxfp4_matrix(rows, cols, 720, 118, 130)
+    X = synth.normal_f32(721, nb * cols).reshape(nb, cols)
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    assert_within(Y, ref, l1, REL_FP32, f"{rows}x{cols} nb={nb}")
+    for t in range(nb):
+        y = run_mv(mx, w_h, rows, cols, X[t])
+        assert_within(y, ref[t], l1[t], REL_FP32, f"{rows}x{cols} mv token {t}")
+        assert_bits_equal(Y[t], y, f"token {t} vs its matvec")

@@ -136,3 +136,27 @@ def test_dense_after_dequant_prefill_config_samples_and_short_workspace(mx):
     x_small = to_dev(synth.normal_f32(3, 8 * 512))
     with pytest.raises(mx.Mxfp4Error):
         mx.mxfp4_mm_bf16_ws(w_small, 64, 512, x_small, 8, empty(8 * 64), ws, nbytes - 1)
+
+
+@pytest.mark.parametrize("fn", ["mxfp4_mm", "mxfp4_mm_bf16_ws"])
+def test_prefill_config_full_token_bands(mx, fn):
+    # every output of the first and the last 128-token band (one tile row of
+    # the tensor-core kernels) over all 4096 rows: every epilogue position of
+    # every weight tile.  The reference is the oracle's exact decode followed
+    # by a float64 matrix product (numpy standing for the oracle's double dot
+    # products, checked against oracle.matmat on a row window below).
+    cfg = synth.PREFILL
+    w_h, X = cfg.weights(), cfg.activations()
+    if fn == "mxfp4_mm":
+        Y = run(mx, fn, w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    else:
+        Y = run_ws(mx, w_h, cfg.rows, cfg.cols, X, cfg.nb)
+    Wd = oracle.dequant(w_h, cfg.rows, cfg.cols).astype(np.float64)
+    for t0 in (0, cfg.nb - 128):
+        Xb = oracle.round_bf16(X[t0:t0 + 128])
+        ref = Xb.astype(np.float64) @ Wd.T
+        l1 = np.abs(Xb.astype(np.float64)) @ np.abs(Wd).T
+        win, win_l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, Xb, 128, 1000, 1004)
+        np.testing.assert_allclose(ref[:, 1000:1004], win, rtol=0, atol=1e-12 * win_l1.max())
+        assert_within(Y[t0:t0 + 128], ref, l1, REL_BF16, f"{fn} band {t0}")
+        assert_within(Y[t0:t0 + 128], ref, l1, REL_FP32, f"{fn} band {t0}, FP32 bound")

@@ -4,64 +4,69 @@
 It serves callers that cannot allocate device memory when they run the layer
 (all of their device memory belongs to their own pool allocator, or they must
 not call cudaMalloc once running because it can block the device).  Its
-scratch is a fixed array inside the library, shared by every call, so this
-test makes two calls in a row with different inputs -- the second one finds
-the first one's leftovers in the array -- and checks each against the
-workspace entry points (mxfp4_moe_gate_up + mxfp4_moe_down) within the suite's
-FP32 tolerance.  The file is named to run last: it must pass alone in a fresh
-process and after every other test.
+scratch is a fixed array inside the library, shared by every call and keeping
+the previous call's contents.  So this test runs a large problem and then a
+small one -- the small call finds the large call's plan, activations and
+per-pair outputs in the array past its own -- and checks every call against
+the CPU oracle within the suite's FP32 tolerance, and that the small call
+changes neither the device's free memory nor torch's allocations.  The file
+is named to run last: it must pass alone in a fresh process and after every
+other test.
 """
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_util import REL_FP32, assert_within, cuda, empty, host, to_dev
+from gpu_util import REL_FP32, assert_within, cuda, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
+SMALL = dict(E=4, hidden=256, inter=128, T=3, K=2)
+LARGE = dict(E=64, hidden=512, inter=384, T=32, K=4)
 
-def _case(seed, E=8, hidden=256, inter=192, T=12, K=3):
+
+def _case(seed, E, hidden, inter, T, K):
     cfg = synth.MoeConfig("noalloc case", E, hidden, inter, T, K, seed)
     gate, up, down = cfg.banks()
     ids, wts = cfg.routes()
     return cfg, gate, up, down, cfg.activations(), ids.astype(np.int32), wts
 
 
-def _with_workspace(mx, cfg, d):
-    P = cfg.n_tokens * cfg.top_k
-    nbytes = mx.mxfp4_moe_workspace_bytes(cfg.n_experts, cfg.n_tokens, cfg.top_k, cfg.hidden,
-                                          cfg.inter)
-    ws = empty(nbytes // 4 + 4)
-    act = empty(P * cfg.inter)
-    y = empty(cfg.n_tokens * cfg.hidden)
-    mx.mxfp4_moe_gate_up(d["gate"], d["up"], cfg.n_experts, cfg.hidden, cfg.inter, d["x"],
-                         cfg.n_tokens, cfg.top_k, d["ids"], act, ws)
-    mx.mxfp4_moe_down(d["down"], cfg.n_experts, cfg.hidden, cfg.inter, act, cfg.n_tokens,
-                      cfg.top_k, d["ids"], d["wts"], y, ws)
-    return host(y)
-
-
-def test_noalloc_layer_matches_the_workspace_entry_points_on_two_calls():
+def _call_and_check(mx, seed, shape, check_memory=False):
     import torch
+    cfg, gate, up, down, x, ids, wts = _case(seed, **shape)
+    d = {"gate": to_dev(gate), "up": to_dev(up), "down": to_dev(down), "x": to_dev(x),
+         "ids": to_dev(ids), "wts": to_dev(wts)}
+    y = torch.full((cfg.n_tokens * cfg.hidden,), float("nan"), device="cuda:0")
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    status = mx.lib().mxfp4_moe_layer_noalloc(
+        d["gate"].data_ptr(), d["up"].data_ptr(), d["down"].data_ptr(), cfg.n_experts,
+        cfg.hidden, cfg.inter, d["x"].data_ptr(), cfg.n_tokens, cfg.top_k,
+        d["ids"].data_ptr(), d["wts"].data_ptr(), y.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    assert status == 0, mx.mxfp4_status_string(status)
+    if check_memory:
+        assert free1 == free0, f"device free memory changed by {free1 - free0} bytes"
+        assert alloc1 == alloc0, f"torch allocations changed by {alloc1 - alloc0} bytes"
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, cfg.n_experts,
+                             cfg.hidden, cfg.inter, x, cfg.n_tokens, cfg.top_k, ids, wts)
+    assert_within(host(y), ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32,
+                  f"no-alloc layer (seed {seed}, {cfg.n_experts} experts, {cfg.n_tokens} tokens)")
+
+
+def test_noalloc_layer_matches_the_oracle_large_then_small():
     mx = cuda()
-    for seed in (31, 32):          # two calls in a row, different inputs
-        cfg, gate, up, down, x, ids, wts = _case(seed)
-        d = {"gate": to_dev(gate), "up": to_dev(up), "down": to_dev(down), "x": to_dev(x),
-             "ids": to_dev(ids), "wts": to_dev(wts)}
-        want = _with_workspace(mx, cfg, d)
-        y = torch.full((cfg.n_tokens * cfg.hidden,), float("nan"), device="cuda:0")
-        status = mx.lib().mxfp4_moe_layer_noalloc(
-            d["gate"].data_ptr(), d["up"].data_ptr(), d["down"].data_ptr(), cfg.n_experts,
-            cfg.hidden, cfg.inter, d["x"].data_ptr(), cfg.n_tokens, cfg.top_k,
-            d["ids"].data_ptr(), d["wts"].data_ptr(), y.data_ptr(),
-            torch.cuda.current_stream().cuda_stream)
-        assert status == 0, mx.mxfp4_status_string(status)
-        got = host(y)
-        ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, cfg.n_experts,
-                                 cfg.hidden, cfg.inter, x, cfg.n_tokens, cfg.top_k, ids, wts)
-        bound = ref["bound_l1"] + ref["bound_prop"]
-        assert_within(got, want, bound, REL_FP32, f"no-alloc call (seed {seed}) vs workspace")
+    # the first call on the device looks up the array's address and loads the
+    # kernels; the large call then fills more of the array than the small one
+    # reads, and the second small call must neither see those leftovers nor
+    # allocate anything
+    _call_and_check(mx, 31, SMALL)
+    _call_and_check(mx, 32, LARGE)
+    _call_and_check(mx, 33, SMALL, check_memory=True)
 
 
 def test_noalloc_layer_refuses_problems_larger_than_its_array():
