@@ -114,8 +114,10 @@ int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
  * X: [nb, cols] row-major floats, Y: [nb, rows] (the page's matmat output
  * layout).  Dispatch on nb:
  *   nb <= MXFP4_MM_SMALL_MAX: the small-batch path -- each weight group is
- *     decoded once and applied to up to 4 tokens per pass over the weights
- *     (PEROP mxfp4_mm shares one decode by up to 8); the arithmetic of
+ *     decoded once and applied to up to 8 tokens per pass over the weights
+ *     (PEROP mxfp4_mm: one decode shared by up to 8 tokens; shapes whose
+ *     eight-token fragments do not fit in shared memory take passes of 4,
+ *     with the same results); the arithmetic of
  *     mxfp4_mv, so per token the result equals mxfp4_mv on that token bit
  *     for bit, whatever the rest of the batch (the page's device test:
  *     "the batch equal to the matvec per token bit for bit").

@@ -1,4 +1,4 @@
-// mv_tc.cu -- MXFP4 matvec and products with up to four tokens per pass, the
+// mv_tc.cu -- MXFP4 matvec and products with up to eight tokens per pass, the
 // dot products on the tensor cores through mma.sync (sm_103a).
 //
 // Y[t*rows + r] = sum_c W[r][c] X[t][c]  ("cortiq-engine 0.8.40
@@ -27,7 +27,10 @@
 // added to one of four FP32 sums per row and token, r = group mod 4 (in group
 // order), and the four are added as ((P0 + P1) + P2) + P3 at the end.  So the
 // arithmetic per token is the same for one, two or four tokens: the batched
-// product equals the matvec bit for bit.  Any scale byte is handled exactly
+// product equals the matvec bit for bit.  Eight tokens take two column sets
+// (tokens 0-3 and 4-7, one n8 MMA each) on the same decoded A fragments, one
+// group per accumulator as with four tokens: each group is decoded once for
+// all eight.  Any scale byte is handled exactly
 // (255 gives NaN) and no partial sum overflows unless the result does.
 //
 // Data movement: a unit is 32 rows x 8 groups (32 rows x 128 code bytes), one
@@ -56,6 +59,13 @@ namespace {
 
 constexpr int kWarpsM = 16;
 constexpr int kThreadsM = kWarpsM * 32;
+// The CTA's tasks are always split into 16 ranges: the ranges fix the order of
+// every sum.  Up to four tokens, each of 16 warps takes one range; eight tokens
+// need twice the activation fragments in shared memory and twice the
+// accumulators, so 8 warps take two consecutive ranges each (the same sums in
+// the same order, so a token's result does not depend on the token count).
+constexpr int kRangesM = 16;
+__host__ __device__ constexpr int warps_mv(int NT) { return NT == 8 ? 8 : kWarpsM; }
 constexpr int kRowsU = 32;                  // rows per unit (two MMA row blocks)
 constexpr int kChunkM = 8;                  // groups per unit (128 code bytes per row)
 constexpr int kStageM = kRowsU * 128;       // one TMA tile, 4 KB
@@ -125,16 +135,16 @@ __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, in
     l.part = (l.part + 15u) & ~15u;
     // [rows][NT]; zero during the units: its bytes 32 .. 47 are the B values of
     // the lanes that hold none
-    l.fin = l.part + static_cast<uint32_t>(kWarpsM + ru_cta - 1) * kRowsU * NT * 4;
-    l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[4], tmax[4]
-    l.bars = (l.misc + 64 + 7u) & ~7u;
-    l.ring = (l.bars + kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
-    l.total = l.ring + static_cast<uint32_t>(kWarpsM * stages) * kStageM + 1024;   // + align slack
+    l.fin = l.part + static_cast<uint32_t>(kRangesM + ru_cta - 1) * kRowsU * NT * 4;
+    l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[8], tmax[8], flag
+    l.bars = (l.misc + 80 + 7u) & ~7u;
+    l.ring = (l.bars + warps_mv(NT) * kMaxStagesM * 8 + 1023u) & ~1023u;
+    l.total = l.ring + static_cast<uint32_t>(warps_mv(NT) * stages) * kStageM + 1024;   // + align slack
     return l;
 }
 
 template <int NT, int CL>
-__global__ void __launch_bounds__(kThreadsM, 1)
+__global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     k_mv_tc(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ w, int rows,
             int cols, const float* __restrict__ X, int nb, float* __restrict__ Y, int ru_cta,
             int ng_max, int stages, int overlap) {
@@ -147,9 +157,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     uint8_t* sc_s = smem + L.sc;
     float* part = reinterpret_cast<float*>(smem + L.part);
     float* fin = reinterpret_cast<float*>(smem + L.fin);
-    int* pexp = reinterpret_cast<int*>(smem + L.misc);                 // [4]
-    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);  // [4]
-    int* not_plain = reinterpret_cast<int*>(smem + L.misc + 32);
+    constexpr int kW = warps_mv(NT), kThr = kW * 32, kRpw = kRangesM / kW;
+    int* pexp = reinterpret_cast<int*>(smem + L.misc);                 // [8]
+    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 32);  // [8]
+    int* not_plain = reinterpret_cast<int*>(smem + L.misc + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -169,16 +180,21 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     const size_t plane = static_cast<size_t>(rows) * cols / 2;
 
     // The CTA's (row unit, chunk) tasks, row unit major, in 16 contiguous ranges
-    // as equal as the count allows (shape only).  Warp w takes range w when the
-    // count divides evenly (consecutive warps then stream neighbouring rows),
-    // else range (w mod 4) 4 + w / 4, so that each scheduler (the warps
-    // w = s mod 4) holds a contiguous quarter of the tasks.  A warp's sums become
-    // the piece of its range for a row unit (slot range + row unit) whenever its
-    // range leaves the unit.
+    // as equal as the count allows (shape only).  With 16 warps, warp w takes
+    // range w when the count divides evenly (consecutive warps then stream
+    // neighbouring rows), else range (w mod 4) 4 + w / 4, so that each scheduler
+    // (the warps w = s mod 4) holds a contiguous quarter of the tasks; with 8
+    // warps, warp w takes ranges 2w and 2w + 1 one after the other.  A warp's
+    // sums become the piece of its range for a row unit (slot range + row unit)
+    // whenever its range leaves the unit or ends.
     const int n_tasks = n_ru * n_c;
-    const int rg = n_tasks % kWarpsM == 0 ? warp : (warp & 3) * (kWarpsM / 4) + (warp >> 2);
-    const int t_lo = rg * n_tasks / kWarpsM;
-    const int n_units = (rg + 1) * n_tasks / kWarpsM - t_lo;
+    const int rg0 = kRpw > 1 ? warp * kRpw
+                             : (n_tasks % kRangesM == 0 ? warp
+                                                        : (warp & 3) * (kRangesM / 4) + (warp >> 2));
+    const int t_lo = rg0 * n_tasks / kRangesM;
+    const int n_units = (rg0 + kRpw) * n_tasks / kRangesM - t_lo;
+    int rg = rg0;                                          // the range of the current unit
+    int rg_end = (rg0 + 1) * n_tasks / kRangesM;           // its end (a task index)
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * stages;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * stages * kStageM;
@@ -199,7 +215,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     if (overlap) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < NT) tmax[tid] = 0u;
     if (tid == 0) *not_plain = 0;
-    for (int i = tid; i < ru_cta * kRowsU * NT / 4; i += kThreadsM)
+    for (int i = tid; i < ru_cta * kRowsU * NT / 4; i += kThr)
         reinterpret_cast<uint4*>(fin)[i] = make_uint4(0u, 0u, 0u, 0u);
 
     // --- prologue: E8M0 table, scale bytes, activations
@@ -209,11 +225,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // alignment (ragged words are stored byte by byte below)
     const bool sc_whole = gpr % 16 == 0 && g_lo % 16 == 0 && ng % 16 == 0;
     const int nch_row = sc_whole ? ng / 16 : (ng + 30) / 16;
-    constexpr int kScU = (kMaxRuCta * kRowsU * ((kGMax + 30) / 16) + kThreadsM - 1) / kThreadsM;
+    constexpr int kScU = (kMaxRuCta * kRowsU * ((kGMax + 30) / 16) + kThr - 1) / kThr;
     uint4 sv[kScU];
 #pragma unroll
     for (int u = 0; u < kScU; ++u) {
-        const int i = tid + u * kThreadsM;
+        const int i = tid + u * kThr;
         const int r = i / nch_row, c = i - r * nch_row;
         sv[u] = make_uint4(0u, 0u, 0u, 0u);
         if (r < nrow) {
@@ -244,24 +260,58 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         start_weights(0, kPreStagesM);
         asm volatile("griddepcontrol.wait;" ::: "memory");
     }
-    // activation items: (token, group, word) = 8 elements
-    constexpr int kXU = (NT * kGMax * 4 + kThreadsM - 1) / kThreadsM;
+    // activation items: (token, group, word) = 8 elements.  Up to four tokens
+    // they wait in registers for the tokens' powers of two; eight tokens are
+    // first staged as floats in the shared-memory bytes their own hi and lo
+    // fragments will take (32 bytes per item, so the split below is in place).
+    constexpr bool kStaged = NT == 8;
+    constexpr int kXU = kStaged ? 1 : (NT * kGMax * 4 + kThr - 1) / kThr;
     const int n_items = NT * ng * 4;
     float xv[kXU][8];
+    float mloc[NT];   // staged: this thread's largest finite |x| per token
 #pragma unroll
-    for (int u = 0; u < kXU; ++u) {
-        const int i = tid + u * kThreadsM;
-        const int tok = i / (ng * 4), rem = i - tok * ng * 4;
-        if (i < n_items && tok < nbt) {
-            const float4* src = reinterpret_cast<const float4*>(
-                X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
-                8 * rem);
-            const float4 a = __ldg(src), b = __ldg(src + 1);
-            xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
-            xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
-        } else {
+    for (int q = 0; q < NT; ++q) mloc[q] = 0.0f;
+    if constexpr (!kStaged) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
+        for (int u = 0; u < kXU; ++u) {
+            const int i = tid + u * kThr;
+            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
+            if (i < n_items && tok < nbt) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
+                    8 * rem);
+                const float4 a = __ldg(src), b = __ldg(src + 1);
+                xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+                xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
+            }
+        }
+    } else {
+        for (int i = tid; i < n_items; i += kThr) {
+            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
+            const int j = rem >> 2, tw = rem & 3;
+            float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
+            if (tok < nbt) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
+                    8 * rem);
+                a = __ldg(src);
+                b = __ldg(src + 1);
+            }
+            const float e8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float m = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = fabsf(e8[e]);
+                m = fmaxf(m, v <= 3.402823466e38f ? v : 0.0f);   // NaN and inf do not count
+            }
+#pragma unroll
+            for (int q = 0; q < NT; ++q)
+                if (q == tok) mloc[q] = fmaxf(mloc[q], m);
+            reinterpret_cast<float4*>(xf)[j * (8 * NT) + (2 * tok) * 4 + tw] = a;
+            reinterpret_cast<float4*>(xf)[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = b;
         }
     }
     start_weights(overlap ? kPreStagesM : 0, stages);   // after the prologue's loads
@@ -274,7 +324,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     bool odd = false;
 #pragma unroll
     for (int u = 0; u < kScU; ++u) {
-        const int i = tid + u * kThreadsM;
+        const int i = tid + u * kThr;
         const int r = i / nch_row, c = i - r * nch_row;
         if (r < nrow) {
             const int mis =
@@ -299,20 +349,28 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             }
         }
     }
+    if constexpr (!kStaged) {
 #pragma unroll
-    for (int u = 0; u < kXU; ++u) {
-        const int i = tid + u * kThreadsM;
-        const int tok = min(i / (ng * 4), NT - 1);
-        float m = 0.0f;
+        for (int u = 0; u < kXU; ++u) {
+            const int i = tid + u * kThr;
+            const int tok = min(i / (ng * 4), NT - 1);
+            float m = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float a = fabsf(xv[u][e]);
-            m = fmaxf(m, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
+            for (int e = 0; e < 8; ++e) {
+                const float a = fabsf(xv[u][e]);
+                m = fmaxf(m, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
+            }
+            // lanes of a token reduce together; one atomic per token and warp
+            const unsigned same = __match_any_sync(0xffffffffu, tok);
+            const unsigned mb = __reduce_max_sync(same, __float_as_uint(m));
+            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
         }
-        // lanes of a token reduce together; one atomic per token and warp
-        const unsigned same = __match_any_sync(0xffffffffu, tok);
-        const unsigned mb = __reduce_max_sync(same, __float_as_uint(m));
-        if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
+    } else {
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mloc[q]));
+            if (mb != 0u && lane == 0) atomicMax(&tmax[q], mb);
+        }
     }
     if (__any_sync(0xffffffffu, odd) && lane == 0) atomicOr(not_plain, 1);
     __syncthreads();
@@ -322,64 +380,95 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         pexp[tid] = m > 0.0f ? min(14 - ilogbf(m), 126) : 0;
     }
     __syncthreads();
+    // x 2^p -> f16 hi = f16(x 2^p) and lo = f16(x 2^p - hi), 8 elements per item
+    auto split8 = [&](const float (&e8)[8], int tok, int j, int tw) {
+        const float pm = exp2i_m(pexp[tok]);   // 2^p is a normal float
+        uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int u = 0; u < kXU; ++u) {
-        const int i = tid + u * kThreadsM;
-        if (i < n_items) {
+        for (int k = 0; k < 4; ++k) {
+            const float a0 = __fmul_rn(e8[2 * k], pm), a1 = __fmul_rn(e8[2 * k + 1], pm);
+            hi[k] = pack_f16x2_m(a0, a1);
+            const float2 h = f16x2_to_f32x2(hi[k]);
+            lo[k] = pack_f16x2_m(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
+        }
+        xf[j * (8 * NT) + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        xf[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    };
+    if constexpr (!kStaged) {
+#pragma unroll
+        for (int u = 0; u < kXU; ++u) {
+            const int i = tid + u * kThr;
+            if (i < n_items) {
+                const int tok = i / (ng * 4), rem = i - tok * ng * 4;
+                split8(xv[u], tok, rem >> 2, rem & 3);
+            }
+        }
+    } else {
+        for (int i = tid; i < n_items; i += kThr) {
             const int tok = i / (ng * 4), rem = i - tok * ng * 4;
             const int j = rem >> 2, tw = rem & 3;
-            const float pm = exp2i_m(pexp[tok]);   // 2^p is a normal float
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float a0 = __fmul_rn(xv[u][2 * k], pm), a1 = __fmul_rn(xv[u][2 * k + 1], pm);
-                hi[k] = pack_f16x2_m(a0, a1);
-                const float2 h = f16x2_to_f32x2(hi[k]);
-                lo[k] = pack_f16x2_m(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
-            }
-            xf[j * (8 * NT) + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            xf[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const float4 a = reinterpret_cast<const float4*>(xf)[j * (8 * NT) + (2 * tok) * 4 + tw];
+            const float4 b =
+                reinterpret_cast<const float4*>(xf)[j * (8 * NT) + (2 * tok + 1) * 4 + tw];
+            const float e8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            split8(e8, tok, j, tw);
         }
     }
     __syncthreads();
 
     // --- this warp's units
-    constexpr int GP = 4 / NT;   // groups sharing one accumulator
-    const int slot = t / NT, tok = t % NT;   // D columns 2t, 2t + 1: group slot, token
-    // acc[q][i]: row g + 8q, token tok, sum r = slot + GP i (groups j, j mod 4 = r)
-    float acc[4][NT];
+    // NS column sets of one n8 MMA each: tokens 4 s .. 4 s + 3 in set s (eight
+    // tokens), else one set holding all NT tokens
+    constexpr int NS = NT == 8 ? 2 : 1;
+    constexpr int NTS = NT / NS;   // tokens per column set
+    constexpr int GP = 4 / NTS;    // groups sharing one accumulator
+    const int slot = t / NTS, tk = t % NTS;   // D columns 2t, 2t + 1: group slot, token in set
+    // acc[s][q][i]: row g + 8q, token s NTS + tk, sum r = slot + GP i (groups j, j mod 4 = r)
+    float acc[NS][4][NTS];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int s = 0; s < NS; ++s)
 #pragma unroll
-        for (int i = 0; i < NT; ++i) acc[q][i] = 0.0f;
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int i = 0; i < NTS; ++i) acc[s][q][i] = 0.0f;
     // hi + lo of a group carries the factor 2^p: undone before the scale, so
     // that no partial sum leaves the float range unless the result does; the
     // 2^p domain is kept only when it is not below the true one (p >= 0, the
     // token's |x| below 2^15), so that it adds no underflow either
-    const int p_t = pexp[tok];
-    const float pinv = exp2i_m(-p_t);
-    const bool plain = *not_plain == 0 && p_t >= 0;
-    // B: lanes 8 NT s .. 8 NT s + 8 NT - 1 hold the fragment of group slot s
-    const int b_slot = lane / (8 * NT);
-    const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * NT)) * 16;
+    float pinv[NS];
+    bool plain[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const int p_t = pexp[s * NTS + tk];
+        pinv[s] = exp2i_m(-p_t);
+        plain[s] = *not_plain == 0 && p_t >= 0;
+    }
+    // B: lanes 8 NTS s .. 8 NTS s + 8 NTS - 1 hold the fragment of group slot s;
+    // column set s of eight tokens is 512 bytes further
+    const int b_slot = lane / (8 * NTS);
+    const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * NTS)) * 16;
     const uint32_t zero_lane = smem_u32(fin) + 32;
     const uint32_t sel0 = 0x4044u + (static_cast<uint32_t>(slot) << 8);   // byte slot -> byte 2
-    // token n's four sums: P_r in lane (g, (r mod GP) NT + n), entry r / GP; lane
+    // token n's four sums: P_r in lane (g, (r mod GP) NTS + n), entry r / GP; lane
     // (g, n) adds them in order and stores them as this warp's piece of row unit ru
     auto flush = [&](int ru) {
         float* pw = part + static_cast<size_t>(rg + ru) * kRowsU * NT;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float p[4];
+        for (int s = 0; s < NS; ++s) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                p[r] = __shfl_sync(0xffffffffu, acc[q][r / GP], (lane & ~3) | ((r % GP) * NT + tok));
-            float v = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
-            // back from the 2^p domain (exact: a power of two, no overflow)
-            if (plain) v = __fmul_rn(v, pinv);
-            if (t < NT) pw[(g + 8 * q) * NT + t] = v;   // lane (g, t) has token t
+            for (int q = 0; q < 4; ++q) {
+                float p[4];
 #pragma unroll
-            for (int i = 0; i < NT; ++i) acc[q][i] = 0.0f;
+                for (int r = 0; r < 4; ++r)
+                    p[r] = __shfl_sync(0xffffffffu, acc[s][q][r / GP],
+                                       (lane & ~3) | ((r % GP) * NTS + tk));
+                float v = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
+                // back from the 2^p domain (exact: a power of two, no overflow)
+                if (plain[s]) v = __fmul_rn(v, pinv[s]);
+                if (t < NTS) pw[(g + 8 * q) * NT + s * NTS + t] = v;   // lane (g, t): token t of set s
+#pragma unroll
+                for (int i = 0; i < NTS; ++i) acc[s][q][i] = 0.0f;
+            }
         }
     };
     bool failed = false;
@@ -395,6 +484,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         if (++u_c == n_c) {
             u_c = 0;
             ++u_ru;
+        }
+        if (kRpw > 1) {
+            // the unit starts the warp's next range: the last range's piece is done
+            while (t_lo + k >= rg_end) {
+                if (cur_ru >= 0) flush(cur_ru);
+                cur_ru = -1;
+                ++rg;
+                rg_end = (rg + 1) * n_tasks / kRangesM;
+            }
         }
         if (ru != cur_ru) {
             if (cur_ru >= 0) flush(cur_ru);
@@ -418,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
         for (int j0 = 0; j0 < kChunkM; j0 += GP) {
             if (j0 < ngc) {
-                float d0[4], d1[4];   // rows g, g+8 and g+16, g+24
+                float d0[NS][4], d1[NS][4];   // per column set: rows g, g+8 and g+16, g+24
 #pragma unroll
                 for (int s = 0; s < GP; ++s) {
                     const int j = j0 + s;
@@ -432,18 +530,22 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                         e2m1x8_to_f16x2x4(cwd[1], h1);
                         e2m1x8_to_f16x2x4(cwd[2], h2);
                         e2m1x8_to_f16x2x4(cwd[3], h3);
-                        const uint4 b = lds128(
-                            b_slot == s ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * NT)
-                                        : zero_lane);
-                        if (s == 0) {
-                            mma16816_z(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                            mma16816_z(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
-                        } else {
-                            mma16816(d0, h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                            mma16816(d1, h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+#pragma unroll
+                        for (int c = 0; c < NS; ++c) {
+                            const uint4 b = lds128(
+                                b_slot == s ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * NT) +
+                                                  static_cast<uint32_t>(c) * 512u
+                                            : zero_lane);
+                            if (s == 0) {
+                                mma16816_z(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                                mma16816_z(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                            } else {
+                                mma16816(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                                mma16816(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                            }
+                            mma16816(d0[c], h0[2], h1[2], h0[3], h1[3], b.z, b.w);
+                            mma16816(d1[c], h2[2], h3[2], h2[3], h3[3], b.z, b.w);
                         }
-                        mma16816(d0, h0[2], h1[2], h0[3], h1[3], b.z, b.w);
-                        mma16816(d1, h2[2], h3[2], h2[3], h3[3], b.z, b.w);
                     }
                 }
                 // this lane's group: j0 + slot (its scale byte: byte (j0 & 3) + slot of
@@ -452,18 +554,22 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                     const uint32_t sel = sel0 + (static_cast<uint32_t>(j0 & 3) << 8);
                     const uint32_t w0 = j0 < 4 ? sb[0].x : sb[0].y, w1 = j0 < 4 ? sb[1].x : sb[1].y;
                     const uint32_t w2 = j0 < 4 ? sb[2].x : sb[2].y, w3 = j0 < 4 ? sb[3].x : sb[3].y;
-                    const float v[4] = {__fadd_rn(d0[0], d0[1]), __fadd_rn(d0[2], d0[3]),
-                                        __fadd_rn(d1[0], d1[1]), __fadd_rn(d1[2], d1[3])};
                     const uint32_t kw[4] = {__byte_perm(w0, 0u, sel), __byte_perm(w1, 0u, sel),
                                             __byte_perm(w2, 0u, sel), __byte_perm(w3, 0u, sel)};
-                    const int i_acc = (j0 / GP) % NT;   // r = (j0 + slot) mod 4 = slot + GP i
+                    const int i_acc = (j0 / GP) % NTS;   // r = (j0 + slot) mod 4 = slot + GP i
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (plain)   // the sums stay in the 2^p domain; 2^(k-127) from its bits
-                            acc[q][i_acc] = __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[q][i_acc]);
-                        else         // any byte: the table, and 2^-p applied first
-                            acc[q][i_acc] =
-                                __fmaf_rn(lut[kw[q] >> 16], __fmul_rn(v[q], pinv), acc[q][i_acc]);
+                    for (int c = 0; c < NS; ++c) {
+                        const float v[4] = {__fadd_rn(d0[c][0], d0[c][1]), __fadd_rn(d0[c][2], d0[c][3]),
+                                            __fadd_rn(d1[c][0], d1[c][1]), __fadd_rn(d1[c][2], d1[c][3])};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (plain[c])   // the sums stay in the 2^p domain; 2^(k-127) from its bits
+                                acc[c][q][i_acc] =
+                                    __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[c][q][i_acc]);
+                            else            // any byte: the table, and 2^-p applied first
+                                acc[c][q][i_acc] = __fmaf_rn(lut[kw[q] >> 16],
+                                                             __fmul_rn(v[q], pinv[c]), acc[c][q][i_acc]);
+                        }
                     }
                 }
             }
@@ -494,14 +600,14 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // --- add each row unit's pieces in chunk order: the ranges from the one
     // holding the unit's first task to the one holding its last (the range of
     // task T is (16 T + 15) / n_tasks), empty ones skipped
-    for (int i = tid; i < n_ru * kRowsU * NT; i += kThreadsM) {
+    for (int i = tid; i < n_ru * kRowsU * NT; i += kThr) {
         const int ru = i / (kRowsU * NT), rem = i - ru * kRowsU * NT;
-        const int r_a = (kWarpsM * ru * n_c + kWarpsM - 1) / n_tasks;
-        const int r_b = (kWarpsM * ((ru + 1) * n_c - 1) + kWarpsM - 1) / n_tasks;
+        const int r_a = (kRangesM * ru * n_c + kRangesM - 1) / n_tasks;
+        const int r_b = (kRangesM * ((ru + 1) * n_c - 1) + kRangesM - 1) / n_tasks;
         float s = 0.0f;
         bool first = true;
         for (int r = r_a; r <= r_b; ++r) {
-            if (r * n_tasks / kWarpsM < (r + 1) * n_tasks / kWarpsM) {
+            if (r * n_tasks / kRangesM < (r + 1) * n_tasks / kRangesM) {
                 const float v = part[static_cast<size_t>(r + ru) * kRowsU * NT + rem];
                 s = first ? v : __fadd_rn(s, v);
                 first = false;
@@ -521,7 +627,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         const int nr = n_ru * kRowsU;
         const int r_lo = static_cast<int>(rank) * nr / CL;
         const int r_hi = static_cast<int>(rank + 1) * nr / CL;
-        for (int i = r_lo * NT + tid; i < r_hi * NT; i += kThreadsM) {
+        for (int i = r_lo * NT + tid; i < r_hi * NT; i += kThr) {
             float s = ld_cluster_m(fin + i, 0);
             for (uint32_t q = 1; q < static_cast<uint32_t>(CL); ++q)
                 s = __fadd_rn(s, ld_cluster_m(fin + i, q));
@@ -615,7 +721,7 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     // weight bytes in flight; the arithmetic does not depend on the depth)
     const uint32_t fixed = mv_layout(NT, ng_max, ru_cta, 0).total;
     int stages = fixed < kSmemMaxM
-                     ? static_cast<int>((kSmemMaxM - fixed) / (kWarpsM * kStageM)) : 0;
+                     ? static_cast<int>((kSmemMaxM - fixed) / (warps_mv(NT) * kStageM)) : 0;
     stages = stages > kMaxStagesM ? kMaxStagesM : stages;
     if (stages < kMinStagesM) return cudaErrorNotSupported;
     const MvLayout l = mv_layout(NT, ng_max, ru_cta, stages);
@@ -633,7 +739,7 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ranges * CL),
                        static_cast<unsigned>((nb + NT - 1) / NT));
-    cfg.blockDim = dim3(kThreadsM);
+    cfg.blockDim = dim3(static_cast<unsigned>(warps_mv(NT) * 32));
     cfg.dynamicSmemBytes = l.total;
     cfg.stream = s;
     const int overlap = launch_overlap() ? 1 : 0;
@@ -679,6 +785,12 @@ cudaError_t launch_mv_tc(const uint8_t* w, int rows, int cols, const float* X, i
                          cudaStream_t s) {
     if (nb <= 1) return launch_mv_nt<1>(w, rows, cols, X, nb, Y, s);
     if (nb == 2) return launch_mv_nt<2>(w, rows, cols, X, nb, Y, s);
+    if (nb <= 4) return launch_mv_nt<4>(w, rows, cols, X, nb, Y, s);
+    // one decode per group for up to eight tokens; passes of four where the
+    // eight tokens' fragments do not fit in shared memory
+    const cudaError_t e = launch_mv_nt<8>(w, rows, cols, X, nb, Y, s);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
     return launch_mv_nt<4>(w, rows, cols, X, nb, Y, s);
 }
 

@@ -152,6 +152,23 @@ def test_mm8_config_every_output(mx):
     ref, l1 = oracle.matmat(w_h, cfg.rows, cfg.cols, X, cfg.nb)
     worst = assert_within(Y, ref, l1, REL_FP32, "mm nb=8")
     print(f"mm nb=8 worst err/tol {worst:.3g}")
+    # one pass decodes each group once for all eight tokens; per token the
+    # result is still the matvec's, bit for bit
+    for t in range(cfg.nb):
+        assert_bits_equal(Y[t], run_mv(mx, w_h, cfg.rows, cfg.cols, X[t]), f"mm8 token {t}")
+
+
+@pytest.mark.parametrize("nb", [5, 6, 7, 8, 16, 21])
+def test_eight_token_passes_equal_the_matvec(mx, nb):
+    # five to eight tokens share one pass; more tokens take passes of eight
+    rows, cols = 160, 4096
+    w_h = synth.mxfp4_matrix(rows, cols, 800 + nb, 118, 130)
+    X = synth.normal_f32(810 + nb, nb * cols).reshape(nb, cols)
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    assert_within(Y, ref, l1, REL_FP32, f"nb={nb}")
+    for t in range(nb):
+        assert_bits_equal(Y[t], run_mv(mx, w_h, rows, cols, X[t]), f"nb={nb} token {t}")
 
 
 @pytest.mark.parametrize("nb", [1, 3, 5, 8, 13])
@@ -262,7 +279,7 @@ def test_host_buffer_entry_matches_device_entry(mx):
     assert_bits_equal(Y_host.numpy(), host(y_dev_ref), "host entry")
 
 
-@pytest.mark.parametrize("nb", [1, 3])
+@pytest.mark.parametrize("nb", [1, 3, 8])
 def test_launch_overlap_chain_is_bit_identical(mx, nb):
     # four layers, each reading the previous one's output: with programmatic
     # dependent launch a kernel starts early but must read its x only after the
