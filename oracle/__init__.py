@@ -65,6 +65,8 @@ _SIG = {
     "mxo_moe_down": (None, [_P, _SZ, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P]),
     "mxo_moe_forward": (None, [_P, _P, _P, _SZ, _SZ, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
     "mxo_moe_plan": (_I, [_P, _I, _I, _P, _P]),
+    "mxo_moe_forward_ex": (None, [_P, _P, _P, _SZ, _SZ, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P,
+                                  _I, ctypes.c_float, _P, _P, _P, _P]),
 }
 
 
@@ -224,3 +226,26 @@ def moe_plan(ids, n_experts: int):
     pair_of = np.full(ids.size, -1, dtype=np.int32)
     bad = lib().mxo_moe_plan(_ptr(ids), ids.size, n_experts, _ptr(offsets), _ptr(pair_of))
     return offsets, pair_of, int(bad)
+
+
+def moe_forward_ex(gate_bank, up_bank, down_bank, gu_stride, down_stride, n_slots, hidden,
+                   inter, x, n_tokens, top_k, ids, route_w, slot_of=None, n_experts=None,
+                   bf16_mode=False, limit=0.0):
+    """The global-bank form of the layer (bf16 boundaries, SwiGLU limit, route
+    weight folded into the act, expert -> slot table with cold experts).
+    dict: out, bound [n_tokens, hidden] float64; cold (int32 pair indices)."""
+    gate_bank, up_bank, down_bank = _u8(gate_bank), _u8(up_bank), _u8(down_bank)
+    x, ids, route_w = _f32(x), _i32(ids), _f32(route_w)
+    n_experts = n_slots if n_experts is None else n_experts
+    so = None if slot_of is None else _i32(slot_of)
+    res = {k: np.empty((n_tokens, hidden)) for k in ("out", "bound")}
+    cold = np.empty(max(ids.size, 1), dtype=np.int32)
+    n_cold = ctypes.c_int(0)
+    lib().mxo_moe_forward_ex(_ptr(gate_bank), _ptr(up_bank), _ptr(down_bank), gu_stride,
+                             down_stride, n_slots, hidden, inter, _ptr(x), n_tokens, top_k,
+                             _ptr(ids), None if so is None else _ptr(so), n_experts,
+                             _ptr(route_w), int(bool(bf16_mode)), float(limit),
+                             _ptr(res["out"]), _ptr(res["bound"]), _ptr(cold),
+                             ctypes.addressof(n_cold))
+    res["cold"] = cold[:n_cold.value].copy()
+    return res

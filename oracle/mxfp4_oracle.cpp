@@ -286,6 +286,137 @@ void mxo_moe_forward(const uint8_t* gate_bank, const uint8_t* up_bank,
     }
 }
 
+namespace {
+
+// bf16 spacing at |v|: 2^(e - 7) with e the binade of |v| (normal range floor).
+double bf16_spacing(double v) {
+    const double a = std::fabs(v);
+    int e = -126;
+    if (a > 0.0 && std::isfinite(a)) e = std::ilogb(a) < -126 ? -126 : std::ilogb(a);
+    return std::ldexp(1.0, e - 7);
+}
+
+// GLOBAL fn mxg_bf16 applied to the float value of v.
+double bf16_of(double v) { return static_cast<double>(mxo_bf16_rne(static_cast<float>(v))); }
+
+// The largest |silu'| on [z - r, z + r] (a Lipschitz constant of SiLU there):
+// |silu'| is monotone between its extremes near -2.3994 (0.0998) and 2.3994
+// (1.0998), so the endpoints and any extreme inside the interval decide it.
+double silu_lipschitz(double z, double r) {
+    const double lo = z - r, hi = z + r;
+    double m = std::fmax(std::fabs(mxo_silu_grad(lo)), std::fabs(mxo_silu_grad(hi)));
+    if (lo <= 2.4 && hi >= 2.39) m = std::fmax(m, 1.1);
+    if (lo <= -2.39 && hi >= -2.4) m = std::fmax(m, 0.1);
+    return m * 1.01;
+}
+
+}  // namespace
+
+// The global-bank kernels with their flags: the gate/up tail (bf16 rounding of
+// gate and up, the SwiGLU limit, the route weight folded into a bf16 act) and
+// the down kernel (pre-weighted acts summed over the slots, the sum rounded to
+// bf16), on a bank addressed through an expert -> slot table.
+void mxo_moe_forward_ex(const uint8_t* gate_bank, const uint8_t* up_bank,
+                        const uint8_t* down_bank, size_t gu_stride_bytes,
+                        size_t down_stride_bytes, int n_slots, int hidden, int inter,
+                        const float* x, int n_tokens, int top_k, const int32_t* ids,
+                        const int32_t* slot_of, int n_experts, const float* route_w,
+                        int bf16_mode, float limit, double* out, double* bound,
+                        int32_t* cold_pairs, int* n_cold) {
+    const double eps = 1e-5;
+    const int n_pairs = n_tokens * top_k;
+    std::vector<int> slot(static_cast<size_t>(n_pairs), -1);
+    int cold = 0;
+    for (int p = 0; p < n_pairs; ++p) {
+        const int32_t e = ids[p];
+        if (e < 0 || e >= n_experts) continue;            // invalid id
+        const int32_t s = slot_of ? slot_of[e] : e;
+        if (s < 0) {                                      // cold: not in the bank
+            cold_pairs[cold++] = p;
+            continue;
+        }
+        if (s < n_slots) slot[p] = s;                     // else invalid slot
+    }
+    *n_cold = cold;
+    std::vector<double> a(static_cast<size_t>(inter)), ea(static_cast<size_t>(inter));
+    std::vector<double> o(static_cast<size_t>(hidden)), eo(static_cast<size_t>(hidden));
+    for (int t = 0; t < n_tokens; ++t) {
+        const float* xt = x + static_cast<size_t>(t) * hidden;
+        std::vector<double> acc(static_cast<size_t>(hidden), 0.0), eacc(acc), mag(acc);
+        for (int j = 0; j < top_k; ++j) {
+            const int p = t * top_k + j;
+            if (slot[p] < 0) continue;
+            const uint8_t* ge = gate_bank + static_cast<size_t>(slot[p]) * gu_stride_bytes;
+            const uint8_t* ue = up_bank + static_cast<size_t>(slot[p]) * gu_stride_bytes;
+            const uint8_t* de = down_bank + static_cast<size_t>(slot[p]) * down_stride_bytes;
+            const double w = static_cast<double>(route_w[p]);
+            const double wpre = bf16_mode ? std::fabs(w) : 1.0;
+            for (int c = 0; c < inter; ++c) {
+                double g, u, l1g, l1u;
+                row_dot(ge, inter, hidden, c, xt, &g, &l1g);
+                row_dot(ue, inter, hidden, c, xt, &u, &l1u);
+                double eg = eps * l1g, eu = eps * l1u;
+                if (bf16_mode) {   // a value eg off may round to a neighbour of bf16(g)
+                    eg += bf16_spacing(std::fabs(g) + eg);
+                    eu += bf16_spacing(std::fabs(u) + eu);
+                    g = bf16_of(g);
+                    u = bf16_of(u);
+                }
+                if (limit > 0.0f) {   // a value clamped with room to spare has no error left
+                    const double lim = static_cast<double>(limit);
+                    if (std::fabs(u) - lim > eu) eu = 0.0;
+                    if (g - lim > eg) eg = 0.0;
+                    u = u < -lim ? -lim : (u > lim ? lim : u);
+                    g = g < lim ? g : lim;
+                }
+                const double sg = mxo_silu(g);
+                double av = sg * u;
+                const double lg = silu_lipschitz(g, eg);
+                // (+ a few float roundings of the SiLU and the products)
+                double e = wpre * ((std::fabs(sg) + lg * eg) * eu + lg * std::fabs(u) * eg +
+                                   std::ldexp(std::fabs(av), -21));
+                if (bf16_mode) {
+                    av = w * av;
+                    e += bf16_spacing(std::fabs(av) + e);
+                    av = bf16_of(av);
+                }
+                a[static_cast<size_t>(c)] = av;
+                ea[static_cast<size_t>(c)] = e;
+            }
+            for (int r = 0; r < hidden; ++r) {
+                double sum = 0.0, l1 = 0.0, prop = 0.0;
+                for (int c = 0; c < inter; ++c) {
+                    const double dw = static_cast<double>(mxo_weight_at(de, hidden, inter, r, c));
+                    sum += dw * a[static_cast<size_t>(c)];
+                    l1 += std::fabs(dw * a[static_cast<size_t>(c)]);
+                    prop += std::fabs(dw) * ea[static_cast<size_t>(c)];
+                }
+                const double eo_r = prop + eps * l1;
+                if (bf16_mode) {
+                    acc[static_cast<size_t>(r)] += sum;
+                    eacc[static_cast<size_t>(r)] += eo_r;
+                    mag[static_cast<size_t>(r)] += std::fabs(sum);
+                } else {
+                    acc[static_cast<size_t>(r)] += w * sum;
+                    eacc[static_cast<size_t>(r)] += std::fabs(w) * eo_r;
+                    mag[static_cast<size_t>(r)] += std::fabs(w * sum);
+                }
+            }
+        }
+        for (int r = 0; r < hidden; ++r) {
+            const size_t i = static_cast<size_t>(t) * hidden + r;
+            double y = acc[static_cast<size_t>(r)];
+            double b = eacc[static_cast<size_t>(r)] + eps * mag[static_cast<size_t>(r)];
+            if (bf16_mode) {
+                b += bf16_spacing(std::fabs(y) + b);
+                y = bf16_of(y);
+            }
+            out[i] = y;
+            bound[i] = b;
+        }
+    }
+}
+
 // grouped_moe_sort_plan: count pairs per expert, prefix-sum the counts into
 // offsets, then place each pair at its expert's next free slot (stable).
 int mxo_moe_plan(const int32_t* ids, int n_pairs, int n_experts, int32_t* offsets,

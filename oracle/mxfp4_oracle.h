@@ -122,6 +122,44 @@ void mxo_moe_forward(const uint8_t* gate_bank, const uint8_t* up_bank,
                      const int32_t* ids, const float* route_w, double* out,
                      double* bound_l1, double* bound_prop);
 
+/* The layer in the general form of the page's global-bank kernels
+ * (GLOBAL dsv4_global_gate_up_mxfp4 / dsv4_global_down_mxfp4 with their
+ * flags; the expert slots and cold experts of its global-bank MoE test).
+ *
+ * Expert ids map to bank slots: slot = slot_of[e] when slot_of is given (a
+ * negative entry marks a cold expert, one not resident in the bank; the page
+ * writes u32::MAX), else slot = e.  A pair whose id is outside [0, n_experts)
+ * or whose slot is outside [0, n_slots) is invalid; invalid and cold pairs
+ * contribute nothing; the cold ones are listed, in increasing pair order, in
+ * cold_pairs (n_cold of them).  Banks hold n_slots experts at the strides.
+ *
+ * Per valid pair p = t*top_k + j with slot s and route weight w:
+ *   g = gate_s . x_t, u = up_s . x_t                   (double)
+ *   bf16 mode: g = bf16(g), u = bf16(u)                 (mxg_bf16 of the float)
+ *   limit > 0: u = clamp(u, -limit, limit), g = min(g, limit)
+ *   a = silu(g) * u; bf16 mode: a = bf16(w * a)         (route weight folded in)
+ *   o_p = down_s . a                                    (double)
+ *   out[t] = sum_j w_j o_p (generic) or bf16(sum_j o_p) (bf16 mode), slots in order.
+ * bound[t*hidden + r]: what an implementation may differ by when each FP32 dot
+ * product carries up to eps = 1e-5 of its L1 norm, each bf16 rounding may land
+ * one bf16 spacing away (the rounded values' neighbours), the limit clamps are
+ * 1-Lipschitz (and remove the error of a value clamped with more than its error
+ * to spare) and L = the largest |silu'| on [g - Eg, g + Eg]:
+ *   Eg = eps L1g (+ sp(|g| + eps L1g)), Eu likewise
+ *   Ea = |w'| ((|silu(g)| + L Eg) Eu + L |u| Eg + 2^-21 |silu(g) u|)
+ *        (+ sp(|w silu(g) u| + that)), w' = w in bf16 mode, else 1
+ *   Eo = sum_c |down| Ea_c + eps sum_c |down a|
+ *   generic: bound = sum_j |w_j| Eo_j + eps sum_j |w_j o_j|
+ *   bf16:    bound = sum_j Eo_j + eps sum_j |o_j| + sp(|out| + that)
+ * where sp(v) is the bf16 spacing at |v| (2^(floor(log2|v|) - 7)). */
+void mxo_moe_forward_ex(const uint8_t* gate_bank, const uint8_t* up_bank,
+                        const uint8_t* down_bank, size_t gu_stride_bytes,
+                        size_t down_stride_bytes, int n_slots, int hidden, int inter,
+                        const float* x, int n_tokens, int top_k, const int32_t* ids,
+                        const int32_t* slot_of, int n_experts, const float* route_w,
+                        int bf16_mode, float limit, double* out, double* bound,
+                        int32_t* cold_pairs, int* n_cold);
+
 /* Routing plan by counting sort (rlx-cpu gguf_matmul.rs grouped_moe_sort_plan):
  * offsets[e] .. offsets[e+1] index the pairs of expert e in pair_of[], in
  * increasing pair order.  Returns the number of pairs with an invalid id (they

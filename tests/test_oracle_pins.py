@@ -456,3 +456,136 @@ def test_moe_invalid_pair_contributes_nothing(orc):
     np.testing.assert_allclose(res["out"][1], want, rtol=1e-12, atol=1e-12)
     offsets, pair_of, bad = orc.moe_plan(ids.reshape(-1), m["E"])
     assert bad == 1 and p_bad not in pair_of[:offsets[-1]]
+
+
+# --- the global-bank form: bf16 boundaries, SwiGLU limit, pre-weighting, slots ----
+
+def _bf16(a):
+    """Round-to-nearest-even bfloat16 of the float32 value (torch's conversion)."""
+    torch = pytest.importorskip("torch")
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float32).numpy().astype(np.float64)
+
+
+def _dense_layer_ex(m, x, ids, wts, bf16_mode, limit, slot_of=None, dtype=np.float64):
+    """The global-bank layer from the dense matrices, in numpy (float64 or
+    float32 arithmetic), bf16 rounding by torch; slot_of maps ids to bank slots."""
+    out = np.zeros((m["T"], m["hidden"]), dtype=np.float64)
+    for t in range(m["T"]):
+        xt = x[t].astype(dtype)
+        acc = np.zeros(m["hidden"], dtype=dtype)
+        for j in range(m["K"]):
+            e = int(ids[t, j])
+            if e < 0 or e >= m["E"]:
+                continue
+            s = e if slot_of is None else int(slot_of[e])
+            if s < 0:
+                continue
+            G, U, D = (m["mats"][k][s].astype(dtype) for k in ("gate", "up", "down"))
+            g, u = G @ xt, U @ xt
+            if bf16_mode:
+                g, u = _bf16(g).astype(dtype), _bf16(u).astype(dtype)
+            if limit > 0:
+                u = np.clip(u, -limit, limit)
+                g = np.minimum(g, dtype(limit))
+            with np.errstate(over="ignore"):
+                a = g / (dtype(1.0) + np.exp(-g)) * u
+            w = dtype(wts[t, j])
+            if bf16_mode:
+                a = _bf16(w * a).astype(dtype)
+                acc = acc + D @ a
+            else:
+                acc = acc + w * (D @ a)
+        out[t] = _bf16(acc) if bf16_mode else acc
+    return out
+
+
+def _fwd_ex(orc, m, ids, wts, **kw):
+    return orc.moe_forward_ex(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
+                              m["stride_gu"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                              m["x"], m["T"], m["K"], ids, wts, **kw)
+
+
+def test_moe_forward_ex_generic_mode_is_the_f32_layer(orc):
+    m = _tiny_moe(seed=7)
+    ex = _fwd_ex(orc, m, m["ids"], m["wts"])
+    fw = orc.moe_forward(m["banks"]["gate"], m["banks"]["up"], m["banks"]["down"],
+                         m["stride_gu"], m["stride_dn"], m["E"], m["hidden"], m["inter"],
+                         m["x"], m["T"], m["K"], m["ids"], m["wts"])
+    assert np.array_equal(ex["out"], fw["out"]) and ex["cold"].size == 0
+
+
+@pytest.mark.parametrize("limit", [0.0, 0.75])
+def test_moe_forward_ex_bf16_mode_against_dense_numpy(orc, limit):
+    m = _tiny_moe(seed=8, E=6, hidden=96, inter=64, T=4, K=3)
+    ex = _fwd_ex(orc, m, m["ids"], m["wts"], bf16_mode=True, limit=limit)
+    want = _dense_layer_ex(m, m["x"], m["ids"], m["wts"], True, limit)
+    # the two sum in different orders before the bf16 roundings: equal but for
+    # rare values on a rounding boundary, which land one bf16 step apart
+    same = ex["out"] == want
+    assert same.mean() > 0.97, same.mean()
+    step = np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(want), 1e-30))).astype(int) - 7)
+    assert (np.abs(ex["out"] - want) <= 2 * step).all()
+    # every output is a bfloat16 value
+    assert np.array_equal(_bf16(ex["out"]), ex["out"])
+    if limit > 0:   # the limit changes the result (it is active on this input)
+        free = _dense_layer_ex(m, m["x"], m["ids"], m["wts"], True, 0.0)
+        assert not np.array_equal(free, want)
+
+
+def test_moe_forward_ex_slot_table_and_cold_experts(orc):
+    m = _tiny_moe(seed=9, E=6, hidden=64, inter=64, T=5, K=2)
+    # the same experts in a permuted bank, addressed through slot_of
+    perm = np.array([3, 0, 5, 1, 4, 2], dtype=np.int32)        # expert e lives in slot perm[e]
+    inv = np.argsort(perm)
+    banks = {}
+    for role, stride in (("gate", m["stride_gu"]), ("up", m["stride_gu"]),
+                         ("down", m["stride_dn"])):
+        b = m["banks"][role].reshape(m["E"], stride)
+        banks[role] = np.ascontiguousarray(b[inv]).reshape(-1)
+    ids = m["ids"].copy()
+    ids[1, 0] = 4
+    ids[3, 1] = 4
+    base = _fwd_ex(orc, m, ids, m["wts"], bf16_mode=True, limit=0.5)
+    mp = dict(m, banks=banks)
+    moved = _fwd_ex(orc, mp, ids, m["wts"], slot_of=perm, bf16_mode=True, limit=0.5)
+    assert np.array_equal(moved["out"], base["out"])
+    # expert 4 cold: its pairs are listed (increasing pair order) and left out
+    cold_tab = perm.copy()
+    cold_tab[4] = -1
+    cold = _fwd_ex(orc, mp, ids, m["wts"], slot_of=cold_tab, bf16_mode=True, limit=0.5)
+    want_pairs = np.flatnonzero(ids.reshape(-1) == 4)
+    assert np.array_equal(cold["cold"], want_pairs)
+    ids_wo = ids.copy()
+    ids_wo[ids_wo == 4] = -1
+    assert np.array_equal(cold["out"], _fwd_ex(orc, m, ids_wo, m["wts"], bf16_mode=True,
+                                               limit=0.5)["out"])
+    # a slot outside the bank is invalid: not listed as cold, contributes nothing
+    bad_tab = perm.copy()
+    bad_tab[4] = m["E"]
+    bad = _fwd_ex(orc, mp, ids, m["wts"], slot_of=bad_tab, bf16_mode=True, limit=0.5)
+    assert bad["cold"].size == 0 and np.array_equal(bad["out"], cold["out"])
+
+
+@pytest.mark.parametrize("bf16_mode,limit", [(False, 0.0), (True, 0.0), (True, 0.75),
+                                             (False, 0.75)])
+def test_moe_forward_ex_bound_holds_for_a_float32_layer(orc, bf16_mode, limit):
+    # an implementation whose dot products are float32 (numpy, another order
+    # than the oracle's) stays inside the bound, and the bound is tight enough
+    # to mean something
+    m = _tiny_moe(seed=10, E=6, hidden=96, inter=64, T=4, K=3)
+    ex = _fwd_ex(orc, m, m["ids"], m["wts"], bf16_mode=bf16_mode, limit=limit)
+    f32 = _dense_layer_ex(m, m["x"], m["ids"], m["wts"], bf16_mode, limit, dtype=np.float32)
+    assert (np.abs(f32 - ex["out"]) <= ex["bound"]).all()
+    # of the order of the errors it stands for: eps = 1e-5 of the L1 norms in the
+    # generic mode (the cancellation of the sums makes L1 / |out| ~ 10-50 here);
+    # in the bf16 mode a step of 2^-8..2^-7 at each of the act's elements
+    rel = np.median(ex["bound"] / np.maximum(np.abs(ex["out"]), 1e-30))
+    assert rel < (2.0 ** -3 if bf16_mode else 1e-3), rel
+    # and tight enough to catch a mistake: the route weights dropped, or (with a
+    # limit) the clamp of up left out
+    wrong = _dense_layer_ex(m, m["x"], m["ids"], np.ones_like(m["wts"]), bf16_mode, limit)
+    assert (np.abs(wrong - ex["out"]) > ex["bound"]).any()
+    if limit > 0:
+        m_wide = _dense_layer_ex(m, m["x"], m["ids"], m["wts"], bf16_mode, 1e30)
+        assert (np.abs(m_wide - ex["out"]) > ex["bound"]).any()
