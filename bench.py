@@ -280,6 +280,24 @@ class PrefillNoWorkspace(Prefill):
         self.mx.mxfp4_mm(self.w, c.rows, c.cols, self.X, c.nb, self.Y)
 
 
+class Dequant(Workload):
+    """Standalone decode of the decode-GEMV matrix to float (mxfp4_dequant)."""
+
+    def __init__(self, mx):
+        import torch
+        import synth
+        c = synth.DECODE
+        self.mx, self.c = mx, c
+        self.name = "mxfp4_dequant 14336x4096"
+        self.w = _dev(c.weights())
+        self.out = torch.empty(c.rows * c.cols, dtype=torch.float32, device="cuda")
+        self.bytes_per_step = mx.mxfp4_nbytes(c.rows, c.cols) + 4 * c.rows * c.cols
+        self.dominant = "k_dequant"
+
+    def step(self):
+        self.mx.mxfp4_dequant(self.w, self.c.rows, self.c.cols, self.out)
+
+
 class Tiny(DecodeGemv):
     def __init__(self, mx):
         import synth
@@ -506,7 +524,8 @@ def run_profile(args):
     mx.lib()
     mx.mxfp4_set_launch_overlap(True)   # as in the timed bench
     cls = {"decode": DecodeGemv, "decode_fp32": DecodeGemvFp32, "mm8": SmallBatch,
-           "moe": MoeLayer, "prefill": Prefill, "prefill_mm": PrefillNoWorkspace}
+           "moe": MoeLayer, "prefill": Prefill, "prefill_mm": PrefillNoWorkspace,
+           "dequant": Dequant}
     w = cls[args.profile](mx)
     for _ in range(args.warmup):
         w.step()
@@ -528,7 +547,8 @@ def main():
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile",
-                    choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm"],
+                    choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm",
+                             "dequant"],
                     help="run only this workload's warm-up and timed steps (eagerly, one "
                          "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()

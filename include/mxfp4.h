@@ -210,6 +210,55 @@ int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter,
                    cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The general form of the two passes: the flags of the page's global-bank
+ * kernels (GLOBAL dsv4_global_gate_up_mxfp4 / dsv4_global_down_mxfp4) and the
+ * expert slots of its global-bank MoE (the expert -> slot remap, with cold
+ * experts left out of the bank).
+ *
+ * Banks hold n_slots experts (slot s at s * mxfp4_nbytes(...) as above).  Expert
+ * ids lie in [0, n_experts); slot_of[id] (device, int32[n_experts], nullable:
+ * then slot = id and n_experts must equal n_slots) gives the id's bank slot,
+ * a negative entry marking a COLD expert (not resident; the page's u32::MAX
+ * remap).  Pairs routed to a cold expert are skipped by both passes and
+ * listed in the workspace (mxfp4_moe_cold_pairs) so that the caller can run
+ * them elsewhere; pairs with an id outside [0, n_experts) or a slot at or past
+ * n_slots are skipped and counted (mxfp4_moe_plan_errors).  The workspace size
+ * is mxfp4_moe_workspace_bytes(n_slots, n_tokens, top_k, hidden, inter).
+ *
+ * mode MXFP4_MOE_MODE_F32: act = silu(g) * u and y[t] = sum_j w_tj o_tj in
+ *   FP32, as mxfp4_moe_gate_up / mxfp4_moe_down.
+ * mode MXFP4_MOE_MODE_V41 (the DeepSeek-V4.1 path: the kernels' flag _p0):
+ *   g and u are rounded to bfloat16 (round to nearest even, GLOBAL fn
+ *   mxg_bf16), act = bf16(w_tj * silu(g) * u) -- the route weight folded into
+ *   the act -- and y[t] = bf16(sum_j o_tj) with o = down . act.
+ * swiglu_limit > 0 (either mode): u is clamped to [-limit, limit] and g to at
+ *   most limit before SiLU; 0 turns the clamp off; NaN is refused.
+ * A shared expert is one more slot of every token: give it a bank slot, an id
+ * and route weight 1 (the page's frame routes its shared slot so).
+ * Error bound: see the oracle's mxo_moe_forward_ex (FP32 dot products within
+ * 1e-5 of their L1 norms, each bf16 rounding at most one bf16 step away). */
+#define MXFP4_MOE_MODE_F32 0
+#define MXFP4_MOE_MODE_V41 1
+int mxfp4_moe_gate_up_ex(const void* gate_bank, const void* up_bank, int n_slots, int hidden,
+                         int inter, const float* x, int n_tokens, int top_k,
+                         const int32_t* expert_ids, const int32_t* slot_of, int n_experts,
+                         const float* route_w, int mode, float swiglu_limit, float* act,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Down pass + combine for mxfp4_moe_gate_up_ex's plan (same workspace, same
+ * routing): route_w is read in MXFP4_MOE_MODE_F32 only (may be NULL in V41). */
+int mxfp4_moe_down_ex(const void* down_bank, int n_slots, int hidden, int inter, const float* act,
+                      int n_tokens, int top_k, const float* route_w, int mode, float* y,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The plan's cold pairs (p = t*top_k + j, increasing): their count in *n_cold
+ * and the first min(count, capacity) indices copied to pairs_host (host).
+ * Synchronises the stream. */
+int mxfp4_moe_cold_pairs(const void* workspace, size_t ws_bytes, int n_slots, int n_tokens,
+                         int top_k, int* n_cold, int32_t* pairs_host, int capacity,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * The routed-expert layer without a workspace.  The source pages have no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory when they run the layer -- for example a serving process whose

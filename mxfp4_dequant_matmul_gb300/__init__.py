@@ -17,12 +17,16 @@ __all__ = [
     "mxfp4_mm", "mxfp4_mm_fp32", "mxfp4_mm_bf16", "mxfp4_mm_bf16_workspace_bytes",
     "mxfp4_mm_bf16_ws", "mxfp4_matmat_host",
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
-    "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
+    "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_moe_gate_up_ex",
+    "mxfp4_moe_down_ex", "mxfp4_moe_cold_pairs", "MOE_MODE_F32", "MOE_MODE_V41",
+    "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libmxfp4.so")
 MM_SMALL_MAX = 64
+MOE_MODE_F32 = 0
+MOE_MODE_V41 = 1
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -47,6 +51,10 @@ _SIG = {
     "mxfp4_moe_down": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "mxfp4_moe_plan_errors": (_I, [_P, _SZ, ctypes.POINTER(_I), _P]),
     "mxfp4_moe_layer_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P]),
+    "mxfp4_moe_gate_up_ex": (_I, [_P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _I,
+                                  ctypes.c_float, _P, _P, _SZ, _P]),
+    "mxfp4_moe_down_ex": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
+    "mxfp4_moe_cold_pairs": (_I, [_P, _SZ, _I, _I, _I, ctypes.POINTER(_I), _P, _I, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIG)
 _lib = None
@@ -214,3 +222,39 @@ def mxfp4_moe_layer_noalloc(gate_bank, up_bank, down_bank, n_experts, hidden, in
     _check("mxfp4_moe_layer_noalloc", lib().mxfp4_moe_layer_noalloc(
         _addr(gate_bank), _addr(up_bank), _addr(down_bank), n_experts, hidden, inter, _addr(x),
         n_tokens, top_k, _addr(expert_ids), _addr(route_w), _addr(y), _stream(stream)))
+
+
+def mxfp4_moe_gate_up_ex(gate_bank, up_bank, n_slots, hidden, inter, x, n_tokens, top_k,
+                         expert_ids, act, workspace, slot_of=None, n_experts=None, route_w=None,
+                         mode=MOE_MODE_F32, swiglu_limit=0.0, ws_bytes=None, stream=None):
+    """Gate/up pass with the global-bank options (see include/mxfp4.h)."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    n_experts = n_slots if n_experts is None else n_experts
+    _check("mxfp4_moe_gate_up_ex", lib().mxfp4_moe_gate_up_ex(
+        _addr(gate_bank), _addr(up_bank), n_slots, hidden, inter, _addr(x), n_tokens, top_k,
+        _addr(expert_ids), _addr(slot_of), n_experts, _addr(route_w), int(mode),
+        float(swiglu_limit), _addr(act), _addr(workspace), ws_bytes, _stream(stream)))
+
+
+def mxfp4_moe_down_ex(down_bank, n_slots, hidden, inter, act, n_tokens, top_k, y, workspace,
+                      route_w=None, mode=MOE_MODE_F32, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mxfp4_moe_down_ex", lib().mxfp4_moe_down_ex(
+        _addr(down_bank), n_slots, hidden, inter, _addr(act), n_tokens, top_k, _addr(route_w),
+        int(mode), _addr(y), _addr(workspace), ws_bytes, _stream(stream)))
+
+
+def mxfp4_moe_cold_pairs(workspace, n_slots, n_tokens, top_k, ws_bytes=None, stream=None):
+    """The plan's cold pairs (increasing pair indices) as a list."""
+    import numpy as np
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    cap = n_tokens * top_k
+    buf = np.zeros(cap, dtype=np.int32)
+    n = ctypes.c_int(0)
+    _check("mxfp4_moe_cold_pairs", lib().mxfp4_moe_cold_pairs(
+        _addr(workspace), ws_bytes, n_slots, n_tokens, top_k, ctypes.byref(n),
+        buf.ctypes.data, cap, _stream(stream)))
+    return buf[:n.value].tolist()

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace mxk {
@@ -43,23 +44,66 @@ size_t dense_ws_bytes(int rows, int cols, int nb);
 cudaError_t launch_mm_dense(const uint8_t* w, int rows, int cols, const float* X, int nb,
                             float* Y, void* ws, cudaStream_t s);
 
-// Routed experts.  The workspace layout is owned by moe.cu.
-size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter);
-cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,
+// Tail of the gate/up pass ("cortiq-engine 0.8.40 src/gpu_wgpu/mxfp4.rs",
+// dsv4_global_gate_up_mxfp4): bf16 != 0 rounds gate and up to bfloat16, folds
+// the pair's route weight into the act and rounds the act too (the V4.1
+// mode); limit > 0 clamps up to [-limit, limit] and gate to at most limit.
+struct MoeAct {
+    const float* route_w;   // [pairs]; read in the bf16 mode only
+    float limit;
+    int bf16;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float moe_bf16(float v) {
+    return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)))
+                           << 16);
+}
+
+// act of pair `pair` from its gate and up dot products g and u (FP32).
+__device__ __forceinline__ float moe_act(float g, float u, const MoeAct& epi, int pair) {
+    if (epi.bf16) {
+        g = moe_bf16(g);
+        u = moe_bf16(u);
+    }
+    if (epi.limit > 0.0f) {
+        const float lim = epi.limit;
+        u = u < -lim ? -lim : (u > lim ? lim : u);
+        g = g < lim ? g : lim;
+    }
+    float a = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    if (epi.bf16) a = moe_bf16(__fmul_rn(__ldg(epi.route_w + pair), a));
+    return a;
+}
+#endif
+
+// Routed experts.  The workspace layout is owned by moe.cu.  n_slots is the
+// number of experts in the banks; ids map to slots through slot_of (nullable:
+// slot = id; a negative entry marks a cold expert, whose pairs are skipped and
+// listed), ids outside [0, n_ids) and slots outside [0, n_slots) are invalid.
+size_t moe_workspace_bytes(int n_slots, int n_tokens, int top_k, int hidden, int inter);
+cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_slots,
                                int hidden, int inter, const float* x, int n_tokens, int top_k,
-                               const int32_t* ids, float* act, void* ws, cudaStream_t s);
-cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden, int inter,
-                            const float* act, int n_tokens, int top_k, const int32_t* ids,
-                            const float* route_w, float* y, void* ws, cudaStream_t s);
+                               const int32_t* ids, const int32_t* slot_of, int n_ids,
+                               MoeAct epi, float* act, void* ws, cudaStream_t s);
+// bf16 != 0: y = bf16(sum over the token's slots of o), the route weights being
+// in the acts already; else y = sum of route_w * o.
+cudaError_t launch_moe_down(const uint8_t* down_bank, int n_slots, int hidden, int inter,
+                            const float* act, int n_tokens, int top_k, const float* route_w,
+                            int bf16, float* y, void* ws, cudaStream_t s);
 cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
+// The plan's cold pairs (increasing pair order): their count, and up to `cap`
+// of them copied to host memory; synchronises the stream.
+cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold,
+                           int32_t* pairs_host, int cap, cudaStream_t s);
 
 // Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu;
 // cudaErrorNotSupported, with nothing launched, for shapes they cannot take.
 cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
                                   int n_experts, int inter, int hidden, int top_k, const float* x,
                                   const int32_t* hdr, const int32_t* offsets,
-                                  const int32_t* touched, const int32_t* pair_of, float* act,
-                                  cudaStream_t s);
+                                  const int32_t* touched, const int32_t* pair_of, MoeAct epi,
+                                  float* act, cudaStream_t s);
 cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
                                int inter, const float* act, const int32_t* hdr,
                                const int32_t* offsets, const int32_t* touched,

@@ -30,18 +30,20 @@ namespace {
 
 // Workspace layout (all offsets 16-byte aligned; o_pairs 256-byte aligned).
 struct WsLayout {
-    size_t hdr, offsets, touched, pair_of, o_pairs, total;
+    size_t hdr, offsets, touched, pair_of, pair_slot, cold, o_pairs, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-WsLayout ws_layout(int n_experts, int n_pairs, int hidden) {
+WsLayout ws_layout(int n_slots, int n_pairs, int hidden) {
     WsLayout l;
-    l.hdr = 0;                                            // int32[4]: invalid, touched
-    l.offsets = 16;                                       // int32[E + 1]
-    l.touched = align_up(l.offsets + 4 * (static_cast<size_t>(n_experts) + 1), 16);
-    l.pair_of = align_up(l.touched + 4 * static_cast<size_t>(n_experts), 16);
-    l.o_pairs = align_up(l.pair_of + 4 * static_cast<size_t>(n_pairs), 256);
+    l.hdr = 0;                                            // int32[4]: invalid, touched, cold
+    l.offsets = 16;                                       // int32[slots + 1]
+    l.touched = align_up(l.offsets + 4 * (static_cast<size_t>(n_slots) + 1), 16);
+    l.pair_of = align_up(l.touched + 4 * static_cast<size_t>(n_slots), 16);
+    l.pair_slot = align_up(l.pair_of + 4 * static_cast<size_t>(n_pairs), 16);   // int32[pairs]
+    l.cold = align_up(l.pair_slot + 4 * static_cast<size_t>(n_pairs), 16);      // int32[pairs]
+    l.o_pairs = align_up(l.cold + 4 * static_cast<size_t>(n_pairs), 256);
     l.total = l.o_pairs + 4 * static_cast<size_t>(n_pairs) * hidden;
     return l;
 }
@@ -51,36 +53,75 @@ struct Plan {
     int32_t* offsets;
     int32_t* touched;
     int32_t* pair_of;
+    int32_t* pair_slot;   // the pair's bank slot; -1 invalid, -2 cold
+    int32_t* cold;        // cold pairs, increasing
     float* o_pairs;
 };
 
-Plan plan_view(void* ws, int n_experts, int n_pairs, int hidden) {
-    const WsLayout l = ws_layout(n_experts, n_pairs, hidden);
+Plan plan_view(void* ws, int n_slots, int n_pairs, int hidden) {
+    const WsLayout l = ws_layout(n_slots, n_pairs, hidden);
     char* b = static_cast<char*>(ws);
     return Plan{reinterpret_cast<int32_t*>(b + l.hdr), reinterpret_cast<int32_t*>(b + l.offsets),
                 reinterpret_cast<int32_t*>(b + l.touched),
                 reinterpret_cast<int32_t*>(b + l.pair_of),
+                reinterpret_cast<int32_t*>(b + l.pair_slot),
+                reinterpret_cast<int32_t*>(b + l.cold),
                 reinterpret_cast<float*>(b + l.o_pairs)};
 }
 
+constexpr int32_t kSlotInvalid = -1, kSlotCold = -2;
+
+// The bank slot of pair p: slot_of[id] (or the id itself without a table);
+// ids outside [0, n_ids) and slots at or past n_slots are invalid, a negative
+// table entry marks a cold expert.
+__device__ __forceinline__ int32_t resolve_slot(const int32_t* __restrict__ ids,
+                                                const int32_t* __restrict__ slot_of, int n_ids,
+                                                int n_slots, int p) {
+    const int32_t e = __ldg(ids + p);
+    if (e < 0 || e >= n_ids) return kSlotInvalid;
+    const int32_t s = slot_of ? __ldg(slot_of + e) : e;
+    if (s < 0) return kSlotCold;
+    return s < n_slots ? s : kSlotInvalid;
+}
+
+// Warp 0 lists the cold pairs in increasing order (a ballot per 32 pairs) and
+// stores their count; the pair slots are visible to the whole CTA.
+__device__ __forceinline__ void list_cold(int n_pairs, Plan plan) {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    int base = 0;
+    for (int p0 = 0; p0 < n_pairs; p0 += 32) {
+        const int p = p0 + lane;
+        const bool c = p < n_pairs && plan.pair_slot[p] == kSlotCold;
+        const unsigned m = __ballot_sync(0xffffffffu, c);
+        if (c) plan.cold[base + __popc(m & ((1u << lane) - 1u))] = p;
+        base += __popc(m);
+    }
+    if (lane == 0) plan.hdr[2] = base;
+}
+
 // ---------------------------------------------------------------------------
-// Routing plan, one CTA.  Thread e counts and then lists the pairs of expert e
+// Routing plan, one CTA.  Thread s counts and then lists the pairs of slot s
 // (stable: increasing pair index), as the counting sort of
 // grouped_moe_sort_plan does; thread 0 prefix-sums the counts.
 __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ ids, int n_pairs,
-                                                   int n_experts, Plan plan) {
+                                                   int n_experts, const int32_t* __restrict__ slot_of,
+                                                   int n_ids, Plan plan) {
     __shared__ int s_invalid;
     if (threadIdx.x == 0) s_invalid = 0;
     __syncthreads();
     int bad = 0;
     for (int p = threadIdx.x; p < n_pairs; p += blockDim.x) {
-        const int32_t e = __ldg(ids + p);
-        bad += (e < 0 || e >= n_experts) ? 1 : 0;
+        const int32_t sl = resolve_slot(ids, slot_of, n_ids, n_experts, p);
+        plan.pair_slot[p] = sl;
+        bad += sl == kSlotInvalid ? 1 : 0;
     }
     if (bad) atomicAdd(&s_invalid, bad);
+    __syncthreads();
+    list_cold(n_pairs, plan);
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
         int count = 0;
-        for (int p = 0; p < n_pairs; ++p) count += (__ldg(ids + p) == e) ? 1 : 0;
+        for (int p = 0; p < n_pairs; ++p) count += (plan.pair_slot[p] == e) ? 1 : 0;
         plan.offsets[e + 1] = count;
     }
     __syncthreads();
@@ -100,7 +141,7 @@ __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ i
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
         int pos = plan.offsets[e];
         for (int p = 0; p < n_pairs; ++p)
-            if (__ldg(ids + p) == e) plan.pair_of[pos++] = p;
+            if (plan.pair_slot[p] == e) plan.pair_of[pos++] = p;
     }
 }
 
@@ -111,8 +152,10 @@ __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ i
 constexpr int kPlanSmemExperts = 4096;
 
 __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__ ids, int n_pairs,
-                                                     int n_experts, Plan plan) {
-    extern __shared__ int s_cnt[];   // [n_experts]
+                                                     int n_experts,
+                                                     const int32_t* __restrict__ slot_of, int n_ids,
+                                                     Plan plan) {
+    extern __shared__ int s_cnt[];   // [n_experts] (bank slots)
     __shared__ int s_wsum[2][32];
     __shared__ int s_invalid;
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
@@ -121,14 +164,16 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
     __syncthreads();
     int bad = 0;
     for (int p = tid; p < n_pairs; p += nt) {
-        const int32_t e = __ldg(ids + p);
-        if (e < 0 || e >= n_experts)
+        const int32_t sl = resolve_slot(ids, slot_of, n_ids, n_experts, p);
+        plan.pair_slot[p] = sl;
+        if (sl == kSlotInvalid)
             ++bad;
-        else
-            atomicAdd(&s_cnt[e], 1);
+        else if (sl >= 0)
+            atomicAdd(&s_cnt[sl], 1);
     }
     if (bad) atomicAdd(&s_invalid, bad);
     __syncthreads();
+    list_cold(n_pairs, plan);
     // thread tid takes experts [e0, e1): its count and touched sums, scanned
     // across the warp, then across the warps
     const int per = (n_experts + nt - 1) / nt;
@@ -184,12 +229,12 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
         plan.hdr[1] = f_run;
     }
     __syncthreads();
-    const int n_valid = n_pairs - s_invalid;
+    const int n_planned = plan.offsets[n_experts];
     for (int e = tid; e < n_experts; e += nt) {
         int pos = s_cnt[e];
-        const int end = e + 1 < n_experts ? s_cnt[e + 1] : n_valid;
+        const int end = e + 1 < n_experts ? s_cnt[e + 1] : n_planned;
         for (int p = 0; p < n_pairs && pos < end; ++p)
-            if (__ldg(ids + p) == e) plan.pair_of[pos++] = p;
+            if (plan.pair_slot[p] == e) plan.pair_of[pos++] = p;
     }
 }
 
@@ -202,7 +247,8 @@ template <Pass P, int R, int NB>
 __device__ __forceinline__ void expert_chunk(const uint8_t* const (&wm)[P == Pass::kGateUp ? 2 : 1],
                                              int rows, int cols, long row_w,
                                              const int32_t* pairs, int n, int top_k,
-                                             const float* vec_base, float* out, float* xs) {
+                                             const float* vec_base, float* out, float* xs,
+                                             const MoeAct& epi) {
     constexpr int NM = P == Pass::kGateUp ? 2 : 1;
     const int lane = threadIdx.x & 31;
     const float* xt[NB];
@@ -226,9 +272,7 @@ __device__ __forceinline__ void expert_chunk(const uint8_t* const (&wm)[P == Pas
             if (lane == ((i * NB + t) & 31) && row_w + i < rows && t < n) {
                 const size_t o = static_cast<size_t>(pr[t]) * rows + row_w + i;
                 if constexpr (P == Pass::kGateUp) {
-                    const float g = acc[0][i][t];
-                    const float u = acc[1][i][t];
-                    out[o] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                    out[o] = moe_act(acc[0][i][t], acc[1][i][t], epi, pr[t]);
                 } else {
                     out[o] = acc[0][i][t];
                 }
@@ -241,7 +285,8 @@ __global__ void __launch_bounds__(kThreads) k_moe_pass(const uint8_t* __restrict
                                                        const uint8_t* __restrict__ bank1,
                                                        size_t stride, int rows, int cols,
                                                        int top_k, const float* __restrict__ vec,
-                                                       Plan plan, float* __restrict__ out) {
+                                                       Plan plan, MoeAct epi,
+                                                       float* __restrict__ out) {
     extern __shared__ float4 smem4[];
     float* xs = reinterpret_cast<float*>(smem4);
     constexpr int NM = P == Pass::kGateUp ? 2 : 1;
@@ -262,22 +307,29 @@ __global__ void __launch_bounds__(kThreads) k_moe_pass(const uint8_t* __restrict
             const int n = min(8, n_e - c);
             const int32_t* pairs = plan.pair_of + beg + c;
             if (n == 1)
-                expert_chunk<P, R, 1>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+                expert_chunk<P, R, 1>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs,
+                                        epi);
             else if (n == 2)
-                expert_chunk<P, R, 2>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+                expert_chunk<P, R, 2>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs,
+                                        epi);
             else if (n <= 4)
-                expert_chunk<P, R, 4>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+                expert_chunk<P, R, 4>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs,
+                                        epi);
             else
-                expert_chunk<P, R, 8>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs);
+                expert_chunk<P, R, 8>(wmc, rows, cols, row_w, pairs, n, top_k, vec, out, xs,
+                                        epi);
         }
     }
 }
 
-// y[t*hidden + r] = sum over slots j (in order) of w[t,j] * o[(t*top_k+j)*hidden + r].
+// y[t*hidden + r] = sum over slots j (in order) of w[t,j] * o[(t*top_k+j)*hidden + r];
+// in the bf16 mode the route weights are in the acts already and the sum of
+// the o's is rounded to bfloat16 (dsv4_global_down_mxfp4).  Pairs the plan left
+// out (invalid or cold) add nothing.
 __global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ o_pairs,
-                                                     const int32_t* __restrict__ ids,
+                                                     const int32_t* __restrict__ pair_slot,
                                                      const float* __restrict__ route_w,
-                                                     int n_experts, int n_tokens, int top_k,
+                                                     int bf16, int n_tokens, int top_k,
                                                      int hidden, float* __restrict__ y) {
     const size_t n = static_cast<size_t>(n_tokens) * hidden;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
@@ -286,11 +338,11 @@ __global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ o
         float acc = 0.0f;
         for (int j = 0; j < top_k; ++j) {
             const size_t p = t * top_k + j;
-            const int32_t e = __ldg(ids + p);
-            if (e >= 0 && e < n_experts)
-                acc = __fmaf_rn(__ldg(route_w + p), __ldg(o_pairs + p * hidden + r), acc);
+            if (pair_slot[p] < 0) continue;
+            const float o = __ldg(o_pairs + p * hidden + r);
+            acc = bf16 ? __fadd_rn(acc, o) : __fmaf_rn(__ldg(route_w + p), o, acc);
         }
-        y[i] = acc;
+        y[i] = bf16 ? moe_bf16(acc) : acc;
     }
 }
 
@@ -327,65 +379,84 @@ constexpr int kRowsPerWarp = 2;
 
 template <Pass P>
 cudaError_t launch_pass(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
-                        int rows, int cols, int top_k, const float* vec, Plan plan, float* out,
-                        cudaStream_t s) {
+                        int rows, int cols, int top_k, const float* vec, Plan plan, MoeAct epi,
+                        float* out, cudaStream_t s) {
     auto kernel = k_moe_pass<P, kRowsPerWarp>;
     const long rbn = (rows + kWarps * kRowsPerWarp - 1) / (kWarps * kRowsPerWarp);
     const long max_units = static_cast<long>(n_experts) * rbn;
     const long cap = persistent_grid(reinterpret_cast<const void*>(kernel), kStageBytes);
     const unsigned grid = static_cast<unsigned>(max_units < cap ? max_units : cap);
     kernel<<<grid, kThreads, kStageBytes, s>>>(bank0, bank1, stride, rows, cols, top_k, vec, plan,
-                                               out);
+                                               epi, out);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden, int inter) {
+size_t moe_workspace_bytes(int n_slots, int n_tokens, int top_k, int hidden, int inter) {
     (void)inter;
-    return ws_layout(n_experts, n_tokens * top_k, hidden).total;
+    return ws_layout(n_slots, n_tokens * top_k, hidden).total;
 }
 
-cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_experts,
+cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_slots,
                                int hidden, int inter, const float* x, int n_tokens, int top_k,
-                               const int32_t* ids, float* act, void* ws, cudaStream_t s) {
+                               const int32_t* ids, const int32_t* slot_of, int n_ids,
+                               MoeAct epi, float* act, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
-    const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
-    if (n_experts <= kPlanSmemExperts)
-        k_moe_plan_s<<<1, 1024, 4 * static_cast<size_t>(n_experts), s>>>(ids, n_pairs, n_experts,
-                                                                         plan);
+    const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
+    if (n_slots <= kPlanSmemExperts)
+        k_moe_plan_s<<<1, 1024, 4 * static_cast<size_t>(n_slots), s>>>(ids, n_pairs, n_slots,
+                                                                       slot_of, n_ids, plan);
     else
-        k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_experts, plan);
+        k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t stride = padded_nbytes(inter, hidden);
-    e = launch_moe_tc_gate_up(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k, x,
-                              plan.hdr, plan.offsets, plan.touched, plan.pair_of, act, s);
+    e = launch_moe_tc_gate_up(gate_bank, up_bank, stride, n_slots, inter, hidden, top_k, x,
+                              plan.hdr, plan.offsets, plan.touched, plan.pair_of, epi, act, s);
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
-    return launch_pass<Pass::kGateUp>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k,
-                                      x, plan, act, s);
+    return launch_pass<Pass::kGateUp>(gate_bank, up_bank, stride, n_slots, inter, hidden, top_k,
+                                      x, plan, epi, act, s);
 }
 
-cudaError_t launch_moe_down(const uint8_t* down_bank, int n_experts, int hidden, int inter,
-                            const float* act, int n_tokens, int top_k, const int32_t* ids,
-                            const float* route_w, float* y, void* ws, cudaStream_t s) {
+cudaError_t launch_moe_down(const uint8_t* down_bank, int n_slots, int hidden, int inter,
+                            const float* act, int n_tokens, int top_k, const float* route_w,
+                            int bf16, float* y, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
-    const Plan plan = plan_view(ws, n_experts, n_pairs, hidden);
+    const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
     const size_t stride = padded_nbytes(hidden, inter);
-    cudaError_t e = launch_moe_tc_down(down_bank, stride, n_experts, hidden, inter, act, plan.hdr,
+    cudaError_t e = launch_moe_tc_down(down_bank, stride, n_slots, hidden, inter, act, plan.hdr,
                                        plan.offsets, plan.touched, plan.pair_of, plan.o_pairs, s);
     if (e == cudaErrorNotSupported) {
         (void)cudaGetLastError();
-        e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_experts, hidden, inter, top_k,
-                                     act, plan, plan.o_pairs, s);
+        e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_slots, hidden, inter, top_k,
+                                     act, plan, MoeAct{nullptr, 0.0f, 0}, plan.o_pairs, s);
     }
     if (e != cudaSuccess) return e;
     const size_t n = static_cast<size_t>(n_tokens) * hidden;
     const unsigned blocks = static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    k_moe_combine<<<blocks, 256, 0, s>>>(plan.o_pairs, ids, route_w, n_experts, n_tokens, top_k,
-                                         hidden, y);
+    k_moe_combine<<<blocks, 256, 0, s>>>(plan.o_pairs, plan.pair_slot, route_w, bf16, n_tokens,
+                                         top_k, hidden, y);
     return cudaGetLastError();
+}
+
+cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold,
+                           int32_t* pairs_host, int cap, cudaStream_t s) {
+    const WsLayout l = ws_layout(n_slots, n_pairs, 32);
+    const char* b = static_cast<const char*>(ws);
+    int32_t n = 0;
+    cudaError_t e = cudaMemcpyAsync(&n, b + l.hdr + 8, sizeof(n), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    *n_cold = n;
+    const int k = n < cap ? n : cap;
+    if (k > 0 && pairs_host != nullptr) {
+        e = cudaMemcpyAsync(pairs_host, b + l.cold, sizeof(int32_t) * static_cast<size_t>(k),
+                            cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
 }
 
 cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s) {

@@ -120,11 +120,11 @@ extern "C" int mxfp4_moe_layer_noalloc(const void* gate_bank, const void* up_ban
         float* act = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + act_offset);
         e = mxk::launch_moe_gate_up(static_cast<const uint8_t*>(gate_bank),
                                     static_cast<const uint8_t*>(up_bank), n_experts, hidden,
-                                    inter, x, n_tokens, top_k, expert_ids, act, scratch, stream);
+                                    inter, x, n_tokens, top_k, expert_ids, nullptr, n_experts,
+                                    mxk::MoeAct{nullptr, 0.0f, 0}, act, scratch, stream);
         if (e == cudaSuccess)
             e = mxk::launch_moe_down(static_cast<const uint8_t*>(down_bank), n_experts, hidden,
-                                     inter, act, n_tokens, top_k, expert_ids, route_w, y, scratch,
-                                     stream);
+                                     inter, act, n_tokens, top_k, route_w, 0, y, scratch, stream);
     }
     if (e != cudaSuccess) {
         mxk::record_cuda_error(static_cast<int>(e));

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     k_moe_tc(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
              const uint8_t* __restrict__ bank0, const uint8_t* __restrict__ bank1, size_t stride,
              int rows, int cols, int top_k, int n_experts, const float* __restrict__ vec,
-             PlanRef plan, float* __restrict__ out) {
+             PlanRef plan, MoeAct epi, float* __restrict__ out) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             if (row < rows && tok < cur.npair) {
                 const size_t o = static_cast<size_t>(spair[tok]) * rows + row;
                 if constexpr (NM == 2)
-                    out[o] = __fmul_rn(__fdiv_rn(v[0], __fadd_rn(1.0f, expf(-v[0]))), v[1]);
+                    out[o] = moe_act(v[0], v[1], epi, spair[tok]);
                 else
                     out[o] = v[0];
             }
@@ -525,8 +525,8 @@ int sm_count_e() {
 
 template <int NM>
 cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
-                     int rows, int cols, int top_k, const float* vec, PlanRef plan, float* out,
-                     cudaStream_t s) {
+                     int rows, int cols, int top_k, const float* vec, PlanRef plan, MoeAct epi,
+                     float* out, cudaStream_t s) {
     const int gpr = cols / kGroup;
     if (gpr > kGMaxE || n_experts > kMaxExpertsE) return cudaErrorNotSupported;
     const ELayout l = e_layout(NM, gpr, n_experts);
@@ -548,7 +548,7 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
         m1 = m0;
     }
     kernel<<<sm_count_e(), kThreadsE, l.total, s>>>(m0, m1, bank0, bank1, stride, rows, cols, top_k,
-                                                    n_experts, vec, plan, out);
+                                                    n_experts, vec, plan, epi, out);
     return cudaGetLastError();
 }
 
@@ -557,10 +557,10 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
 cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
                                   int n_experts, int inter, int hidden, int top_k, const float* x,
                                   const int32_t* hdr, const int32_t* offsets,
-                                  const int32_t* touched, const int32_t* pair_of, float* act,
-                                  cudaStream_t s) {
+                                  const int32_t* touched, const int32_t* pair_of, MoeAct epi,
+                                  float* act, cudaStream_t s) {
     return launch_e<2>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k, x,
-                       PlanRef{hdr, offsets, touched, pair_of}, act, s);
+                       PlanRef{hdr, offsets, touched, pair_of}, epi, act, s);
 }
 
 cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
@@ -568,7 +568,8 @@ cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_ex
                                const int32_t* offsets, const int32_t* touched,
                                const int32_t* pair_of, float* o_pairs, cudaStream_t s) {
     return launch_e<1>(down_bank, down_bank, stride, n_experts, hidden, inter, 1, act,
-                       PlanRef{hdr, offsets, touched, pair_of}, o_pairs, s);
+                       PlanRef{hdr, offsets, touched, pair_of}, MoeAct{nullptr, 0.0f, 0}, o_pairs,
+                       s);
 }
 
 cudaError_t read_fault_moetc(int* value, bool reset) {

@@ -207,8 +207,8 @@ int mxfp4_moe_gate_up(const void* gate_bank, const void* up_bank, int n_experts,
     if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
         return MXFP4_STATUS_BAD_POINTER;
     return from_cuda(mxk::launch_moe_gate_up(u8(gate_bank), u8(up_bank), n_experts, hidden, inter,
-                                             x, n_tokens, top_k, expert_ids, act, workspace,
-                                             stream));
+                                             x, n_tokens, top_k, expert_ids, nullptr, n_experts,
+                                             mxk::MoeAct{nullptr, 0.0f, 0}, act, workspace, stream));
 }
 
 int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter, const float* act,
@@ -222,7 +222,71 @@ int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter, 
         route_w == nullptr || (reinterpret_cast<uintptr_t>(route_w) & 3u))
         return MXFP4_STATUS_BAD_POINTER;
     return from_cuda(mxk::launch_moe_down(u8(down_bank), n_experts, hidden, inter, act, n_tokens,
-                                          top_k, expert_ids, route_w, y, workspace, stream));
+                                          top_k, route_w, 0, y, workspace, stream));
+}
+
+namespace {
+
+bool ptr4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_mode(int mode, float swiglu_limit) {
+    if (mode != MXFP4_MOE_MODE_F32 && mode != MXFP4_MOE_MODE_V41) return MXFP4_STATUS_INVALID_ARGUMENT;
+    if (!(swiglu_limit == swiglu_limit) || swiglu_limit > 3.0e38f) return MXFP4_STATUS_INVALID_ARGUMENT;
+    return MXFP4_STATUS_OK;
+}
+
+}  // namespace
+
+int mxfp4_moe_gate_up_ex(const void* gate_bank, const void* up_bank, int n_slots, int hidden,
+                         int inter, const float* x, int n_tokens, int top_k,
+                         const int32_t* expert_ids, const int32_t* slot_of, int n_experts,
+                         const float* route_w, int mode, float swiglu_limit, float* act,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_moe(n_slots, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
+    MXFP4_TRY(check_mode(mode, swiglu_limit));
+    if (n_experts < 1 || n_experts > (1 << 24)) return MXFP4_STATUS_INVALID_ARGUMENT;
+    if (slot_of == nullptr && n_experts != n_slots) return MXFP4_STATUS_INVALID_ARGUMENT;
+    MXFP4_TRY(check_ptr(gate_bank));
+    MXFP4_TRY(check_ptr(up_bank));
+    MXFP4_TRY(check_ptr(x));
+    MXFP4_TRY(check_ptr(act));
+    if (!ptr4(expert_ids) || (slot_of != nullptr && !ptr4(slot_of)) ||
+        (mode == MXFP4_MOE_MODE_V41 && !ptr4(route_w)))
+        return MXFP4_STATUS_BAD_POINTER;
+    const mxk::MoeAct epi{route_w, swiglu_limit > 0.0f ? swiglu_limit : 0.0f,
+                          mode == MXFP4_MOE_MODE_V41 ? 1 : 0};
+    return from_cuda(mxk::launch_moe_gate_up(u8(gate_bank), u8(up_bank), n_slots, hidden, inter,
+                                             x, n_tokens, top_k, expert_ids, slot_of, n_experts,
+                                             epi, act, workspace, stream));
+}
+
+int mxfp4_moe_down_ex(const void* down_bank, int n_slots, int hidden, int inter, const float* act,
+                      int n_tokens, int top_k, const float* route_w, int mode, float* y,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_moe(n_slots, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
+    MXFP4_TRY(check_mode(mode, 0.0f));
+    MXFP4_TRY(check_ptr(down_bank));
+    MXFP4_TRY(check_ptr(act));
+    MXFP4_TRY(check_ptr(y));
+    if (mode == MXFP4_MOE_MODE_F32 && !ptr4(route_w)) return MXFP4_STATUS_BAD_POINTER;
+    return from_cuda(mxk::launch_moe_down(u8(down_bank), n_slots, hidden, inter, act, n_tokens,
+                                          top_k, route_w, mode == MXFP4_MOE_MODE_V41 ? 1 : 0, y,
+                                          workspace, stream));
+}
+
+int mxfp4_moe_cold_pairs(const void* workspace, size_t ws_bytes, int n_slots, int n_tokens,
+                         int top_k, int* n_cold, int32_t* pairs_host, int capacity,
+                         cudaStream_t stream) {
+    if (n_slots < 1 || n_tokens < 1 || top_k < 1 ||
+        static_cast<long long>(n_tokens) * top_k > (1 << 22) || capacity < 0)
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    if (workspace == nullptr || n_cold == nullptr || !aligned16(workspace) ||
+        (capacity > 0 && pairs_host == nullptr))
+        return MXFP4_STATUS_BAD_POINTER;
+    if (ws_bytes < mxk::moe_workspace_bytes(n_slots, n_tokens, top_k, 32, 32))
+        return MXFP4_STATUS_WORKSPACE_TOO_SMALL;
+    return from_cuda(mxk::moe_cold_pairs(workspace, n_slots, n_tokens * top_k, n_cold, pairs_host,
+                                         capacity, stream));
 }
 
 int mxfp4_moe_plan_errors(const void* workspace, size_t ws_bytes, int* n_invalid,
