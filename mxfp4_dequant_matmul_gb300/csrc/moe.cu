@@ -146,19 +146,28 @@ __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ i
 }
 
 // The same plan with the counts, offsets and touched flags in shared memory
-// (up to kPlanSmemExperts experts): counts by shared atomics, offsets and the
-// touched list by block-wide exclusive scans, then each touched expert lists
-// its pairs in increasing order.  The arrays it writes are those of k_moe_plan.
+// (up to kPlanSmemExperts slots) and the pairs' slots too (up to
+// kPlanSmemPairs pairs; beyond, read back from the workspace): counts by
+// shared atomics, offsets and the touched list by block-wide exclusive scans,
+// then each warp lists the pairs of its touched slots in increasing order, 32
+// pairs per ballot.  The arrays it writes are those of k_moe_plan.
 constexpr int kPlanSmemExperts = 4096;
+constexpr int kPlanSmemPairs = 6144;   // with 4096 slots: 40 KB, under the 48 KB default
 
 __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__ ids, int n_pairs,
                                                      int n_experts,
                                                      const int32_t* __restrict__ slot_of, int n_ids,
                                                      Plan plan) {
-    extern __shared__ int s_cnt[];   // [n_experts] (bank slots)
+    extern __shared__ int s_dyn[];   // [n_experts] counts, then [n_pairs] slots (if they fit)
+    int* s_cnt = s_dyn;
+    int* s_ps = s_dyn + n_experts;
     __shared__ int s_wsum[2][32];
     __shared__ int s_invalid;
     const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+    // the expert pass may be scheduled now; it waits for this plan to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const bool ps_smem = n_pairs <= kPlanSmemPairs;
+    const int32_t* ps = ps_smem ? s_ps : plan.pair_slot;
     for (int e = tid; e < n_experts; e += nt) s_cnt[e] = 0;
     if (tid == 0) s_invalid = 0;
     __syncthreads();
@@ -166,6 +175,7 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
     for (int p = tid; p < n_pairs; p += nt) {
         const int32_t sl = resolve_slot(ids, slot_of, n_ids, n_experts, p);
         plan.pair_slot[p] = sl;
+        if (ps_smem) s_ps[p] = sl;
         if (sl == kSlotInvalid)
             ++bad;
         else if (sl >= 0)
@@ -173,7 +183,17 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
     }
     if (bad) atomicAdd(&s_invalid, bad);
     __syncthreads();
-    list_cold(n_pairs, plan);
+    if (w == 0) {   // the cold pairs, increasing
+        int base = 0;
+        for (int p0 = 0; p0 < n_pairs; p0 += 32) {
+            const int p = p0 + lane;
+            const bool c = p < n_pairs && ps[p] == kSlotCold;
+            const unsigned m = __ballot_sync(0xffffffffu, c);
+            if (c) plan.cold[base + __popc(m & ((1u << lane) - 1u))] = p;
+            base += __popc(m);
+        }
+        if (lane == 0) plan.hdr[2] = base;
+    }
     // thread tid takes experts [e0, e1): its count and touched sums, scanned
     // across the warp, then across the warps
     const int per = (n_experts + nt - 1) / nt;
@@ -230,11 +250,17 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
     }
     __syncthreads();
     const int n_planned = plan.offsets[n_experts];
-    for (int e = tid; e < n_experts; e += nt) {
+    const int nw = nt >> 5;
+    for (int e = w; e < n_experts; e += nw) {   // warp w lists slots w, w + nw, ...
         int pos = s_cnt[e];
         const int end = e + 1 < n_experts ? s_cnt[e + 1] : n_planned;
-        for (int p = 0; p < n_pairs && pos < end; ++p)
-            if (plan.pair_slot[p] == e) plan.pair_of[pos++] = p;
+        for (int p0 = 0; p0 < n_pairs && pos < end; p0 += 32) {
+            const int p = p0 + lane;
+            const bool mine = p < n_pairs && ps[p] == e;
+            const unsigned m = __ballot_sync(0xffffffffu, mine);
+            if (mine) plan.pair_of[pos + __popc(m & ((1u << lane) - 1u))] = p;
+            pos += __popc(m);
+        }
     }
 }
 
@@ -331,6 +357,8 @@ __global__ void __launch_bounds__(256) k_moe_combine(const float* __restrict__ o
                                                      const float* __restrict__ route_w,
                                                      int bf16, int n_tokens, int top_k,
                                                      int hidden, float* __restrict__ y) {
+    // launched dependent on the down pass: its per-pair outputs after it completes
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t n = static_cast<size_t>(n_tokens) * hidden;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -405,8 +433,10 @@ cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
     const int n_pairs = n_tokens * top_k;
     const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
     if (n_slots <= kPlanSmemExperts)
-        k_moe_plan_s<<<1, 1024, 4 * static_cast<size_t>(n_slots), s>>>(ids, n_pairs, n_slots,
-                                                                       slot_of, n_ids, plan);
+        k_moe_plan_s<<<1, 1024,
+                       4 * (static_cast<size_t>(n_slots) +
+                            static_cast<size_t>(n_pairs <= kPlanSmemPairs ? n_pairs : 0)),
+                       s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
     else
         k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
     cudaError_t e = cudaGetLastError();
@@ -436,8 +466,19 @@ cudaError_t launch_moe_down(const uint8_t* down_bank, int n_slots, int hidden, i
     if (e != cudaSuccess) return e;
     const size_t n = static_cast<size_t>(n_tokens) * hidden;
     const unsigned blocks = static_cast<unsigned>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    k_moe_combine<<<blocks, 256, 0, s>>>(plan.o_pairs, plan.pair_slot, route_w, bf16, n_tokens,
-                                         top_k, hidden, y);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_moe_combine, static_cast<const float*>(plan.o_pairs),
+                           static_cast<const int32_t*>(plan.pair_slot), route_w, bf16, n_tokens,
+                           top_k, hidden, y);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -133,8 +133,13 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const int n_c = (gpr + kChunkE - 1) / kChunkE;
     const uint64_t policy = l2_evict_first();
 
+    // launched dependent on the previous kernel of the layer (programmatic
+    // dependent launch): let the next one be scheduled, set up, then wait for
+    // the previous kernel's plan / activations before reading them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
     if (tid < 4) reinterpret_cast<uint32_t*>(smem + L.misc + 64)[tid] = 0u;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) {
         mbar_init(&sbar[0], 1);
         mbar_init(&sbar[1], 1);
@@ -547,8 +552,19 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
     } else {
         m1 = m0;
     }
-    kernel<<<sm_count_e(), kThreadsE, l.total, s>>>(m0, m1, bank0, bank1, stride, rows, cols, top_k,
-                                                    n_experts, vec, plan, epi, out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count_e()));
+    cfg.blockDim = dim3(kThreadsE);
+    cfg.dynamicSmemBytes = l.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, bank0, bank1, stride, rows, cols,
+                                             top_k, n_experts, vec, plan, epi, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
