@@ -251,6 +251,27 @@ int mxfp4_moe_down_ex(const void* down_bank, int n_slots, int hidden, int inter,
                       int n_tokens, int top_k, const float* route_w, int mode, float* y,
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* The same two passes on a SEGMENTED bank: the bank's n_segments *
+ * segment_slots slots live in n_segments separate buffers (segments, at most
+ * 16), slot s at local index s % segment_slots of segment s / segment_slots,
+ * each segment holding its slots back to back at the same stride as a
+ * one-buffer bank (the page's global bank: binding arrays of 8 or 16 segment
+ * buffers, gg_sel's flat slot split into segment and local index).
+ * gate_segments / up_segments / down_segments are HOST arrays of n_segments
+ * DEVICE pointers (16-byte aligned), read during the call.  Every other
+ * argument, the workspace and the results are those of the _ex passes with
+ * n_slots = n_segments * segment_slots. */
+int mxfp4_moe_gate_up_seg(const void* const* gate_segments, const void* const* up_segments,
+                          int n_segments, int segment_slots, int hidden, int inter, const float* x,
+                          int n_tokens, int top_k, const int32_t* expert_ids,
+                          const int32_t* slot_of, int n_experts, const float* route_w, int mode,
+                          float swiglu_limit, float* act, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream);
+int mxfp4_moe_down_seg(const void* const* down_segments, int n_segments, int segment_slots,
+                       int hidden, int inter, const float* act, int n_tokens, int top_k,
+                       const float* route_w, int mode, float* y, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream);
+
 /* The plan's cold pairs (p = t*top_k + j, increasing): their count in *n_cold
  * and the first min(count, capacity) indices copied to pairs_host (host).
  * Synchronises the stream. */

@@ -18,7 +18,8 @@ __all__ = [
     "mxfp4_mm_bf16_ws", "mxfp4_matmat_host",
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
     "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_moe_gate_up_ex",
-    "mxfp4_moe_down_ex", "mxfp4_moe_cold_pairs", "MOE_MODE_F32", "MOE_MODE_V41",
+    "mxfp4_moe_down_ex", "mxfp4_moe_cold_pairs", "mxfp4_moe_gate_up_seg", "mxfp4_moe_down_seg",
+    "MOE_MODE_F32", "MOE_MODE_V41",
     "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
 ]
 
@@ -55,6 +56,9 @@ _SIG = {
                                   ctypes.c_float, _P, _P, _SZ, _P]),
     "mxfp4_moe_down_ex": (_I, [_P, _I, _I, _I, _P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "mxfp4_moe_cold_pairs": (_I, [_P, _SZ, _I, _I, _I, ctypes.POINTER(_I), _P, _I, _P]),
+    "mxfp4_moe_gate_up_seg": (_I, [_P, _P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _I,
+                                   ctypes.c_float, _P, _P, _SZ, _P]),
+    "mxfp4_moe_down_seg": (_I, [_P, _I, _I, _I, _I, _P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIG)
 _lib = None
@@ -258,3 +262,34 @@ def mxfp4_moe_cold_pairs(workspace, n_slots, n_tokens, top_k, ws_bytes=None, str
         _addr(workspace), ws_bytes, n_slots, n_tokens, top_k, ctypes.byref(n),
         buf.ctypes.data, cap, _stream(stream)))
     return buf[:n.value].tolist()
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[_addr(t) for t in tensors])
+    return arr
+
+
+def mxfp4_moe_gate_up_seg(gate_segments, up_segments, segment_slots, hidden, inter, x, n_tokens,
+                          top_k, expert_ids, act, workspace, slot_of=None, n_experts=None,
+                          route_w=None, mode=MOE_MODE_F32, swiglu_limit=0.0, ws_bytes=None,
+                          stream=None):
+    """Gate/up pass on a bank in segments (lists of device tensors, one per segment)."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    n_seg = len(gate_segments)
+    n_experts = n_seg * segment_slots if n_experts is None else n_experts
+    g, u = _ptr_array(gate_segments), _ptr_array(up_segments)
+    _check("mxfp4_moe_gate_up_seg", lib().mxfp4_moe_gate_up_seg(
+        ctypes.cast(g, _P), ctypes.cast(u, _P), n_seg, segment_slots, hidden, inter, _addr(x),
+        n_tokens, top_k, _addr(expert_ids), _addr(slot_of), n_experts, _addr(route_w), int(mode),
+        float(swiglu_limit), _addr(act), _addr(workspace), ws_bytes, _stream(stream)))
+
+
+def mxfp4_moe_down_seg(down_segments, segment_slots, hidden, inter, act, n_tokens, top_k, y,
+                       workspace, route_w=None, mode=MOE_MODE_F32, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    d = _ptr_array(down_segments)
+    _check("mxfp4_moe_down_seg", lib().mxfp4_moe_down_seg(
+        ctypes.cast(d, _P), len(down_segments), segment_slots, hidden, inter, _addr(act), n_tokens,
+        top_k, _addr(route_w), int(mode), _addr(y), _addr(workspace), ws_bytes, _stream(stream)))

@@ -77,18 +77,42 @@ __device__ __forceinline__ float moe_act(float g, float u, const MoeAct& epi, in
 }
 #endif
 
+// An expert bank: its slots held in up to kMaxSegments separate buffers
+// (segments) of seg_slots slots each, slot s at local index s % seg_slots of
+// segment s / seg_slots, `stride` bytes per slot.  A bank in one buffer is
+// one segment of all its slots.
+constexpr int kMaxSegments = 16;
+struct Bank {
+    const uint8_t* seg[kMaxSegments];
+    int n_seg;
+    int seg_slots;
+    size_t stride;
+    __host__ __device__ const uint8_t* slot(int s) const {
+        const int q = s / seg_slots;
+        return seg[q] + static_cast<size_t>(s - q * seg_slots) * stride;
+    }
+};
+inline Bank one_segment_bank(const uint8_t* base, int n_slots, size_t stride) {
+    Bank b{};
+    b.seg[0] = base;
+    b.n_seg = 1;
+    b.seg_slots = n_slots;
+    b.stride = stride;
+    return b;
+}
+
 // Routed experts.  The workspace layout is owned by moe.cu.  n_slots is the
 // number of experts in the banks; ids map to slots through slot_of (nullable:
 // slot = id; a negative entry marks a cold expert, whose pairs are skipped and
 // listed), ids outside [0, n_ids) and slots outside [0, n_slots) are invalid.
 size_t moe_workspace_bytes(int n_slots, int n_tokens, int top_k, int hidden, int inter);
-cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_slots,
-                               int hidden, int inter, const float* x, int n_tokens, int top_k,
+cudaError_t launch_moe_gate_up(const Bank& gate, const Bank& up, int n_slots, int hidden,
+                               int inter, const float* x, int n_tokens, int top_k,
                                const int32_t* ids, const int32_t* slot_of, int n_ids,
                                MoeAct epi, float* act, void* ws, cudaStream_t s);
 // bf16 != 0: y = bf16(sum over the token's slots of o), the route weights being
 // in the acts already; else y = sum of route_w * o.
-cudaError_t launch_moe_down(const uint8_t* down_bank, int n_slots, int hidden, int inter,
+cudaError_t launch_moe_down(const Bank& down, int n_slots, int hidden, int inter,
                             const float* act, int n_tokens, int top_k, const float* route_w,
                             int bf16, float* y, void* ws, cudaStream_t s);
 cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
@@ -99,15 +123,14 @@ cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold
 
 // Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu;
 // cudaErrorNotSupported, with nothing launched, for shapes they cannot take.
-cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
-                                  int n_experts, int inter, int hidden, int top_k, const float* x,
-                                  const int32_t* hdr, const int32_t* offsets,
-                                  const int32_t* touched, const int32_t* pair_of, MoeAct epi,
-                                  float* act, cudaStream_t s);
-cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
-                               int inter, const float* act, const int32_t* hdr,
-                               const int32_t* offsets, const int32_t* touched,
-                               const int32_t* pair_of, float* o_pairs, cudaStream_t s);
+cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
+                                  int hidden, int top_k, const float* x, const int32_t* hdr,
+                                  const int32_t* offsets, const int32_t* touched,
+                                  const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s);
+cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
+                               const float* act, const int32_t* hdr, const int32_t* offsets,
+                               const int32_t* touched, const int32_t* pair_of, float* o_pairs,
+                               cudaStream_t s);
 
 // Device fault words (set when a bounded wait gives up); read and optionally clear.
 cudaError_t read_fault_matvec(int* value, bool reset);

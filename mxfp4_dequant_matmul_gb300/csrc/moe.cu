@@ -307,9 +307,8 @@ __device__ __forceinline__ void expert_chunk(const uint8_t* const (&wm)[P == Pas
 
 // Persistent over units (touched expert u, row block rb), u-major.
 template <Pass P, int R>
-__global__ void __launch_bounds__(kThreads) k_moe_pass(const uint8_t* __restrict__ bank0,
-                                                       const uint8_t* __restrict__ bank1,
-                                                       size_t stride, int rows, int cols,
+__global__ void __launch_bounds__(kThreads) k_moe_pass(const Bank bank0, const Bank bank1,
+                                                       int rows, int cols,
                                                        int top_k, const float* __restrict__ vec,
                                                        Plan plan, MoeAct epi,
                                                        float* __restrict__ out) {
@@ -326,8 +325,8 @@ __global__ void __launch_bounds__(kThreads) k_moe_pass(const uint8_t* __restrict
         const int beg = plan.offsets[e], n_e = plan.offsets[e + 1] - beg;
         const long row_w = static_cast<long>(rb) * (kWarps * R) + warp * R;
         const uint8_t* wm[NM];
-        wm[0] = bank0 + static_cast<size_t>(e) * stride;
-        if constexpr (NM == 2) wm[1] = bank1 + static_cast<size_t>(e) * stride;
+        wm[0] = bank0.slot(e);
+        if constexpr (NM == 2) wm[1] = bank1.slot(e);
         const uint8_t* const(&wmc)[NM] = wm;
         for (int c = 0; c < n_e; c += 8) {
             const int n = min(8, n_e - c);
@@ -406,16 +405,16 @@ int persistent_grid(const void* kernel, size_t smem) {
 constexpr int kRowsPerWarp = 2;
 
 template <Pass P>
-cudaError_t launch_pass(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
-                        int rows, int cols, int top_k, const float* vec, Plan plan, MoeAct epi,
-                        float* out, cudaStream_t s) {
+cudaError_t launch_pass(const Bank& bank0, const Bank& bank1, int n_experts, int rows, int cols,
+                        int top_k, const float* vec, Plan plan, MoeAct epi, float* out,
+                        cudaStream_t s) {
     auto kernel = k_moe_pass<P, kRowsPerWarp>;
     const long rbn = (rows + kWarps * kRowsPerWarp - 1) / (kWarps * kRowsPerWarp);
     const long max_units = static_cast<long>(n_experts) * rbn;
     const long cap = persistent_grid(reinterpret_cast<const void*>(kernel), kStageBytes);
     const unsigned grid = static_cast<unsigned>(max_units < cap ? max_units : cap);
-    kernel<<<grid, kThreads, kStageBytes, s>>>(bank0, bank1, stride, rows, cols, top_k, vec, plan,
-                                               epi, out);
+    kernel<<<grid, kThreads, kStageBytes, s>>>(bank0, bank1, rows, cols, top_k, vec, plan, epi,
+                                               out);
     return cudaGetLastError();
 }
 
@@ -426,8 +425,8 @@ size_t moe_workspace_bytes(int n_slots, int n_tokens, int top_k, int hidden, int
     return ws_layout(n_slots, n_tokens * top_k, hidden).total;
 }
 
-cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, int n_slots,
-                               int hidden, int inter, const float* x, int n_tokens, int top_k,
+cudaError_t launch_moe_gate_up(const Bank& gate, const Bank& up, int n_slots, int hidden,
+                               int inter, const float* x, int n_tokens, int top_k,
                                const int32_t* ids, const int32_t* slot_of, int n_ids,
                                MoeAct epi, float* act, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
@@ -441,27 +440,25 @@ cudaError_t launch_moe_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank,
         k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t stride = padded_nbytes(inter, hidden);
-    e = launch_moe_tc_gate_up(gate_bank, up_bank, stride, n_slots, inter, hidden, top_k, x,
-                              plan.hdr, plan.offsets, plan.touched, plan.pair_of, epi, act, s);
+    e = launch_moe_tc_gate_up(gate, up, n_slots, inter, hidden, top_k, x, plan.hdr, plan.offsets,
+                              plan.touched, plan.pair_of, epi, act, s);
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
-    return launch_pass<Pass::kGateUp>(gate_bank, up_bank, stride, n_slots, inter, hidden, top_k,
-                                      x, plan, epi, act, s);
+    return launch_pass<Pass::kGateUp>(gate, up, n_slots, inter, hidden, top_k, x, plan, epi, act,
+                                      s);
 }
 
-cudaError_t launch_moe_down(const uint8_t* down_bank, int n_slots, int hidden, int inter,
+cudaError_t launch_moe_down(const Bank& down, int n_slots, int hidden, int inter,
                             const float* act, int n_tokens, int top_k, const float* route_w,
                             int bf16, float* y, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
     const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
-    const size_t stride = padded_nbytes(hidden, inter);
-    cudaError_t e = launch_moe_tc_down(down_bank, stride, n_slots, hidden, inter, act, plan.hdr,
-                                       plan.offsets, plan.touched, plan.pair_of, plan.o_pairs, s);
+    cudaError_t e = launch_moe_tc_down(down, n_slots, hidden, inter, act, plan.hdr, plan.offsets,
+                                       plan.touched, plan.pair_of, plan.o_pairs, s);
     if (e == cudaErrorNotSupported) {
         (void)cudaGetLastError();
-        e = launch_pass<Pass::kDown>(down_bank, nullptr, stride, n_slots, hidden, inter, top_k,
-                                     act, plan, MoeAct{nullptr, 0.0f, 0}, plan.o_pairs, s);
+        e = launch_pass<Pass::kDown>(down, down, n_slots, hidden, inter, top_k, act, plan,
+                                     MoeAct{nullptr, 0.0f, 0}, plan.o_pairs, s);
     }
     if (e != cudaSuccess) return e;
     const size_t n = static_cast<size_t>(n_tokens) * hidden;

@@ -118,13 +118,17 @@ extern "C" int mxfp4_moe_layer_noalloc(const void* gate_bank, const void* up_ban
     cudaError_t e = scratch_address(&scratch);
     if (e == cudaSuccess) {
         float* act = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + act_offset);
-        e = mxk::launch_moe_gate_up(static_cast<const uint8_t*>(gate_bank),
-                                    static_cast<const uint8_t*>(up_bank), n_experts, hidden,
-                                    inter, x, n_tokens, top_k, expert_ids, nullptr, n_experts,
-                                    mxk::MoeAct{nullptr, 0.0f, 0}, act, scratch, stream);
+        const size_t gu_stride = mxk::padded_nbytes(inter, hidden);
+        e = mxk::launch_moe_gate_up(
+            mxk::one_segment_bank(static_cast<const uint8_t*>(gate_bank), n_experts, gu_stride),
+            mxk::one_segment_bank(static_cast<const uint8_t*>(up_bank), n_experts, gu_stride),
+            n_experts, hidden, inter, x, n_tokens, top_k, expert_ids, nullptr, n_experts,
+            mxk::MoeAct{nullptr, 0.0f, 0}, act, scratch, stream);
         if (e == cudaSuccess)
-            e = mxk::launch_moe_down(static_cast<const uint8_t*>(down_bank), n_experts, hidden,
-                                     inter, act, n_tokens, top_k, route_w, 0, y, scratch, stream);
+            e = mxk::launch_moe_down(
+                mxk::one_segment_bank(static_cast<const uint8_t*>(down_bank), n_experts,
+                                      mxk::padded_nbytes(hidden, inter)),
+                n_experts, hidden, inter, act, n_tokens, top_k, route_w, 0, y, scratch, stream);
     }
     if (e != cudaSuccess) {
         mxk::record_cuda_error(static_cast<int>(e));

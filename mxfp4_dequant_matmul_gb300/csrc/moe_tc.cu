@@ -101,14 +101,19 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     return l;
 }
 
+// The code planes of a bank's segments as 3-D byte tensors [slots][rows][cols/2]
+// (one tensor map per segment; those past the bank's segment count unused).
+struct BankMaps {
+    CUtensorMap m[kMaxSegments];
+};
+
 // NM = 2: the gate/up pass (matrices gate, up; vector = the token's x),
 // NM = 1: the down pass (matrix down; vector = the pair's act row).
 template <int NM>
 __global__ void __launch_bounds__(kThreadsE, 1)
-    k_moe_tc(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-             const uint8_t* __restrict__ bank0, const uint8_t* __restrict__ bank1, size_t stride,
-             int rows, int cols, int top_k, int n_experts, const float* __restrict__ vec,
-             PlanRef plan, MoeAct epi, float* __restrict__ out) {
+    k_moe_tc(const __grid_constant__ BankMaps tm0, const __grid_constant__ BankMaps tm1,
+             const Bank bank0, const Bank bank1, int rows, int cols, int top_k, int n_experts,
+             const float* __restrict__ vec, PlanRef plan, MoeAct epi, float* __restrict__ out) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
 
     // A segment as this warp sees it.
     struct Seg {
-        int e, beg, npair, row0, nrow, n_ru, WK, m, my_ru, c_lo, n_units;
+        int e, sg, z, beg, npair, row0, nrow, n_ru, WK, m, my_ru, c_lo, n_units;
         bool active;
     };
     auto seg_of = [&](int s) {
@@ -171,6 +176,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         int u = 0;
         while (segst[u + 1] <= s) ++u;
         q.e = plan.touched[u];
+        // the expert's bank segment and its plane in that segment (both banks of
+        // a pass are split alike)
+        q.sg = bank0.n_seg == 1 ? 0 : q.e / bank0.seg_slots;
+        q.z = q.e - q.sg * bank0.seg_slots;
         const int b0 = plan.offsets[q.e], n_e = plan.offsets[q.e + 1] - b0;
         const int rel = s - segst[u];
         const int ck = rel / n_blocks, b = rel - ck * n_blocks;
@@ -189,7 +198,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         q.n_units = q.active ? (kk + 1) * n_c / q.WK - q.c_lo : 0;
         return q;
     };
-    // this warp's unit k of segment q into stage st (lane 0)
+    // this warp's unit k of segment q into stage st (lane 0): expert slot q.e is
+    // plane q.e % seg_slots of its bank segment's tensor map
     auto issue = [&](const Seg& q, int k, int st) {
         const int x = (q.c_lo + k) * kChunkE * kGroupBytes;
         const int y = q.row0 + q.my_ru * kRowsUE;
@@ -198,8 +208,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
             ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
                 smem_u32(ring + st * kStageE)),
-            "l"(q.m == 0 ? &tm0 : &tm1), "r"(x), "r"(y), "r"(q.e), "r"(smem_u32(&bars[st])),
-            "l"(policy)
+            "l"(q.m == 0 ? &tm0.m[q.sg] : &tm1.m[q.sg]), "r"(x), "r"(y), "r"(q.z),
+            "r"(smem_u32(&bars[st])), "l"(policy)
             : "memory");
     };
     // the scale rows of segment q into buffer bi (thread 0): one bulk copy per matrix
@@ -208,9 +218,9 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         uint32_t sz[NM];
         const uint8_t* a0[NM];
         for (int mm = 0; mm < NM; ++mm) {
-            const uint8_t* bank = mm == 0 ? bank0 : bank1;
-            const uint8_t* src =
-                bank + static_cast<size_t>(q.e) * stride + plane + static_cast<size_t>(q.row0) * gpr;
+            const Bank& bk = mm == 0 ? bank0 : bank1;
+            const uint8_t* src = bk.seg[q.sg] + static_cast<size_t>(q.z) * bk.stride + plane +
+                                 static_cast<size_t>(q.row0) * gpr;
             a0[mm] = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(src) &
                                                       ~static_cast<uintptr_t>(15));
             lead[bi * 2 + mm] = static_cast<int>(src - a0[mm]);
@@ -499,8 +509,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_e() {
     return fn;
 }
 
-// The code planes of a bank as a 3-D byte tensor [experts][rows][cols/2] (the
-// expert stride is the padded matrix size), tiles of 32 rows x 128 bytes.
+// The code planes of one bank segment as a 3-D byte tensor [slots][rows][cols/2]
+// (the slot stride is the padded matrix size), tiles of 32 rows x 128 bytes.
 bool bank_map(CUtensorMap* map, const uint8_t* bank, size_t stride, int n_experts, int rows,
               int cols) {
     auto fn = encode_fn_e();
@@ -529,7 +539,7 @@ int sm_count_e() {
 }
 
 template <int NM>
-cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, int n_experts,
+cudaError_t launch_e(const Bank& bank0, const Bank& bank1, int n_experts,
                      int rows, int cols, int top_k, const float* vec, PlanRef plan, MoeAct epi,
                      float* out, cudaStream_t s) {
     const int gpr = cols / kGroup;
@@ -545,12 +555,14 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
         }));
         if (attr_err != cudaSuccess) return attr_err;
     }
-    CUtensorMap m0, m1;
-    if (!bank_map(&m0, bank0, stride, n_experts, rows, cols)) return cudaErrorNotSupported;
+    BankMaps m0{}, m1{};
+    for (int i = 0; i < bank0.n_seg; ++i)
+        if (!bank_map(&m0.m[i], bank0.seg[i], bank0.stride, bank0.seg_slots, rows, cols))
+            return cudaErrorNotSupported;
     if (NM == 2) {
-        if (!bank_map(&m1, bank1, stride, n_experts, rows, cols)) return cudaErrorNotSupported;
-    } else {
-        m1 = m0;
+        for (int i = 0; i < bank1.n_seg; ++i)
+            if (!bank_map(&m1.m[i], bank1.seg[i], bank1.stride, bank1.seg_slots, rows, cols))
+                return cudaErrorNotSupported;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count_e()));
@@ -562,28 +574,27 @@ cudaError_t launch_e(const uint8_t* bank0, const uint8_t* bank1, size_t stride, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, bank0, bank1, stride, rows, cols,
-                                             top_k, n_experts, vec, plan, epi, out);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, bank0, bank1, rows, cols, top_k,
+                                             n_experts, vec, plan, epi, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_moe_tc_gate_up(const uint8_t* gate_bank, const uint8_t* up_bank, size_t stride,
-                                  int n_experts, int inter, int hidden, int top_k, const float* x,
-                                  const int32_t* hdr, const int32_t* offsets,
-                                  const int32_t* touched, const int32_t* pair_of, MoeAct epi,
-                                  float* act, cudaStream_t s) {
-    return launch_e<2>(gate_bank, up_bank, stride, n_experts, inter, hidden, top_k, x,
+cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
+                                  int hidden, int top_k, const float* x, const int32_t* hdr,
+                                  const int32_t* offsets, const int32_t* touched,
+                                  const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s) {
+    return launch_e<2>(gate, up, n_experts, inter, hidden, top_k, x,
                        PlanRef{hdr, offsets, touched, pair_of}, epi, act, s);
 }
 
-cudaError_t launch_moe_tc_down(const uint8_t* down_bank, size_t stride, int n_experts, int hidden,
-                               int inter, const float* act, const int32_t* hdr,
-                               const int32_t* offsets, const int32_t* touched,
-                               const int32_t* pair_of, float* o_pairs, cudaStream_t s) {
-    return launch_e<1>(down_bank, down_bank, stride, n_experts, hidden, inter, 1, act,
+cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
+                               const float* act, const int32_t* hdr, const int32_t* offsets,
+                               const int32_t* touched, const int32_t* pair_of, float* o_pairs,
+                               cudaStream_t s) {
+    return launch_e<1>(down, down, n_experts, hidden, inter, 1, act,
                        PlanRef{hdr, offsets, touched, pair_of}, MoeAct{nullptr, 0.0f, 0}, o_pairs,
                        s);
 }

@@ -206,9 +206,12 @@ int mxfp4_moe_gate_up(const void* gate_bank, const void* up_bank, int n_experts,
     MXFP4_TRY(check_ptr(act));
     if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u))
         return MXFP4_STATUS_BAD_POINTER;
-    return from_cuda(mxk::launch_moe_gate_up(u8(gate_bank), u8(up_bank), n_experts, hidden, inter,
-                                             x, n_tokens, top_k, expert_ids, nullptr, n_experts,
-                                             mxk::MoeAct{nullptr, 0.0f, 0}, act, workspace, stream));
+    const size_t stride = mxk::padded_nbytes(inter, hidden);
+    return from_cuda(mxk::launch_moe_gate_up(
+        mxk::one_segment_bank(u8(gate_bank), n_experts, stride),
+        mxk::one_segment_bank(u8(up_bank), n_experts, stride), n_experts, hidden, inter, x,
+        n_tokens, top_k, expert_ids, nullptr, n_experts, mxk::MoeAct{nullptr, 0.0f, 0}, act,
+        workspace, stream));
 }
 
 int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter, const float* act,
@@ -221,8 +224,9 @@ int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter, 
     if (expert_ids == nullptr || (reinterpret_cast<uintptr_t>(expert_ids) & 3u) ||
         route_w == nullptr || (reinterpret_cast<uintptr_t>(route_w) & 3u))
         return MXFP4_STATUS_BAD_POINTER;
-    return from_cuda(mxk::launch_moe_down(u8(down_bank), n_experts, hidden, inter, act, n_tokens,
-                                          top_k, route_w, 0, y, workspace, stream));
+    return from_cuda(mxk::launch_moe_down(
+        mxk::one_segment_bank(u8(down_bank), n_experts, mxk::padded_nbytes(hidden, inter)),
+        n_experts, hidden, inter, act, n_tokens, top_k, route_w, 0, y, workspace, stream));
 }
 
 namespace {
@@ -237,17 +241,35 @@ int check_mode(int mode, float swiglu_limit) {
 
 }  // namespace
 
-int mxfp4_moe_gate_up_ex(const void* gate_bank, const void* up_bank, int n_slots, int hidden,
-                         int inter, const float* x, int n_tokens, int top_k,
-                         const int32_t* expert_ids, const int32_t* slot_of, int n_experts,
-                         const float* route_w, int mode, float swiglu_limit, float* act,
-                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+namespace {
+
+// A bank given as segment base pointers (host array of device pointers).
+int make_bank(const void* const* segs, int n_segments, int segment_slots, size_t stride,
+              mxk::Bank* out) {
+    if (segs == nullptr) return MXFP4_STATUS_BAD_POINTER;
+    if (n_segments < 1 || n_segments > mxk::kMaxSegments || segment_slots < 1)
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    mxk::Bank b{};
+    for (int i = 0; i < n_segments; ++i) {
+        MXFP4_TRY(check_ptr(segs[i]));
+        b.seg[i] = static_cast<const uint8_t*>(segs[i]);
+    }
+    b.n_seg = n_segments;
+    b.seg_slots = segment_slots;
+    b.stride = stride;
+    *out = b;
+    return MXFP4_STATUS_OK;
+}
+
+int gate_up_general(const mxk::Bank& gate, const mxk::Bank& up, int n_slots, int hidden,
+                    int inter, const float* x, int n_tokens, int top_k, const int32_t* expert_ids,
+                    const int32_t* slot_of, int n_experts, const float* route_w, int mode,
+                    float swiglu_limit, float* act, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream) {
     MXFP4_TRY(check_moe(n_slots, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
     MXFP4_TRY(check_mode(mode, swiglu_limit));
     if (n_experts < 1 || n_experts > (1 << 24)) return MXFP4_STATUS_INVALID_ARGUMENT;
     if (slot_of == nullptr && n_experts != n_slots) return MXFP4_STATUS_INVALID_ARGUMENT;
-    MXFP4_TRY(check_ptr(gate_bank));
-    MXFP4_TRY(check_ptr(up_bank));
     MXFP4_TRY(check_ptr(x));
     MXFP4_TRY(check_ptr(act));
     if (!ptr4(expert_ids) || (slot_of != nullptr && !ptr4(slot_of)) ||
@@ -255,23 +277,85 @@ int mxfp4_moe_gate_up_ex(const void* gate_bank, const void* up_bank, int n_slots
         return MXFP4_STATUS_BAD_POINTER;
     const mxk::MoeAct epi{route_w, swiglu_limit > 0.0f ? swiglu_limit : 0.0f,
                           mode == MXFP4_MOE_MODE_V41 ? 1 : 0};
-    return from_cuda(mxk::launch_moe_gate_up(u8(gate_bank), u8(up_bank), n_slots, hidden, inter,
-                                             x, n_tokens, top_k, expert_ids, slot_of, n_experts,
-                                             epi, act, workspace, stream));
+    return from_cuda(mxk::launch_moe_gate_up(gate, up, n_slots, hidden, inter, x, n_tokens, top_k,
+                                             expert_ids, slot_of, n_experts, epi, act, workspace,
+                                             stream));
+}
+
+int down_general(const mxk::Bank& down, int n_slots, int hidden, int inter, const float* act,
+                 int n_tokens, int top_k, const float* route_w, int mode, float* y,
+                 void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_moe(n_slots, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
+    MXFP4_TRY(check_mode(mode, 0.0f));
+    MXFP4_TRY(check_ptr(act));
+    MXFP4_TRY(check_ptr(y));
+    if (mode == MXFP4_MOE_MODE_F32 && !ptr4(route_w)) return MXFP4_STATUS_BAD_POINTER;
+    return from_cuda(mxk::launch_moe_down(down, n_slots, hidden, inter, act, n_tokens, top_k,
+                                          route_w, mode == MXFP4_MOE_MODE_V41 ? 1 : 0, y,
+                                          workspace, stream));
+}
+
+}  // namespace
+
+int mxfp4_moe_gate_up_ex(const void* gate_bank, const void* up_bank, int n_slots, int hidden,
+                         int inter, const float* x, int n_tokens, int top_k,
+                         const int32_t* expert_ids, const int32_t* slot_of, int n_experts,
+                         const float* route_w, int mode, float swiglu_limit, float* act,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    MXFP4_TRY(check_ptr(gate_bank));
+    MXFP4_TRY(check_ptr(up_bank));
+    MXFP4_TRY(check_shape(inter, hidden));
+    if (n_slots < 1) return MXFP4_STATUS_INVALID_ARGUMENT;
+    const size_t stride = mxk::padded_nbytes(inter, hidden);
+    return gate_up_general(mxk::one_segment_bank(u8(gate_bank), n_slots, stride),
+                           mxk::one_segment_bank(u8(up_bank), n_slots, stride), n_slots, hidden,
+                           inter, x, n_tokens, top_k, expert_ids, slot_of, n_experts, route_w,
+                           mode, swiglu_limit, act, workspace, ws_bytes, stream);
 }
 
 int mxfp4_moe_down_ex(const void* down_bank, int n_slots, int hidden, int inter, const float* act,
                       int n_tokens, int top_k, const float* route_w, int mode, float* y,
                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    MXFP4_TRY(check_moe(n_slots, hidden, inter, n_tokens, top_k, workspace, ws_bytes));
-    MXFP4_TRY(check_mode(mode, 0.0f));
     MXFP4_TRY(check_ptr(down_bank));
-    MXFP4_TRY(check_ptr(act));
-    MXFP4_TRY(check_ptr(y));
-    if (mode == MXFP4_MOE_MODE_F32 && !ptr4(route_w)) return MXFP4_STATUS_BAD_POINTER;
-    return from_cuda(mxk::launch_moe_down(u8(down_bank), n_slots, hidden, inter, act, n_tokens,
-                                          top_k, route_w, mode == MXFP4_MOE_MODE_V41 ? 1 : 0, y,
-                                          workspace, stream));
+    MXFP4_TRY(check_shape(hidden, inter));
+    if (n_slots < 1) return MXFP4_STATUS_INVALID_ARGUMENT;
+    return down_general(
+        mxk::one_segment_bank(u8(down_bank), n_slots, mxk::padded_nbytes(hidden, inter)), n_slots,
+        hidden, inter, act, n_tokens, top_k, route_w, mode, y, workspace, ws_bytes, stream);
+}
+
+int mxfp4_moe_gate_up_seg(const void* const* gate_segments, const void* const* up_segments,
+                          int n_segments, int segment_slots, int hidden, int inter, const float* x,
+                          int n_tokens, int top_k, const int32_t* expert_ids,
+                          const int32_t* slot_of, int n_experts, const float* route_w, int mode,
+                          float swiglu_limit, float* act, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
+    MXFP4_TRY(check_shape(inter, hidden));
+    if (segment_slots < 1 || n_segments < 1 || n_segments > mxk::kMaxSegments ||
+        static_cast<long long>(n_segments) * segment_slots > (1 << 20))
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    const size_t stride = mxk::padded_nbytes(inter, hidden);
+    mxk::Bank gate{}, up{};
+    MXFP4_TRY(make_bank(gate_segments, n_segments, segment_slots, stride, &gate));
+    MXFP4_TRY(make_bank(up_segments, n_segments, segment_slots, stride, &up));
+    return gate_up_general(gate, up, n_segments * segment_slots, hidden, inter, x, n_tokens, top_k,
+                           expert_ids, slot_of, n_experts, route_w, mode, swiglu_limit, act,
+                           workspace, ws_bytes, stream);
+}
+
+int mxfp4_moe_down_seg(const void* const* down_segments, int n_segments, int segment_slots,
+                       int hidden, int inter, const float* act, int n_tokens, int top_k,
+                       const float* route_w, int mode, float* y, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream) {
+    MXFP4_TRY(check_shape(hidden, inter));
+    if (segment_slots < 1 || n_segments < 1 || n_segments > mxk::kMaxSegments ||
+        static_cast<long long>(n_segments) * segment_slots > (1 << 20))
+        return MXFP4_STATUS_INVALID_ARGUMENT;
+    mxk::Bank down{};
+    MXFP4_TRY(make_bank(down_segments, n_segments, segment_slots,
+                        mxk::padded_nbytes(hidden, inter), &down));
+    return down_general(down, n_segments * segment_slots, hidden, inter, act, n_tokens, top_k,
+                        route_w, mode, y, workspace, ws_bytes, stream);
 }
 
 int mxfp4_moe_cold_pairs(const void* workspace, size_t ws_bytes, int n_slots, int n_tokens,

@@ -172,3 +172,46 @@ def test_ex_refusals(mx):
     # the V4.1 mode needs the route weights in the gate/up pass
     assert lib.mxfp4_moe_gate_up_ex(A, A, 8, 64, 64, A, 2, 2, A, None, 8, None, 1, 0.0, A, A,
                                     1 << 20, None) == 2
+
+
+@pytest.mark.parametrize("n_seg,seg_slots,where", [
+    (3, 2, [0, 1, 2, 3, 4]),            # five experts over segments 0, 0, 1, 1, 2
+    (16, 2, [1, 3, 5, 7, 31]),          # sixteen segments, local index 1 of each
+    (4, 3, [11, 2, 6, 9, 0]),           # any slot order
+])
+def test_segmented_bank_equals_the_one_buffer_bank(mx, n_seg, seg_slots, where):
+    # each segment its own device buffer; expert e in slot where[e] (slot_of):
+    # the result is the one-buffer bank's, bit for bit, in both passes and both
+    # kernel families (128 groups per row: tensor cores; 144: the FP32 passes)
+    import torch
+    for hidden in (256, 4608):
+        cfg = synth.MoeConfig("seg", 5, hidden, 64, 6, 3, 49, scale_lo=113, scale_hi=121)
+        gate, up, down = cfg.banks()
+        x = cfg.activations()
+        ids, wts = cfg.routes()
+        y_ref, _, _ = run_ex(mx, cfg, gate, up, down, x, ids, wts, V41, 0.5)
+        n_slots = n_seg * seg_slots
+        slot_of = np.array(where, dtype=np.int32)
+
+        def segments(bank, stride):
+            out = [torch.zeros(seg_slots * stride, dtype=torch.uint8, device="cuda:0")
+                   for _ in range(n_seg)]
+            for e, s in enumerate(where):
+                out[s // seg_slots][(s % seg_slots) * stride:(s % seg_slots + 1) * stride] = \
+                    to_dev(bank[e * stride:(e + 1) * stride])
+            return out
+
+        gs, us = segments(gate, cfg.gu_stride), segments(up, cfg.gu_stride)
+        ds = segments(down, cfg.down_stride)
+        T, K = ids.shape
+        nbytes = mx.mxfp4_moe_workspace_bytes(n_slots, T, K, hidden, 64)
+        ws = empty(nbytes // 4 + 4)
+        act = empty(T * K * 64)
+        y = empty(T * hidden)
+        w_d = to_dev(wts)
+        mx.mxfp4_moe_gate_up_seg(gs, us, seg_slots, hidden, 64, to_dev(x), T, K, to_dev(ids), act,
+                                 ws, slot_of=to_dev(slot_of), n_experts=5, route_w=w_d, mode=V41,
+                                 swiglu_limit=0.5)
+        mx.mxfp4_moe_down_seg(ds, seg_slots, hidden, 64, act, T, K, y, ws, route_w=w_d, mode=V41)
+        got = host(y).reshape(T, hidden)
+        assert np.array_equal(got.view(np.uint32), y_ref.view(np.uint32)), (hidden, where)
