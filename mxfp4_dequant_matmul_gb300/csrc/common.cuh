@@ -221,6 +221,20 @@ __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
                  : "memory");
 }
 
+// Two 8 x 16-byte matrices: lane (g, t) gets word t of row g of matrix i in
+// r_i; lanes 8i .. 8i + 7 give the row addresses of matrix i.
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(a)
+                 : "memory");
+}
+
+// One arrival on an mbarrier (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive_m(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -60,12 +60,15 @@ namespace {
 constexpr int kWarpsM = 16;
 constexpr int kThreadsM = kWarpsM * 32;
 // The CTA's tasks are always split into 16 ranges: the ranges fix the order of
-// every sum.  Up to four tokens, each of 16 warps takes one range; eight tokens
-// need twice the activation fragments in shared memory and twice the
-// accumulators, so 8 warps take two consecutive ranges each (the same sums in
-// the same order, so a token's result does not depend on the token count).
+// every sum.  Up to four tokens, each of the 16 warps takes one range with a
+// ring of its own.  Eight tokens need twice the activation fragments in shared
+// memory, so there is room for only 8 rings: the warps work in pairs, a pair
+// taking two consecutive ranges in turn through one ring, each warp of the
+// pair the 16-row half of every unit.  Every row's sums are the same in the
+// same order either way, so a token's result does not depend on the token
+// count.
 constexpr int kRangesM = 16;
-__host__ __device__ constexpr int warps_mv(int NT) { return NT == 8 ? 8 : kWarpsM; }
+__host__ __device__ constexpr int rings_mv(int NT) { return NT == 8 ? 8 : kWarpsM; }
 constexpr int kRowsU = 32;                  // rows per unit (two MMA row blocks)
 constexpr int kChunkM = 8;                  // groups per unit (128 code bytes per row)
 constexpr int kStageM = kRowsU * 128;       // one TMA tile, 4 KB
@@ -137,14 +140,14 @@ __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, in
     // the lanes that hold none
     l.fin = l.part + static_cast<uint32_t>(kRangesM + ru_cta - 1) * kRowsU * NT * 4;
     l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[8], tmax[8], flag
-    l.bars = (l.misc + 80 + 7u) & ~7u;
-    l.ring = (l.bars + warps_mv(NT) * kMaxStagesM * 8 + 1023u) & ~1023u;
-    l.total = l.ring + static_cast<uint32_t>(warps_mv(NT) * stages) * kStageM + 1024;   // + align slack
+    l.bars = (l.misc + 80 + 7u) & ~7u;   // [full, empty][rings][kMaxStagesM]
+    l.ring = (l.bars + 2 * kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
+    l.total = l.ring + static_cast<uint32_t>(rings_mv(NT) * stages) * kStageM + 1024;   // + align slack
     return l;
 }
 
 template <int NT, int CL>
-__global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
+__global__ void __launch_bounds__(kThreadsM, 1)
     k_mv_tc(const __grid_constant__ CUtensorMap tmap, const uint8_t* __restrict__ w, int rows,
             int cols, const float* __restrict__ X, int nb, float* __restrict__ Y, int ru_cta,
             int ng_max, int stages, int overlap) {
@@ -157,13 +160,18 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     uint8_t* sc_s = smem + L.sc;
     float* part = reinterpret_cast<float*>(smem + L.part);
     float* fin = reinterpret_cast<float*>(smem + L.fin);
-    constexpr int kW = warps_mv(NT), kThr = kW * 32, kRpw = kRangesM / kW;
+    constexpr int kThr = kThreadsM;
+    constexpr bool kPaired = NT == 8;                   // two warps per ring
+    constexpr int kRpw = kRangesM / rings_mv(NT);       // ranges per ring
     int* pexp = reinterpret_cast<int*>(smem + L.misc);                 // [8]
     unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 32);  // [8]
     int* not_plain = reinterpret_cast<int*>(smem + L.misc + 64);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int owner = kPaired ? warp >> 1 : warp;        // the ring this warp reads
+    const int half = kPaired ? warp & 1 : 0;            // its 16-row half of a unit (pairs)
+    const bool issuer = lane == 0 && half == 0;         // starts the ring's copies
     const uint32_t rank = CL > 1 ? cluster_rank_m() : 0u;
     const int range = blockIdx.x / CL;
     const int t0 = blockIdx.y * NT;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     // sums become the piece of its range for a row unit (slot range + row unit)
     // whenever its range leaves the unit or ends.
     const int n_tasks = n_ru * n_c;
-    const int rg0 = kRpw > 1 ? warp * kRpw
+    const int rg0 = kRpw > 1 ? owner * kRpw
                              : (n_tasks % kRangesM == 0 ? warp
                                                         : (warp & 3) * (kRangesM / 4) + (warp >> 2));
     const int t_lo = rg0 * n_tasks / kRangesM;
@@ -196,8 +204,9 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     int rg = rg0;                                          // the range of the current unit
     int rg_end = (rg0 + 1) * n_tasks / kRangesM;           // its end (a task index)
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * stages;
-    uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * stages * kStageM;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars) + owner * kMaxStagesM;
+    uint64_t* empty = bars + kWarpsM * kMaxStagesM;      // (pairs) both warps done with a stage
+    uint8_t* ring = smem + L.ring + static_cast<size_t>(owner) * stages * kStageM;
     const uint64_t policy = l2_evict_first();
     // the unit of row unit ru, chunk c into stage st (lane 0)
     auto issue_rc = [&](int ru, int c, int st) {
@@ -244,10 +253,13 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     // weights, which that kernel does not write, start at once, and x (which
     // it may write) is read only once it has completed.
     // (unit k goes to stage k: never more units than the ring has stages)
-    auto start_weights = [&](int k0, int k1) {   // this warp's units k0 .. k1-1
-        if (lane == 0) {
+    auto start_weights = [&](int k0, int k1) {   // this ring's units k0 .. k1-1
+        if (issuer) {
             if (k0 == 0) {
-                for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+                for (int st = 0; st < stages; ++st) {
+                    mbar_init(&bars[st], 1);
+                    if (kPaired) mbar_init(&empty[st], 2);
+                }
                 fence_mbar_init();
             }
             for (int k = k0; k < k1 && k < stages && k < n_units; ++k) {
@@ -422,13 +434,16 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     constexpr int NS = NT == 8 ? 2 : 1;
     constexpr int NTS = NT / NS;   // tokens per column set
     constexpr int GP = 4 / NTS;    // groups sharing one accumulator
+    constexpr int RQ = kPaired ? 2 : 4;   // rows per lane in a unit: g + 8q (+ 16 half)
     const int slot = t / NTS, tk = t % NTS;   // D columns 2t, 2t + 1: group slot, token in set
-    // acc[s][q][i]: row g + 8q, token s NTS + tk, sum r = slot + GP i (groups j, j mod 4 = r)
-    float acc[NS][4][NTS];
+    const int rbase = 16 * half;              // this warp's first row in a unit
+    // acc[s][q][i]: row rbase + g + 8q, token s NTS + tk, sum r = slot + GP i
+    // (groups j, j mod 4 = r)
+    float acc[NS][RQ][NTS];
 #pragma unroll
     for (int s = 0; s < NS; ++s)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < RQ; ++q)
 #pragma unroll
             for (int i = 0; i < NTS; ++i) acc[s][q][i] = 0.0f;
     // hi + lo of a group carries the factor 2^p: undone before the scale, so
@@ -456,7 +471,7 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < RQ; ++q) {
                 float p[4];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
@@ -465,7 +480,8 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
                 float v = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), p[2]), p[3]);
                 // back from the 2^p domain (exact: a power of two, no overflow)
                 if (plain[s]) v = __fmul_rn(v, pinv[s]);
-                if (t < NTS) pw[(g + 8 * q) * NT + s * NTS + t] = v;   // lane (g, t): token t of set s
+                if (t < NTS)   // lane (g, t): token t of set s
+                    pw[(rbase + g + 8 * q) * NT + s * NTS + t] = v;
 #pragma unroll
                 for (int i = 0; i < NTS; ++i) acc[s][q][i] = 0.0f;
             }
@@ -486,7 +502,7 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
             ++u_ru;
         }
         if (kRpw > 1) {
-            // the unit starts the warp's next range: the last range's piece is done
+            // the unit starts the ring's next range: the last range's piece is done
             while (t_lo + k >= rg_end) {
                 if (cur_ru >= 0) flush(cur_ru);
                 cur_ru = -1;
@@ -497,21 +513,23 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
         if (ru != cur_ru) {
             if (cur_ru >= 0) flush(cur_ru);
             cur_ru = ru;
-            scr = sc_s + static_cast<size_t>(ru * kRowsU + g) * L.sc_pitch;
+            scr = sc_s + static_cast<size_t>(ru * kRowsU + rbase + g) * L.sc_pitch;
         }
         if (!mbar_wait(&bars[st], phase, kWaitM)) {
             failed = true;
             break;
         }
         const uint8_t* stg = ring + st * kStageM;
-        // this lane's row (lane) of the tile, chunk 0 after the swizzle; chunk j
-        // is at that address ^ (j << 4) (the tile is 1024-byte aligned)
-        const uint32_t row_addr = smem_u32(stg) + lane * 128 + ((lane & 7) << 4);
+        // this lane's row of the tile (lane, or rbase + lane % 16 for a pair's
+        // half), chunk 0 after the swizzle; chunk j is at that address ^ (j << 4)
+        // (the tile is 1024-byte aligned; rbase is a multiple of 8)
+        const int trow = kPaired ? rbase + (lane & 15) : lane;
+        const uint32_t row_addr = smem_u32(stg) + trow * 128 + ((lane & 7) << 4);
         const int gc0 = chunk * kChunkM;   // first group of the unit in the slice
         const int ngc = min(kChunkM, ng - gc0);
-        uint2 sb[4];   // the unit's 8 scale bytes of rows g, g+8, g+16, g+24
+        uint2 sb[RQ];   // the unit's 8 scale bytes of rows rbase + g + 8q
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < RQ; ++q)
             sb[q] = *reinterpret_cast<const uint2*>(scr + q * 8 * L.sc_pitch + gc0);
 #pragma unroll
         for (int j0 = 0; j0 < kChunkM; j0 += GP) {
@@ -521,15 +539,19 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
                 for (int s = 0; s < GP; ++s) {
                     const int j = j0 + s;
                     if (j < ngc) {
-                        // code word t of rows g, g+8, g+16, g+24 (128-byte swizzle:
-                        // chunk j of row r sits at chunk j ^ (r & 7))
+                        // code word t of the lane's rows (128-byte swizzle: chunk j
+                        // of row r sits at chunk j ^ (r & 7))
                         uint32_t cwd[4];
-                        ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
                         uint32_t h0[4], h1[4], h2[4], h3[4];
+                        if constexpr (kPaired) {
+                            ldsm_x2(row_addr ^ static_cast<uint32_t>(j << 4), cwd[0], cwd[1]);
+                        } else {
+                            ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
+                            e2m1x8_to_f16x2x4(cwd[2], h2);
+                            e2m1x8_to_f16x2x4(cwd[3], h3);
+                        }
                         e2m1x8_to_f16x2x4(cwd[0], h0);
                         e2m1x8_to_f16x2x4(cwd[1], h1);
-                        e2m1x8_to_f16x2x4(cwd[2], h2);
-                        e2m1x8_to_f16x2x4(cwd[3], h3);
 #pragma unroll
                         for (int c = 0; c < NS; ++c) {
                             const uint4 b = lds128(
@@ -538,13 +560,13 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
                                             : zero_lane);
                             if (s == 0) {
                                 mma16816_z(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                                mma16816_z(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                                if (!kPaired) mma16816_z(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
                             } else {
                                 mma16816(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                                mma16816(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                                if (!kPaired) mma16816(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
                             }
                             mma16816(d0[c], h0[2], h1[2], h0[3], h1[3], b.z, b.w);
-                            mma16816(d1[c], h2[2], h3[2], h2[3], h3[3], b.z, b.w);
+                            if (!kPaired) mma16816(d1[c], h2[2], h3[2], h2[3], h3[3], b.z, b.w);
                         }
                     }
                 }
@@ -552,17 +574,22 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
                 // word j0 / 4 of the unit's bytes)
                 if (j0 + slot < ngc) {
                     const uint32_t sel = sel0 + (static_cast<uint32_t>(j0 & 3) << 8);
-                    const uint32_t w0 = j0 < 4 ? sb[0].x : sb[0].y, w1 = j0 < 4 ? sb[1].x : sb[1].y;
-                    const uint32_t w2 = j0 < 4 ? sb[2].x : sb[2].y, w3 = j0 < 4 ? sb[3].x : sb[3].y;
-                    const uint32_t kw[4] = {__byte_perm(w0, 0u, sel), __byte_perm(w1, 0u, sel),
-                                            __byte_perm(w2, 0u, sel), __byte_perm(w3, 0u, sel)};
+                    uint32_t kw[RQ];
+#pragma unroll
+                    for (int q = 0; q < RQ; ++q)
+                        kw[q] = __byte_perm(j0 < 4 ? sb[q].x : sb[q].y, 0u, sel);
                     const int i_acc = (j0 / GP) % NTS;   // r = (j0 + slot) mod 4 = slot + GP i
 #pragma unroll
                     for (int c = 0; c < NS; ++c) {
-                        const float v[4] = {__fadd_rn(d0[c][0], d0[c][1]), __fadd_rn(d0[c][2], d0[c][3]),
-                                            __fadd_rn(d1[c][0], d1[c][1]), __fadd_rn(d1[c][2], d1[c][3])};
+                        float v[RQ];
+                        v[0] = __fadd_rn(d0[c][0], d0[c][1]);
+                        v[1] = __fadd_rn(d0[c][2], d0[c][3]);
+                        if constexpr (RQ == 4) {
+                            v[RQ - 2] = __fadd_rn(d1[c][0], d1[c][1]);
+                            v[RQ - 1] = __fadd_rn(d1[c][2], d1[c][3]);
+                        }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < RQ; ++q) {
                             if (plain[c])   // the sums stay in the 2^p domain; 2^(k-127) from its bits
                                 acc[c][q][i_acc] =
                                     __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[c][q][i_acc]);
@@ -575,7 +602,23 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
             }
         }
         __syncwarp();   // every lane is done with the stage
-        if (lane == 0 && k + stages < n_units) {
+        if constexpr (kPaired) {
+            // the stage is free once both warps of the pair are done with it
+            if (lane == 0) mbar_arrive_m(&empty[st]);
+            if (issuer && k + stages < n_units) {
+                if (!mbar_wait(&empty[st], phase, kWaitM)) {
+                    failed = true;
+                } else {
+                    fence_proxy_async_smem();
+                    issue_rc(i_ru, i_c, st);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, failed ? 1 : 0, 0)) break;
+            if (k + stages < n_units && ++i_c == n_c) {
+                i_c = 0;
+                ++i_ru;
+            }
+        } else if (lane == 0 && k + stages < n_units) {
             fence_proxy_async_smem();
             issue_rc(i_ru, i_c, st);
             if (++i_c == n_c) {
@@ -590,9 +633,10 @@ __global__ void __launch_bounds__(warps_mv(NT) * 32, 1)
     }
     if (failed) {
         if (lane == 0) atomicOr(&g_fault_mvtc, 1);
-        // let this warp's copies in flight land before the CTA can exit
-        for (int kq = k; kq < k + stages && kq < n_units; ++kq)
-            mbar_wait(&bars[kq % stages], static_cast<uint32_t>(kq / stages) & 1u, kWaitM);
+        // let this ring's copies in flight land before the CTA can exit
+        if (issuer)
+            for (int kq = k; kq < k + stages && kq < n_units; ++kq)
+                mbar_wait(&bars[kq % stages], static_cast<uint32_t>(kq / stages) & 1u, kWaitM);
     }
     if (cur_ru >= 0) flush(cur_ru);
     __syncthreads();
@@ -721,7 +765,7 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     // weight bytes in flight; the arithmetic does not depend on the depth)
     const uint32_t fixed = mv_layout(NT, ng_max, ru_cta, 0).total;
     int stages = fixed < kSmemMaxM
-                     ? static_cast<int>((kSmemMaxM - fixed) / (warps_mv(NT) * kStageM)) : 0;
+                     ? static_cast<int>((kSmemMaxM - fixed) / (rings_mv(NT) * kStageM)) : 0;
     stages = stages > kMaxStagesM ? kMaxStagesM : stages;
     if (stages < kMinStagesM) return cudaErrorNotSupported;
     const MvLayout l = mv_layout(NT, ng_max, ru_cta, stages);
@@ -739,7 +783,7 @@ cudaError_t launch_mv(const uint8_t* w, int rows, int cols, const float* X, int 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ranges * CL),
                        static_cast<unsigned>((nb + NT - 1) / NT));
-    cfg.blockDim = dim3(static_cast<unsigned>(warps_mv(NT) * 32));
+    cfg.blockDim = dim3(kThreadsM);
     cfg.dynamicSmemBytes = l.total;
     cfg.stream = s;
     const int overlap = launch_overlap() ? 1 : 0;
