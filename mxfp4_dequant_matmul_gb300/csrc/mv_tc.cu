@@ -327,6 +327,17 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         }
     }
     start_weights(overlap ? kPreStagesM : 0, stages);   // after the prologue's loads
+    // the ring's later units: fetched into L2 now, so that their ring loads,
+    // issued as stages free up, find them there
+    if (!kPaired && issuer)   // (eight tokens: measured slower with it)
+        for (int k = stages; k < n_units; ++k) {
+            const int task = t_lo + k, ru = task / n_c;
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                             &tmap),
+                         "r"((g_lo + (task - ru * n_c) * kChunkM) * kGroupBytes),
+                         "r"(row0 + ru * kRowsU)
+                         : "memory");
+        }
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
     __syncthreads();   // tmax is zero before any atomic below
     // "plain" scales: no byte 0 or 255 and none above kPlainMax, so that 2^(k-127)
