@@ -46,6 +46,7 @@
 #include <cstdint>
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -469,6 +470,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         pinv[s] = exp2i_m(-p_t);
         plain[s] = *not_plain == 0 && p_t >= 0;
     }
+    // every lane's tokens in the 2^p domain (the usual case): a warp-uniform flag
+    const bool all_plain = __all_sync(0xffffffffu, plain[0] && plain[NS - 1]) != 0;
     // B: lanes 8 NTS s .. 8 NTS s + 8 NTS - 1 hold the fragment of group slot s;
     // column set s of eight tokens is 512 bytes further
     const int b_slot = lane / (8 * NTS);
@@ -542,76 +545,87 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
         for (int q = 0; q < RQ; ++q)
             sb[q] = *reinterpret_cast<const uint2*>(scr + q * 8 * L.sc_pitch + gc0);
+        // B fragments of the unit's first group (column set c and group j at
+        // immediate offsets from it)
+        const uint32_t xb = xf_lane + static_cast<uint32_t>(gc0) * (128 * NT);
+        // the unit's groups; FAST: a whole unit (8 groups) and every lane's token
+        // in the 2^p domain, so that no guard and no table path is needed (the
+        // same arithmetic as the general form for such units)
+        auto run_unit = [&](auto fast_c) {
+            constexpr bool FAST = decltype(fast_c)::value;
 #pragma unroll
-        for (int j0 = 0; j0 < kChunkM; j0 += GP) {
-            if (j0 < ngc) {
-                float d0[NS][4], d1[NS][4];   // per column set: rows g, g+8 and g+16, g+24
+            for (int j0 = 0; j0 < kChunkM; j0 += GP) {
+                if (FAST || j0 < ngc) {
+                    float d0[NS][4], d1[NS][4];   // per column set: rows g, g+8 and g+16, g+24
 #pragma unroll
-                for (int s = 0; s < GP; ++s) {
-                    const int j = j0 + s;
-                    if (j < ngc) {
-                        // code word t of the lane's rows (128-byte swizzle: chunk j
-                        // of row r sits at chunk j ^ (r & 7))
-                        uint32_t cwd[4];
-                        uint32_t h0[4], h1[4], h2[4], h3[4];
-                        if constexpr (kPaired) {
-                            ldsm_x2(row_addr ^ static_cast<uint32_t>(j << 4), cwd[0], cwd[1]);
-                        } else {
-                            ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
-                            e2m1x8_to_f16x2x4(cwd[2], h2);
-                            e2m1x8_to_f16x2x4(cwd[3], h3);
-                        }
-                        e2m1x8_to_f16x2x4(cwd[0], h0);
-                        e2m1x8_to_f16x2x4(cwd[1], h1);
-#pragma unroll
-                        for (int c = 0; c < NS; ++c) {
-                            const uint4 b = lds128(
-                                b_slot == s ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * NT) +
-                                                  static_cast<uint32_t>(c) * 512u
-                                            : zero_lane);
-                            if (s == 0) {
-                                mma16816_z(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                                if (!kPaired) mma16816_z(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                    for (int s = 0; s < GP; ++s) {
+                        const int j = j0 + s;
+                        if (FAST || j < ngc) {
+                            // code word t of the lane's rows (128-byte swizzle: chunk j
+                            // of row r sits at chunk j ^ (r & 7))
+                            uint32_t cwd[4];
+                            uint32_t h0[4], h1[4], h2[4], h3[4];
+                            if constexpr (kPaired) {
+                                ldsm_x2(row_addr ^ static_cast<uint32_t>(j << 4), cwd[0], cwd[1]);
                             } else {
-                                mma16816(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
-                                if (!kPaired) mma16816(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                                ldsm_x4(row_addr ^ static_cast<uint32_t>(j << 4), cwd);
+                                e2m1x8_to_f16x2x4(cwd[2], h2);
+                                e2m1x8_to_f16x2x4(cwd[3], h3);
                             }
-                            mma16816(d0[c], h0[2], h1[2], h0[3], h1[3], b.z, b.w);
-                            if (!kPaired) mma16816(d1[c], h2[2], h3[2], h2[3], h3[3], b.z, b.w);
+                            e2m1x8_to_f16x2x4(cwd[0], h0);
+                            e2m1x8_to_f16x2x4(cwd[1], h1);
+#pragma unroll
+                            for (int c = 0; c < NS; ++c) {
+                                const uint32_t ba = xb + static_cast<uint32_t>(j * (128 * NT) + c * 512);
+                                const uint4 b = lds128(GP == 1 || b_slot == s ? ba : zero_lane);
+                                if (s == 0) {
+                                    mma16816_z(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                                    if (!kPaired) mma16816_z(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                                } else {
+                                    mma16816(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
+                                    if (!kPaired) mma16816(d1[c], h2[0], h3[0], h2[1], h3[1], b.x, b.y);
+                                }
+                                mma16816(d0[c], h0[2], h1[2], h0[3], h1[3], b.z, b.w);
+                                if (!kPaired) mma16816(d1[c], h2[2], h3[2], h2[3], h3[3], b.z, b.w);
+                            }
                         }
                     }
-                }
-                // this lane's group: j0 + slot (its scale byte: byte (j0 & 3) + slot of
-                // word j0 / 4 of the unit's bytes)
-                if (j0 + slot < ngc) {
-                    const uint32_t sel = sel0 + (static_cast<uint32_t>(j0 & 3) << 8);
-                    uint32_t kw[RQ];
+                    // this lane's group: j0 + slot (its scale byte: byte (j0 & 3) + slot of
+                    // word j0 / 4 of the unit's bytes)
+                    if (FAST || j0 + slot < ngc) {
+                        const uint32_t sel = sel0 + (static_cast<uint32_t>(j0 & 3) << 8);
+                        uint32_t kw[RQ];
 #pragma unroll
-                    for (int q = 0; q < RQ; ++q)
-                        kw[q] = __byte_perm(j0 < 4 ? sb[q].x : sb[q].y, 0u, sel);
-                    const int i_acc = (j0 / GP) % NTS;   // r = (j0 + slot) mod 4 = slot + GP i
+                        for (int q = 0; q < RQ; ++q)
+                            kw[q] = __byte_perm(j0 < 4 ? sb[q].x : sb[q].y, 0u, sel);
+                        const int i_acc = (j0 / GP) % NTS;   // r = (j0 + slot) mod 4 = slot + GP i
 #pragma unroll
-                    for (int c = 0; c < NS; ++c) {
-                        float v[RQ];
-                        v[0] = __fadd_rn(d0[c][0], d0[c][1]);
-                        v[1] = __fadd_rn(d0[c][2], d0[c][3]);
-                        if constexpr (RQ == 4) {
-                            v[RQ - 2] = __fadd_rn(d1[c][0], d1[c][1]);
-                            v[RQ - 1] = __fadd_rn(d1[c][2], d1[c][3]);
-                        }
+                        for (int c = 0; c < NS; ++c) {
+                            float v[RQ];
+                            v[0] = __fadd_rn(d0[c][0], d0[c][1]);
+                            v[1] = __fadd_rn(d0[c][2], d0[c][3]);
+                            if constexpr (RQ == 4) {
+                                v[RQ - 2] = __fadd_rn(d1[c][0], d1[c][1]);
+                                v[RQ - 1] = __fadd_rn(d1[c][2], d1[c][3]);
+                            }
 #pragma unroll
-                        for (int q = 0; q < RQ; ++q) {
-                            if (plain[c])   // the sums stay in the 2^p domain; 2^(k-127) from its bits
-                                acc[c][q][i_acc] =
-                                    __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[c][q][i_acc]);
-                            else            // any byte: the table, and 2^-p applied first
-                                acc[c][q][i_acc] = __fmaf_rn(lut[kw[q] >> 16],
-                                                             __fmul_rn(v[q], pinv[c]), acc[c][q][i_acc]);
+                            for (int q = 0; q < RQ; ++q) {
+                                if (FAST || plain[c])   // the sums stay in the 2^p domain; 2^(k-127) from its bits
+                                    acc[c][q][i_acc] =
+                                        __fmaf_rn(__uint_as_float(kw[q] << 7), v[q], acc[c][q][i_acc]);
+                                else                    // any byte: the table, and 2^-p applied first
+                                    acc[c][q][i_acc] = __fmaf_rn(
+                                        lut[kw[q] >> 16], __fmul_rn(v[q], pinv[c]), acc[c][q][i_acc]);
+                            }
                         }
                     }
                 }
             }
-        }
+        };
+        if (all_plain && ngc == kChunkM)
+            run_unit(std::true_type{});
+        else
+            run_unit(std::false_type{});
         __syncwarp();   // every lane is done with the stage
         if constexpr (kPaired) {
             // the stage is free once both warps of the pair are done with it
