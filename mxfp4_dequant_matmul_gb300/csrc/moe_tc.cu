@@ -93,8 +93,8 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;                             // pexp, tmax, pairs, lead, 16 zeros
-    l.segst = l.misc + 80;                                            // [touched + 1] int
+    l.misc = l.lut + 1024;                   // pexp, tmax, pairs, lead, 16 zeros, odd flag
+    l.segst = l.misc + 96;                                            // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
     l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
     l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2 buffers][2 matrices]
     const uint32_t zero16 = smem_u32(smem + L.misc + 64);               // 16 zero bytes
     int* segst = reinterpret_cast<int*>(smem + L.segst);
+    int* seg_odd = reinterpret_cast<int*>(smem + L.misc + 80);          // a segment's odd byte
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
     uint64_t* ring_bars = sbar + 2;
 
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             tmax[tid] = 0u;
             spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
         }
+        if (tid == 0) *seg_odd = 0;
         __syncthreads();
         // column sets of this segment: NP >= its pairs
         const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
@@ -335,8 +337,36 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             failed = true;
         } else {
             if (tid == 0) sc_pend = -1;
+            // "plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits
+            // k << 23 and the rows' sums may stay in the 2^p domain (|sum| below
+            // 128*32 * 6 * 2^(200-127) * 2^15): any other byte of the segment sends
+            // it through the table and 2^-p per group
+            bool odd = false;
+            for (int mm = 0; mm < NM; ++mm) {
+                const uint8_t* sbuf = smem + L.sc + (bi * NM + mm) * L.sc_bytes;
+                const int lo = lead[bi * 2 + mm], hi = lo + cur.nrow * gpr;
+                for (int c = tid; 16 * c < hi; c += kThreadsE) {
+                    const int b0 = 16 * c;
+                    if (b0 + 16 <= lo) continue;
+                    if (b0 >= lo && b0 + 16 <= hi) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(sbuf + b0);
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            odd |= (__vcmpeq4(wv[q], 0u) | __vcmpgtu4(wv[q], 200u * 0x01010101u)) != 0u;
+                    } else {
+                        for (int b = max(b0, lo); b < min(b0 + 16, hi); ++b)
+                            odd |= sbuf[b] == 0 || sbuf[b] > 200;
+                    }
+                }
+            }
+            if (odd) atomicOr(seg_odd, 1);
         }
         failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
+        // the whole segment in the 2^p domain: no odd scale byte, every pair's p >= 0
+        bool fast = *seg_odd == 0;
+#pragma unroll
+        for (int q = 0; q < kTokSeg; ++q) fast = fast && pexp[q] >= 0;
 
         // --- this warp's units
         float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24, this lane's groups
@@ -347,9 +377,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * np)) * 16;
         const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
         // the groups of a unit, GP to an accumulator
-        auto unit_groups = [&](auto gp_c, uint32_t row_addr, int gc0, int ngc,
+        auto unit_groups = [&](auto gp_c, auto fast_c, uint32_t row_addr, int gc0, int ngc,
                                const uint32_t (&sb)[4][2]) {
             constexpr int GP = decltype(gp_c)::value;
+            constexpr bool FAST = decltype(fast_c)::value;
 #pragma unroll
             for (int j0 = 0; j0 < kChunkE; j0 += GP) {
                 if (j0 < ngc) {
@@ -381,15 +412,21 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                     }
                     if (j0 + slot < ngc) {   // this lane's group j0 + slot
                         const int hw = j0 >> 2;
-                        const uint32_t sel = 0x4440u + static_cast<uint32_t>((j0 & 3) + slot);
-                        acc[0] = __fmaf_rn(lut[__byte_perm(sb[0][hw], 0u, sel)],
-                                           __fmul_rn(__fadd_rn(d0[0], d0[1]), pinv), acc[0]);
-                        acc[1] = __fmaf_rn(lut[__byte_perm(sb[1][hw], 0u, sel)],
-                                           __fmul_rn(__fadd_rn(d0[2], d0[3]), pinv), acc[1]);
-                        acc[2] = __fmaf_rn(lut[__byte_perm(sb[2][hw], 0u, sel)],
-                                           __fmul_rn(__fadd_rn(d1[0], d1[1]), pinv), acc[2]);
-                        acc[3] = __fmaf_rn(lut[__byte_perm(sb[3][hw], 0u, sel)],
-                                           __fmul_rn(__fadd_rn(d1[2], d1[3]), pinv), acc[3]);
+                        const float v[4] = {__fadd_rn(d0[0], d0[1]), __fadd_rn(d0[2], d0[3]),
+                                            __fadd_rn(d1[0], d1[1]), __fadd_rn(d1[2], d1[3])};
+                        if constexpr (FAST) {   // 2^(k-127) from its bits; 2^-p at the end
+                            const uint32_t sel = 0x4044u + (static_cast<uint32_t>((j0 & 3) + slot) << 8);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                acc[q] = __fmaf_rn(__uint_as_float(__byte_perm(sb[q][hw], 0u, sel) << 7),
+                                                   v[q], acc[q]);
+                        } else {                // any byte: the table, and 2^-p first
+                            const uint32_t sel = 0x4440u + static_cast<uint32_t>((j0 & 3) + slot);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                acc[q] = __fmaf_rn(lut[__byte_perm(sb[q][hw], 0u, sel)],
+                                                   __fmul_rn(v[q], pinv), acc[q]);
+                        }
                     }
                 }
             }
@@ -418,12 +455,21 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 sb[r4][0] = __funnelshift_r(w0, w1, sh);
                 sb[r4][1] = __funnelshift_r(w1, w2, sh);
             }
-            if (np == 1)
-                unit_groups(std::integral_constant<int, 4>{}, row_addr, gc0, ngc, sb);
-            else if (np == 2)
-                unit_groups(std::integral_constant<int, 2>{}, row_addr, gc0, ngc, sb);
-            else
-                unit_groups(std::integral_constant<int, 1>{}, row_addr, gc0, ngc, sb);
+            if (fast) {
+                if (np == 1)
+                    unit_groups(std::integral_constant<int, 4>{}, std::true_type{}, row_addr, gc0, ngc, sb);
+                else if (np == 2)
+                    unit_groups(std::integral_constant<int, 2>{}, std::true_type{}, row_addr, gc0, ngc, sb);
+                else
+                    unit_groups(std::integral_constant<int, 1>{}, std::true_type{}, row_addr, gc0, ngc, sb);
+            } else {
+                if (np == 1)
+                    unit_groups(std::integral_constant<int, 4>{}, std::false_type{}, row_addr, gc0, ngc, sb);
+                else if (np == 2)
+                    unit_groups(std::integral_constant<int, 2>{}, std::false_type{}, row_addr, gc0, ngc, sb);
+                else
+                    unit_groups(std::integral_constant<int, 1>{}, std::false_type{}, row_addr, gc0, ngc, sb);
+            }
             __syncwarp();   // every lane is done with the stage
             if (lane == 0 && issued < stream_end) {   // refill: this segment's or the next one's
                 fence_proxy_async_smem();
@@ -451,6 +497,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             for (int sl = 1; sl < 4 / np; ++sl)
                 v = __fadd_rn(v, __shfl_sync(0xffffffffu, acc[q], (lane & ~3) | (sl * np + tok)));
             acc[q] = v;
+        }
+        if (fast) {   // back from the 2^p domain (a power of two: exact)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = __fmul_rn(acc[q], pinv);
         }
         if (cur.active && t < np) {   // lane (g, t) has pair t
             float* pw = part + static_cast<size_t>(warp) * kRowsUE * kTokSeg;
