@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 LAYERS = 16
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of k_mv_tc<1,1> on the decode
 # GEMV, from one ncu capture of `bench.py --profile decode` (cold L2, one launch)
-MV_TC_TRAFFIC_BYTES = 31266048
+MV_TC_TRAFFIC_BYTES = 31272704
 REPEATS = 5          # timed regions per workload; the median is reported
 METRIC = "MXFP4 fused dequant-matvec weight GB/s (decode GEMV 14336x4096)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -546,6 +546,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-seconds", type=float, default=1.0,
+                    help="extra seconds of the main step replayed while the clocks are sampled")
     ap.add_argument("--profile",
                     choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm",
                              "dequant"],
@@ -583,8 +585,9 @@ def main():
     sampler.start()
     time.sleep(0.3)
     secs, regions, graph = time_graph(main_w, args.steps, args.warmup, barrier)
-    # keep the same step running ~1 s so the sampler sees the clocks under this load
-    t_end = time.perf_counter() + 1.0
+    # keep the same step running a while (1 s by default) so the sampler sees the
+    # clocks under this load
+    t_end = time.perf_counter() + args.clock_seconds
     while time.perf_counter() < t_end:
         for _ in range(50):
             graph.replay()
