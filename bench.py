@@ -156,16 +156,28 @@ class DecodeGemv(Workload):
         for w, y in zip(self.ws, self.ys):
             self.mx.mxfp4_mv(w, self.rows, self.cols, self.x, y)
 
-    # p2-style host entry: x from pinned host memory, y back to host, per layer
+    # end to end: every step copies x from pinned host memory, runs the layers'
+    # mxfp4_mv calls and reads every layer's y back into pinned host memory, then
+    # waits for the stream (one synchronisation per step)
     def setup_e2e(self):
         import torch
         self.xh = torch.from_numpy(self.x_host.copy()).pin_memory()
         self.yh = [torch.empty(self.rows, dtype=torch.float32).pin_memory() for _ in self.ws]
         self.x_stage = torch.empty(self.cols, dtype=torch.float32, device="cuda")
-        self.h2d = len(self.ws) * 4 * self.cols
+        self.h2d = 4 * self.cols
         self.d2h = len(self.ws) * 4 * self.rows
 
     def step_e2e(self):
+        import torch
+        self.x_stage.copy_(self.xh, non_blocking=True)
+        for w, y in zip(self.ws, self.ys):
+            self.mx.mxfp4_mv(w, self.rows, self.cols, self.x_stage, y)
+        for yh, y in zip(self.yh, self.ys):
+            yh.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    # the page's host entry per layer (fn matmat): x in, y out, a synchronisation each
+    def step_matmat_host(self):
         for w, yh, y in zip(self.ws, self.yh, self.ys):
             self.mx.mxfp4_matmat_host(w, self.rows, self.cols, self.xh, 1, yh, self.x_stage, y)
 
@@ -340,15 +352,16 @@ def time_graph(work: Workload, steps: int, warmup: int, barrier=None, repeats: i
     return statistics.median(regions), regions, g
 
 
-def time_e2e(work, steps: int, warmup: int):
+def time_e2e(work, steps: int, warmup: int, fn=None):
+    """Host wall time of `steps` calls of fn (work.step_e2e by default)."""
     import torch
-    work.setup_e2e()
+    fn = fn or work.step_e2e
     for _ in range(max(warmup, 1)):
-        work.step_e2e()
+        fn()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(steps):
-        work.step_e2e()
+        fn()
     torch.cuda.synchronize()
     return time.perf_counter() - t0
 
@@ -391,7 +404,7 @@ def time_oracle_decode(threads: int, seconds_target: float):
     return n * per_launch / el / 1e9, n, el
 
 
-def time_oracle_mm8(threads: int, rows_sample: int = 512):
+def time_oracle_mm8(threads: int, rows_sample: int = 4096):
     """The small-batch product (8 tokens) on a window of rows: weight GB/s, in the
     bench's byte units scaled to the rows computed."""
     import oracle
@@ -439,7 +452,8 @@ def cpu_baseline(seconds_target: float = 8.0):
                               "sample": f"{n1} full matvecs in {el1:.1f} s"},
             "per_workload": {
                 "mm8": {"value": mm8_gbs, "unit": "GB/s", "cores": cores,
-                        "sample": f"512 of 4096 rows x 8 tokens in {el_mm:.1f} s"},
+                        "sample": f"all 4096 rows x 8 tokens over {cores} threads in "
+                                  f"{el_mm:.2f} s"},
                 "moe": {"value": moe_tps, "unit": "tokens/s", "cores": 1,
                         "sample": f"2 of 32 tokens, whole layer, in {el_moe:.1f} s"}}}
 
@@ -604,9 +618,12 @@ def main():
     mx.mxfp4_set_launch_overlap(True)
     us_off = secs_off / (args.steps * main_w.launches_per_step) * 1e6
 
-    e2e_secs = time_e2e(main_w, max(args.steps // 5, 3), args.warmup)
-    e2e_steps = max(args.steps // 5, 3)
+    main_w.setup_e2e()
+    e2e_steps = args.steps
+    e2e_secs = time_e2e(main_w, e2e_steps, args.warmup)
     e2e_val = ws * e2e_steps * main_w.bytes_per_step / e2e_secs / 1e9
+    mm_secs = time_e2e(main_w, e2e_steps, args.warmup, main_w.step_matmat_host)
+    e2e_matmat = ws * e2e_steps * main_w.bytes_per_step / mm_secs / 1e9
 
     workloads = {}
     if not args.only_main:
@@ -674,7 +691,14 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "GB/s",
                     "h2d_bytes_per_step": main_w.h2d, "d2h_bytes_per_step": main_w.d2h,
-                    "api": "mxfp4_matmat_host per layer (pinned host x in, y out, stream sync)"},
+                    "api": "per step: x from pinned host memory, mxfp4_mv per layer, every "
+                           "layer's y to pinned host memory, one stream synchronisation",
+                    "per_layer_host_entry": {
+                        "value": e2e_matmat, "unit": "GB/s",
+                        "api": "mxfp4_matmat_host per layer (x in, y out, a synchronisation "
+                               "each: the page's matmat contract)",
+                        "h2d_bytes_per_step": LAYERS * 4 * main_w.cols,
+                        "d2h_bytes_per_step": main_w.d2h}},
             "gpu_launches": args.steps * main_w.launches_per_step,
             "clocks": clocks,
             "workloads": workloads,
