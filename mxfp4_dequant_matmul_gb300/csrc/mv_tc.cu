@@ -129,7 +129,7 @@ struct MvLayout {
 __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, int stages) {
     MvLayout l;
     l.lut = 0;                                                        // [256] f32
-    l.xf = 1024;                                                      // [ng][8 NT] uint4
+    l.xf = 1024;                                                      // [NT][ng][128] bytes
     l.sc = l.xf + static_cast<uint32_t>(ng_max) * 128 * NT;           // [rows][pitch] u8
     // an odd number of 16-byte words per row: eight rows' scale bytes of a unit
     // fall in eight different bank groups
@@ -140,8 +140,8 @@ __host__ __device__ inline MvLayout mv_layout(int NT, int ng_max, int ru_cta, in
     // [rows][NT]; zero during the units: its bytes 32 .. 47 are the B values of
     // the lanes that hold none
     l.fin = l.part + static_cast<uint32_t>(kRangesM + ru_cta - 1) * kRowsU * NT * 4;
-    l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;  // pexp[8], tmax[8], flag
-    l.bars = (l.misc + 80 + 7u) & ~7u;   // [full, empty][rings][kMaxStagesM]
+    l.misc = l.fin + static_cast<uint32_t>(ru_cta) * kRowsU * NT * 4;   // tmax[8], flag, x barrier
+    l.bars = l.misc + 48;   // [full, empty][rings][kMaxStagesM]
     l.ring = (l.bars + 2 * kWarpsM * kMaxStagesM * 8 + 1023u) & ~1023u;
     l.total = l.ring + static_cast<uint32_t>(rings_mv(NT) * stages) * kStageM + 1024;   // + align slack
     return l;
@@ -157,16 +157,16 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const MvLayout L = mv_layout(NT, ng_max, ru_cta, stages);
     float* lut = reinterpret_cast<float*>(smem + L.lut);
-    uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
+    uint8_t* xf_b = smem + L.xf;
     uint8_t* sc_s = smem + L.sc;
     float* part = reinterpret_cast<float*>(smem + L.part);
     float* fin = reinterpret_cast<float*>(smem + L.fin);
     constexpr int kThr = kThreadsM;
     constexpr bool kPaired = NT == 8;                   // two warps per ring
     constexpr int kRpw = kRangesM / rings_mv(NT);       // ranges per ring
-    int* pexp = reinterpret_cast<int*>(smem + L.misc);                 // [8]
-    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 32);  // [8]
-    int* not_plain = reinterpret_cast<int*>(smem + L.misc + 64);
+    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc);   // [8]
+    int* not_plain = reinterpret_cast<int*>(smem + L.misc + 32);
+    uint64_t* x_bar = reinterpret_cast<uint64_t*>(smem + L.misc + 40);   // the activations' copy
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -224,11 +224,15 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // one before touching anything this one writes)
     if (overlap) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < NT) tmax[tid] = 0u;
-    if (tid == 0) *not_plain = 0;
+    if (tid == 0) {
+        *not_plain = 0;
+        mbar_init(x_bar, 1);
+        fence_mbar_init();
+    }
     for (int i = tid; i < ru_cta * kRowsU * NT / 4; i += kThr)
         reinterpret_cast<uint4*>(fin)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-    // --- prologue: E8M0 table, scale bytes, activations
+    // --- prologue: scale bytes, weights, activations
     const int nrow = min(n_ru * kRowsU, rows - row0);
     // 16-byte words covering a row's ng scale bytes: exactly ng / 16 when the
     // rows' slices start on 16 bytes and fill whole words, else enough for any
@@ -251,9 +255,10 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     // The weights stream after the prologue's own loads, which would otherwise
     // wait behind them in the memory system -- unless the launch overlaps the
     // previous kernel of the stream (programmatic dependent launch): then the
-    // weights, which that kernel does not write, start at once, and x (which
-    // it may write) is read only once it has completed.
-    // (unit k goes to stage k: never more units than the ring has stages)
+    // weights, which that kernel does not write, start at once (behind the
+    // scale bytes), and x (which it may write) is read only once it has
+    // completed.  (unit k goes to stage k: never more units than the ring has
+    // stages)
     auto start_weights = [&](int k0, int k1) {   // this ring's units k0 .. k1-1
         if (issuer) {
             if (k0 == 0) {
@@ -271,25 +276,36 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     };
     if (overlap) {
         start_weights(0, kPreStagesM);
+        __syncthreads();   // tmax, not_plain and x_bar are set before any use below
         asm volatile("griddepcontrol.wait;" ::: "memory");
     }
-    // activation items: (token, group, word) = 8 elements.  Up to four tokens
-    // they wait in registers for the tokens' powers of two; eight tokens are
-    // first staged as floats in the shared-memory bytes their own hi and lo
-    // fragments will take (32 bytes per item, so the split below is in place).
-    constexpr bool kStaged = NT == 8;
-    constexpr int kXU = kStaged ? 1 : (NT * kGMax * 4 + kThr - 1) / kThr;
-    const int n_items = NT * ng * 4;
-    float xv[kXU][8];
-    float mloc[NT];   // staged: this thread's largest finite |x| per token
-#pragma unroll
-    for (int q = 0; q < NT; ++q) mloc[q] = 0.0f;
-    if constexpr (!kStaged) {
+
+    // Activation items: item i = (n ng + j) 4 + w is word w (8 elements) of group
+    // j of token n; group j of token n takes bytes (n ng + j) 128 of xf, first as
+    // floats (eight tokens), then as its hi and lo halves.  Up to four tokens
+    // each thread loads its items into registers (one round trip); eight tokens'
+    // items (up to 8 a thread) come by one bulk copy per token.
+    const int n4 = ng * 4;
+    const int n_items = NT * n4;
+    constexpr int kXU = (NT * kGMax * 4 + kThr - 1) / kThr;
+    constexpr bool kBulkX = NT == 8;
+    float xv[kXU][8];   // (eight tokens: filled from shared memory once the copies land)
+    if constexpr (kBulkX) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(x_bar, static_cast<uint32_t>(nbt * ng * 128));
+            uint64_t keep;   // x is read by every CTA of the row split: keep it in L2
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+            for (int n = 0; n < nbt; ++n)
+                bulk_g2s(xf_b + static_cast<size_t>(n) * ng * 128,
+                         X + static_cast<size_t>(t0 + n) * cols +
+                             static_cast<size_t>(g_lo) * kGroup,
+                         static_cast<uint32_t>(ng * 128), x_bar, keep);
+        }
+    } else {
+        int tok = tid / n4, rem = tid - (tid / n4) * n4;
 #pragma unroll
         for (int u = 0; u < kXU; ++u) {
-            const int i = tid + u * kThr;
-            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
-            if (i < n_items && tok < nbt) {
+            if (tid + u * kThr < n_items && tok < nbt) {
                 const float4* src = reinterpret_cast<const float4*>(
                     X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
                     8 * rem);
@@ -300,31 +316,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
             }
-        }
-    } else {
-        for (int i = tid; i < n_items; i += kThr) {
-            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
-            const int j = rem >> 2, tw = rem & 3;
-            float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
-            if (tok < nbt) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    X + static_cast<size_t>(t0 + tok) * cols + static_cast<size_t>(g_lo) * kGroup +
-                    8 * rem);
-                a = __ldg(src);
-                b = __ldg(src + 1);
-            }
-            const float e8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float m = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float v = fabsf(e8[e]);
-                m = fmaxf(m, v <= 3.402823466e38f ? v : 0.0f);   // NaN and inf do not count
-            }
-#pragma unroll
-            for (int q = 0; q < NT; ++q)
-                if (q == tok) mloc[q] = fmaxf(mloc[q], m);
-            reinterpret_cast<float4*>(xf)[j * (8 * NT) + (2 * tok) * 4 + tw] = a;
-            reinterpret_cast<float4*>(xf)[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = b;
+            for (rem += kThr; rem >= n4; rem -= n4) ++tok;
         }
     }
     start_weights(overlap ? kPreStagesM : 0, stages);   // after the prologue's loads
@@ -339,8 +331,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                          "r"(row0 + ru * kRowsU)
                          : "memory");
         }
+    if (!overlap) __syncthreads();   // (the same, once the loads are on their way)
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
-    __syncthreads();   // tmax is zero before any atomic below
     // "plain" scales: no byte 0 or 255 and none above kPlainMax, so that 2^(k-127)
     // is the float with bits k << 23 and the rows' sums can stay in the 2^p
     // domain without overflow (|sum| < 128*32 * 6 * 2^(kPlainMax-127) * 2^15)
@@ -373,69 +365,82 @@ __global__ void __launch_bounds__(kThreadsM, 1)
             }
         }
     }
-    if constexpr (!kStaged) {
+    if (__any_sync(0xffffffffu, odd) && lane == 0) atomicOr(not_plain, 1);
+
+    // Each token gets one power of two p, putting the largest finite |x| of its
+    // slice in [2^14, 2^15) (p = 0 for zeros; capped at 126 so that 2^-p stays
+    // normal), and x 2^p is split into f16 halves hi = f16(x 2^p) and
+    // lo = f16(x 2^p - hi): item i's go to bytes 16 w and 64 + 16 w of its
+    // group's 128.
+    if constexpr (kBulkX) {
+        if (!mbar_wait(x_bar, 0u, kWaitM) && lane == 0) atomicOr(&g_fault_mvtc, 1);
+        int tok = tid / n4, rem = tid - (tid / n4) * n4;
 #pragma unroll
         for (int u = 0; u < kXU; ++u) {
             const int i = tid + u * kThr;
-            const int tok = min(i / (ng * 4), NT - 1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
+            if (i < n_items && tok < nbt) {
+                const float4* f = reinterpret_cast<const float4*>(xf_b + static_cast<size_t>(i) * 32);
+                const float4 a = f[0], b = f[1];
+                xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+                xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
+            }
+            for (rem += kThr; rem >= n4; rem -= n4) ++tok;
+        }
+    }
+    {
+        float mloc[NT];   // this thread's largest finite |x| per token
+#pragma unroll
+        for (int q = 0; q < NT; ++q) mloc[q] = 0.0f;
+        int tok = tid / n4, rem = tid - (tid / n4) * n4;
+#pragma unroll
+        for (int u = 0; u < kXU; ++u) {
             float m = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float a = fabsf(xv[u][e]);
                 m = fmaxf(m, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
             }
-            // lanes of a token reduce together; one atomic per token and warp
-            const unsigned same = __match_any_sync(0xffffffffu, tok);
-            const unsigned mb = __reduce_max_sync(same, __float_as_uint(m));
-            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
+#pragma unroll
+            for (int q = 0; q < NT; ++q)
+                if (q == tok) mloc[q] = fmaxf(mloc[q], m);
+            for (rem += kThr; rem >= n4; rem -= n4) ++tok;
         }
-    } else {
 #pragma unroll
         for (int q = 0; q < NT; ++q) {
             const unsigned mb = __reduce_max_sync(0xffffffffu, __float_as_uint(mloc[q]));
             if (mb != 0u && lane == 0) atomicMax(&tmax[q], mb);
         }
     }
-    if (__any_sync(0xffffffffu, odd) && lane == 0) atomicOr(not_plain, 1);
     __syncthreads();
-    if (tid < NT) {
-        const float m = __uint_as_float(tmax[tid]);
-        // puts the largest |x| in [2^14, 2^15); capped so 2^-p stays normal
-        pexp[tid] = m > 0.0f ? min(14 - ilogbf(m), 126) : 0;
-    }
-    __syncthreads();
-    // x 2^p -> f16 hi = f16(x 2^p) and lo = f16(x 2^p - hi), 8 elements per item
-    auto split8 = [&](const float (&e8)[8], int tok, int j, int tw) {
-        const float pm = exp2i_m(pexp[tok]);   // 2^p is a normal float
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float a0 = __fmul_rn(e8[2 * k], pm), a1 = __fmul_rn(e8[2 * k + 1], pm);
-            hi[k] = pack_f16x2_m(a0, a1);
-            const float2 h = f16x2_to_f32x2(hi[k]);
-            lo[k] = pack_f16x2_m(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
-        }
-        xf[j * (8 * NT) + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        xf[j * (8 * NT) + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    // 2^p of token q from its largest |x|
+    auto p_of = [&](int q) {
+        const float m = __uint_as_float(tmax[q]);
+        const int e = static_cast<int>(__float_as_uint(m) >> 23);   // exponent field (m >= 0)
+        return m > 0.0f ? (e == 0 ? 126 : min(141 - e, 126)) : 0;
     };
-    if constexpr (!kStaged) {
+    {
+        int tok = tid / n4, rem = tid - (tid / n4) * n4;
 #pragma unroll
         for (int u = 0; u < kXU; ++u) {
             const int i = tid + u * kThr;
+            const float (&e8)[8] = xv[u];
             if (i < n_items) {
-                const int tok = i / (ng * 4), rem = i - tok * ng * 4;
-                split8(xv[u], tok, rem >> 2, rem & 3);
+                const float pm = __uint_as_float(static_cast<uint32_t>(p_of(tok) + 127) << 23);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float a0 = __fmul_rn(e8[2 * k], pm), a1 = __fmul_rn(e8[2 * k + 1], pm);
+                    hi[k] = pack_f16x2_m(a0, a1);
+                    const float2 h = f16x2_to_f32x2(hi[k]);
+                    lo[k] = pack_f16x2_m(__fsub_rn(a0, h.x), __fsub_rn(a1, h.y));
+                }
+                uint4* blk = reinterpret_cast<uint4*>(xf_b + static_cast<size_t>(i >> 2) * 128);
+                blk[i & 3] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                blk[4 + (i & 3)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-        }
-    } else {
-        for (int i = tid; i < n_items; i += kThr) {
-            const int tok = i / (ng * 4), rem = i - tok * ng * 4;
-            const int j = rem >> 2, tw = rem & 3;
-            const float4 a = reinterpret_cast<const float4*>(xf)[j * (8 * NT) + (2 * tok) * 4 + tw];
-            const float4 b =
-                reinterpret_cast<const float4*>(xf)[j * (8 * NT) + (2 * tok + 1) * 4 + tw];
-            const float e8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            split8(e8, tok, j, tw);
+            for (rem += kThr; rem >= n4; rem -= n4) ++tok;
         }
     }
     __syncthreads();
@@ -466,16 +471,23 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     bool plain[NS];
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
-        const int p_t = pexp[s * NTS + tk];
+        const int p_t = p_of(s * NTS + tk);
         pinv[s] = exp2i_m(-p_t);
         plain[s] = *not_plain == 0 && p_t >= 0;
     }
     // every lane's tokens in the 2^p domain (the usual case): a warp-uniform flag
     const bool all_plain = __all_sync(0xffffffffu, plain[0] && plain[NS - 1]) != 0;
-    // B: lanes 8 NTS s .. 8 NTS s + 8 NTS - 1 hold the fragment of group slot s;
-    // column set s of eight tokens is 512 bytes further
+    // B: lanes 8 NTS s .. 8 NTS s + 8 NTS - 1 hold the fragment of group slot s,
+    // lane 8 n + 4 h + w of them word w's half h (hi, lo) of token n of the
+    // column set (column set c: tokens c NTS ..), 16 bytes of group j's 128 of
+    // that token
     const int b_slot = lane / (8 * NTS);
-    const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * NTS)) * 16;
+    uint32_t xf_lane[NS];
+#pragma unroll
+    for (int c = 0; c < NS; ++c)
+        xf_lane[c] = smem_u32(xf_b) +
+                     static_cast<uint32_t>((c * NTS + (lane % (8 * NTS)) / 8) * ng * 128 +
+                                           (lane % 8) * 16);
     const uint32_t zero_lane = smem_u32(fin) + 32;
     const uint32_t sel0 = 0x4044u + (static_cast<uint32_t>(slot) << 8);   // byte slot -> byte 2
     // token n's four sums: P_r in lane (g, (r mod GP) NTS + n), entry r / GP; lane
@@ -545,9 +557,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 #pragma unroll
         for (int q = 0; q < RQ; ++q)
             sb[q] = *reinterpret_cast<const uint2*>(scr + q * 8 * L.sc_pitch + gc0);
-        // B fragments of the unit's first group (column set c and group j at
-        // immediate offsets from it)
-        const uint32_t xb = xf_lane + static_cast<uint32_t>(gc0) * (128 * NT);
+        // B fragments of the unit's first group (group j at immediate offsets
+        // from it)
+        uint32_t xb[NS];
+#pragma unroll
+        for (int c = 0; c < NS; ++c) xb[c] = xf_lane[c] + static_cast<uint32_t>(gc0) * 128;
         // the unit's groups; FAST: a whole unit (8 groups) and every lane's token
         // in the 2^p domain, so that no guard and no table path is needed (the
         // same arithmetic as the general form for such units)
@@ -576,7 +590,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
                             e2m1x8_to_f16x2x4(cwd[1], h1);
 #pragma unroll
                             for (int c = 0; c < NS; ++c) {
-                                const uint32_t ba = xb + static_cast<uint32_t>(j * (128 * NT) + c * 512);
+                                const uint32_t ba = xb[c] + static_cast<uint32_t>(j * 128);
                                 const uint4 b = lds128(GP == 1 || b_slot == s ? ba : zero_lane);
                                 if (s == 0) {
                                     mma16816_z(d0[c], h0[0], h1[0], h0[1], h1[1], b.x, b.y);
@@ -697,9 +711,12 @@ __global__ void __launch_bounds__(kThreadsM, 1)
         const int r_lo = static_cast<int>(rank) * nr / CL;
         const int r_hi = static_cast<int>(rank + 1) * nr / CL;
         for (int i = r_lo * NT + tid; i < r_hi * NT; i += kThr) {
-            float s = ld_cluster_m(fin + i, 0);
-            for (uint32_t q = 1; q < static_cast<uint32_t>(CL); ++q)
-                s = __fadd_rn(s, ld_cluster_m(fin + i, q));
+            float v[CL];   // every rank's value requested before the first is used
+#pragma unroll
+            for (int q = 0; q < CL; ++q) v[q] = ld_cluster_m(fin + i, static_cast<uint32_t>(q));
+            float s = v[0];
+#pragma unroll
+            for (int q = 1; q < CL; ++q) s = __fadd_rn(s, v[q]);
             const int row = row0 + i / NT, tok = i % NT;
             if (row < rows && tok < nbt) Y[static_cast<size_t>(t0 + tok) * rows + row] = s;
         }
