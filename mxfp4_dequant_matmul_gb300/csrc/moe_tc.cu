@@ -93,8 +93,8 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;                   // pexp, tmax, pairs, lead, 16 zeros, odd flag
-    l.segst = l.misc + 96;                                            // [touched + 1] int
+    l.misc = l.lut + 1024;   // tmax[2][4], pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][4]
+    l.segst = l.misc + 160;                                           // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
     l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
     l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
@@ -121,13 +121,16 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const ELayout L = e_layout(NM, gpr, n_experts);
     uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
     float* lut = reinterpret_cast<float*>(smem + L.lut);
-    int* pexp = reinterpret_cast<int*>(smem + L.misc);                  // [4]
-    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc + 16);   // [4]
-    int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [4]
-    int* lead = reinterpret_cast<int*>(smem + L.misc + 48);             // [2 buffers][2 matrices]
-    const uint32_t zero16 = smem_u32(smem + L.misc + 64);               // 16 zero bytes
+    // per segment, double-buffered (buffer = the CTA's segment count mod 2, so
+    // that the next segment's are set while this one runs): the pairs' largest
+    // |x|, the pair ids and the flag of an odd scale byte
+    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc);        // [2][4]
+    int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [2][4]
+    int* lead = reinterpret_cast<int*>(smem + L.misc + 64);             // [2 buffers][2 matrices]
+    const uint32_t zero16 = smem_u32(smem + L.misc + 80);               // 16 zero bytes
+    int* seg_odd = reinterpret_cast<int*>(smem + L.misc + 96);          // [2]
+    int* segmeta = reinterpret_cast<int*>(smem + L.misc + 112);         // [2][u, e, b0, n_e]
     int* segst = reinterpret_cast<int*>(smem + L.segst);
-    int* seg_odd = reinterpret_cast<int*>(smem + L.misc + 80);          // a segment's odd byte
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
     uint64_t* ring_bars = sbar + 2;
 
@@ -144,25 +147,82 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     // the previous kernel's plan / activations before reading them
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid < 256) lut[tid] = e8m0_to_f32(static_cast<uint32_t>(tid));
-    if (tid < 4) reinterpret_cast<uint32_t*>(smem + L.misc + 64)[tid] = 0u;
+    if (tid < 4) reinterpret_cast<uint32_t*>(smem + L.misc + 80)[tid] = 0u;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (tid == 0) {
         mbar_init(&sbar[0], 1);
         mbar_init(&sbar[1], 1);
         for (int i = 0; i < kWarpsE * kStagesE; ++i) mbar_init(&ring_bars[i], 1);
         fence_mbar_init();
-        // segments per touched expert: ceil(pairs / 4) x row blocks
-        const int n_touched = plan.hdr[1];
-        segst[0] = 0;
-        for (int u = 0; u < n_touched; ++u) {
-            const int e = plan.touched[u];
-            const int n_e = plan.offsets[e + 1] - plan.offsets[e];
-            segst[u + 1] = segst[u] + (n_e + kTokSeg - 1) / kTokSeg * n_blocks;
+    }
+    // segst: the first segment of each touched expert (ceil(pairs / 4) x row
+    // blocks each), a prefix sum over the touched experts, thread t taking
+    // experts 2t and 2t + 1 (at most 1024 of them)
+    const int n_touched = plan.hdr[1];
+    int n_seg;
+    {
+        int* wtot = reinterpret_cast<int*>(smem + L.xf);   // [16] (xf is not in use yet)
+        int eu[2], bu[2], nu[2], cu[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int u = 2 * tid + k;
+            eu[k] = bu[k] = nu[k] = cu[k] = 0;
+            if (u < n_touched) {
+                eu[k] = __ldg(plan.touched + u);
+                bu[k] = __ldg(plan.offsets + eu[k]);
+                nu[k] = __ldg(plan.offsets + eu[k] + 1) - bu[k];
+                cu[k] = (nu[k] + kTokSeg - 1) / kTokSeg * n_blocks;
+            }
+        }
+        const int tsum = cu[0] + cu[1];
+        int incl = tsum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) wtot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int v = lane < kWarpsE ? wtot[lane] : 0;
+#pragma unroll
+            for (int d = 1; d < kWarpsE; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += o;
+            }
+            __syncwarp();
+            if (lane < kWarpsE) wtot[lane] = v;
+        }
+        __syncthreads();
+        const int excl = (warp > 0 ? wtot[warp - 1] : 0) + incl - tsum;
+        n_seg = wtot[kWarpsE - 1];
+        if (tid == 0) segst[0] = 0;
+        int lo = excl;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int u = 2 * tid + k;
+            if (u < n_touched) {
+                segst[u + 1] = lo + cu[k];
+                // the meta slots of this CTA's first two segments
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int sq = static_cast<int>(blockIdx.x + q * gridDim.x);
+                    if (sq >= lo && sq < lo + cu[k]) {
+                        segmeta[q * 4 + 0] = u;
+                        segmeta[q * 4 + 1] = eu[k];
+                        segmeta[q * 4 + 2] = bu[k];
+                        segmeta[q * 4 + 3] = nu[k];
+                    }
+                }
+            }
+            lo += cu[k];
         }
     }
     __syncthreads();
-    const int n_touched = plan.hdr[1];
-    const int n_seg = segst[n_touched];
+    // (thread 0) the segment after next: looked up while this one runs, its
+    // loads issued in one phase and used in a later one, so that they wait on
+    // nothing (touched index and id, then first pair and count)
+    int la_s = 0, la_u = segmeta[4], la_e = 0, la_b0 = 0, la_b1 = 0;
     uint64_t* bars = ring_bars + warp * kStagesE;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * kStagesE * kStageE;
 
@@ -171,17 +231,17 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         int e, sg, z, beg, npair, row0, nrow, n_ru, WK, m, my_ru, c_lo, n_units;
         bool active;
     };
-    auto seg_of = [&](int s) {
+    // segment s from its expert's entry in meta slot `slot`
+    auto seg_of = [&](int s, int slot) {
         Seg q{};
         if (s >= n_seg) return q;   // none: no units
-        int u = 0;
-        while (segst[u + 1] <= s) ++u;
-        q.e = plan.touched[u];
+        const int* m = segmeta + slot * 4;
+        const int u = m[0], b0 = m[2], n_e = m[3];
+        q.e = m[1];
         // the expert's bank segment and its plane in that segment (both banks of
         // a pass are split alike)
         q.sg = bank0.n_seg == 1 ? 0 : q.e / bank0.seg_slots;
         q.z = q.e - q.sg * bank0.seg_slots;
-        const int b0 = plan.offsets[q.e], n_e = plan.offsets[q.e + 1] - b0;
         const int rel = s - segst[u];
         const int ck = rel / n_blocks, b = rel - ck * n_blocks;
         q.beg = b0 + ck * kTokSeg;
@@ -238,17 +298,22 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     int issued = 0;     // this warp's units issued so far (lane 0): never more than kglob + stages
     int nseg_cta = 0;   // segments this CTA has taken so far (scale buffer and phase)
     bool failed = false;
-    Seg cur = seg_of(blockIdx.x);
+    Seg cur = seg_of(blockIdx.x, 0);
     int sc_pend = -1;   // (thread 0) buffer of a scale copy not yet seen complete
     uint32_t sc_pend_par = 0;
     if (tid == 0 && blockIdx.x < n_seg) {
         issue_scales(cur, 0);
         sc_pend = 0;
     }
+    if (tid < kTokSeg) {   // the first segment's pairs and maxima (its first barrier below)
+        tmax[tid] = 0u;
+        spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
+    }
+    if (tid == 0) seg_odd[0] = 0;
 
     for (int s = blockIdx.x; s < n_seg; s += gridDim.x, ++nseg_cta) {
-        const Seg nxt = seg_of(s + gridDim.x);
         const int bi = nseg_cta & 1;
+        const Seg nxt = seg_of(s + gridDim.x, bi ^ 1);
         // the next unit of this warp's stream (this segment's, then the next one's)
         auto issue_next = [&]() {
             const int j = issued - kglob;
@@ -262,12 +327,20 @@ __global__ void __launch_bounds__(kThreadsE, 1)
 
         // --- prologue: the pairs' vectors -> B fragments
         __syncthreads();   // the last segment is done with the fragments and the pairs
-        if (tid < kTokSeg) {
-            tmax[tid] = 0u;
-            spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
+        const int* sp = spair + bi * kTokSeg;
+        unsigned* tm = tmax + bi * kTokSeg;
+        if (tid < kTokSeg) {   // the next segment's (the last one is done with them)
+            tmax[(bi ^ 1) * kTokSeg + tid] = 0u;
+            spair[(bi ^ 1) * kTokSeg + tid] = tid < nxt.npair ? plan.pair_of[nxt.beg + tid] : 0;
         }
-        if (tid == 0) *seg_odd = 0;
-        __syncthreads();
+        if (tid == 0) {
+            seg_odd[bi ^ 1] = 0;
+            la_s = s + 2 * static_cast<int>(gridDim.x);
+            if (la_s < n_seg) {
+                while (segst[la_u + 1] <= la_s) ++la_u;
+                la_e = __ldg(plan.touched + la_u);
+            }
+        }
         // column sets of this segment: NP >= its pairs
         const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
         constexpr int kXU = (kTokSeg * kGMaxE * 4 + kThreadsE - 1) / kThreadsE;
@@ -278,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             const int i = tid + uu * kThreadsE;
             const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
             if (i < n_items && tok < cur.npair) {
-                const int pr = spair[tok];
+                const int pr = sp[tok];
                 const size_t vrow = NM == 2 ? static_cast<size_t>(pr / top_k) : static_cast<size_t>(pr);
                 const float4* src = reinterpret_cast<const float4*>(vec + vrow * cols + 8 * rem);
                 const float4 a = __ldg(src), bb = __ldg(src + 1);
@@ -306,21 +379,28 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             }
             const unsigned same = __match_any_sync(0xffffffffu, tok);
             const unsigned mb = __reduce_max_sync(same, __float_as_uint(mx));
-            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tmax[tok], mb);
+            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tm[tok], mb);
         }
         __syncthreads();
-        if (tid < kTokSeg) {
-            const float mt = __uint_as_float(tmax[tid]);
-            pexp[tid] = mt > 0.0f ? min(14 - ilogbf(mt), 126) : 0;
+        if (tid == 0 && la_s < n_seg) {
+            la_b0 = __ldg(plan.offsets + la_e);
+            la_b1 = __ldg(plan.offsets + la_e + 1);
         }
-        __syncthreads();
+        // pair q's power of two p: its largest |x| into [2^14, 2^15) (p = 14 -
+        // floor(log2 m) from m's exponent field; a subnormal m takes the cap,
+        // 126, which keeps 2^-p normal; 0 for zeros)
+        auto p_of = [&](int q) {
+            const unsigned mb = tm[q];
+            const int e = static_cast<int>(mb >> 23);
+            return mb != 0u ? (e == 0 ? 126 : min(141 - e, 126)) : 0;
+        };
 #pragma unroll
         for (int uu = 0; uu < kXU; ++uu) {
             const int i = tid + uu * kThreadsE;
             const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
             if (i < n_items && tok < np) {
                 const int j = rem >> 2, tw = rem & 3;
-                const float pm = exp2i_e(pexp[tok]);
+                const float pm = exp2i_e(p_of(tok));
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -360,18 +440,18 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                     }
                 }
             }
-            if (odd) atomicOr(seg_odd, 1);
+            if (odd) atomicOr(&seg_odd[bi], 1);
         }
         failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
         // the whole segment in the 2^p domain: no odd scale byte, every pair's p >= 0
-        bool fast = *seg_odd == 0;
+        bool fast = seg_odd[bi] == 0;
 #pragma unroll
-        for (int q = 0; q < kTokSeg; ++q) fast = fast && pexp[q] >= 0;
+        for (int q = 0; q < kTokSeg; ++q) fast = fast && p_of(q) >= 0;
 
         // --- this warp's units
         float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24, this lane's groups
         const int slot = t / np, tok = t % np;   // D columns 2t, 2t + 1: group slot, pair
-        const float pinv = exp2i_e(-pexp[tok]);
+        const float pinv = exp2i_e(-p_of(tok));
         // B: lanes 8 np s .. 8 np s + 8 np - 1 hold the fragment of group slot s
         const int b_slot = lane / (8 * np);
         const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * np)) * 16;
@@ -482,6 +562,12 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
         }
         kglob += cur.n_units;
+        if (tid == 0 && la_s < n_seg) {   // the segment after next, for the next iteration
+            segmeta[bi * 4 + 0] = la_u;
+            segmeta[bi * 4 + 1] = la_e;
+            segmeta[bi * 4 + 2] = la_b0;
+            segmeta[bi * 4 + 3] = la_b1 - la_b0;
+        }
         failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales
         // the next segment's scale rows go to the other buffer
         if (tid == 0 && !failed && s + static_cast<int>(gridDim.x) < n_seg) {
@@ -524,9 +610,9 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 v[mm] = sacc;
             }
             if (row < rows && tok < cur.npair) {
-                const size_t o = static_cast<size_t>(spair[tok]) * rows + row;
+                const size_t o = static_cast<size_t>(sp[tok]) * rows + row;
                 if constexpr (NM == 2)
-                    out[o] = moe_act(v[0], v[1], epi, spair[tok]);
+                    out[o] = moe_act(v[0], v[1], epi, sp[tok]);
                 else
                     out[o] = v[0];
             }
