@@ -124,11 +124,11 @@ cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold
 // Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu;
 // cudaErrorNotSupported, with nothing launched, for shapes they cannot take.
 cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
-                                  int hidden, int top_k, const float* x, const int32_t* hdr,
+                                  int hidden, int top_k, const float* x, int32_t* hdr,
                                   const int32_t* offsets, const int32_t* touched,
                                   const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s);
 cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
-                               const float* act, const int32_t* hdr, const int32_t* offsets,
+                               const float* act, int32_t* hdr, const int32_t* offsets,
                                const int32_t* touched, const int32_t* pair_of, float* o_pairs,
                                cudaStream_t s);
 

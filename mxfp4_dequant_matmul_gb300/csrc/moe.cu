@@ -37,8 +37,10 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 WsLayout ws_layout(int n_slots, int n_pairs, int hidden) {
     WsLayout l;
-    l.hdr = 0;                                            // int32[4]: invalid, touched, cold
-    l.offsets = 16;                                       // int32[slots + 1]
+    // int32[8]: invalid pairs, touched experts, cold pairs, -, the tensor-core
+    // passes' segment claim counter and finished-CTA counter, -, -
+    l.hdr = 0;
+    l.offsets = 32;                                       // int32[slots + 1]
     l.touched = align_up(l.offsets + 4 * (static_cast<size_t>(n_slots) + 1), 16);
     l.pair_of = align_up(l.touched + 4 * static_cast<size_t>(n_slots), 16);
     l.pair_slot = align_up(l.pair_of + 4 * static_cast<size_t>(n_pairs), 16);   // int32[pairs]
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(1024) k_moe_plan(const int32_t* __restrict__ i
         }
         plan.hdr[0] = s_invalid;
         plan.hdr[1] = touched;
+        plan.hdr[4] = 0;
+        plan.hdr[5] = 0;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < n_experts; e += blockDim.x) {
@@ -247,6 +251,8 @@ __global__ void __launch_bounds__(1024) k_moe_plan_s(const int32_t* __restrict__
         plan.offsets[n_experts] = c_run;
         plan.hdr[0] = s_invalid;
         plan.hdr[1] = f_run;
+        plan.hdr[4] = 0;
+        plan.hdr[5] = 0;
     }
     __syncthreads();
     const int n_planned = plan.offsets[n_experts];

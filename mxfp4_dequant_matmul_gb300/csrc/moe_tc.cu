@@ -17,14 +17,16 @@
 // end of the warp's units.
 //
 // Work: a segment is (touched expert, up to four of its pairs, 128 rows of its
-// gate and up matrices or 256 rows of its down matrix); the segments of all
-// touched experts are dealt to persistent CTAs in turn.  For each segment a
-// CTA copies the rows' scale bytes with one bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
+// gate and up matrices or 256 rows of its down matrix); persistent CTAs claim
+// the segments of all touched experts in order from a counter in the
+// workspace, two ahead of use.  For each segment a CTA copies the rows' scale
+// bytes with one bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
 // (matrix, 32-row unit, chunk range) units of 32 rows x 8 groups through
 // per-warp rings of TMA tile loads (a 3-D tensor map over the bank: bytes,
 // rows, experts).  Partial sums are added in chunk order; the gate/up pass
 // applies SiLU(g) * u and writes act[pair][row], the down pass writes
-// o[pair][row].  Every order depends on the shapes and the routing only.
+// o[pair][row].  Every order depends on the shapes and the routing only (not
+// on which CTA takes a segment).
 #include <cstdint>
 #include <mutex>
 #include <type_traits>
@@ -71,7 +73,8 @@ __device__ __forceinline__ uint32_t pack_f16x2_e(float lo, float hi) {
 
 // Plan arrays written by the routing plan kernel (moe.cu).
 struct PlanRef {
-    const int32_t* hdr;       // [1] = number of touched experts
+    int32_t* hdr;             // [1] = number of touched experts; [4], [5] = the
+                              // pass's segment claim and finished-CTA counters
     const int32_t* offsets;   // [E + 1]
     const int32_t* touched;   // [touched]
     const int32_t* pair_of;   // pairs grouped by expert
@@ -93,8 +96,8 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;   // tmax[2][4], pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][4]
-    l.segst = l.misc + 160;                                           // [touched + 1] int
+    l.misc = l.lut + 1024;   // tmax[2][4], pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][8]
+    l.segst = l.misc + 192;                                           // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
     l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
     l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     int* lead = reinterpret_cast<int*>(smem + L.misc + 64);             // [2 buffers][2 matrices]
     const uint32_t zero16 = smem_u32(smem + L.misc + 80);               // 16 zero bytes
     int* seg_odd = reinterpret_cast<int*>(smem + L.misc + 96);          // [2]
-    int* segmeta = reinterpret_cast<int*>(smem + L.misc + 112);         // [2][u, e, b0, n_e]
+    int* segmeta = reinterpret_cast<int*>(smem + L.misc + 112);   // [2][u, e, b0, n_e, s, -, -, -]
     int* segst = reinterpret_cast<int*>(smem + L.segst);
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
     uint64_t* ring_bars = sbar + 2;
@@ -154,6 +157,12 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         mbar_init(&sbar[1], 1);
         for (int i = 0; i < kWarpsE * kStagesE; ++i) mbar_init(&ring_bars[i], 1);
         fence_mbar_init();
+        // segments are claimed in order from a counter of the workspace (zeroed by
+        // the plan and again by the last CTA of each pass), so that CTAs that
+        // start late or run slow take fewer: this CTA's first two
+        const int c0 = atomicAdd(plan.hdr + 4, 2);
+        segmeta[4] = c0;
+        segmeta[8 + 4] = c0 + 1;
     }
     // segst: the first segment of each touched expert (ceil(pairs / 4) x row
     // blocks each), a prefix sum over the touched experts, thread t taking
@@ -206,12 +215,12 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 // the meta slots of this CTA's first two segments
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const int sq = static_cast<int>(blockIdx.x + q * gridDim.x);
+                    const int sq = segmeta[q * 8 + 4];
                     if (sq >= lo && sq < lo + cu[k]) {
-                        segmeta[q * 4 + 0] = u;
-                        segmeta[q * 4 + 1] = eu[k];
-                        segmeta[q * 4 + 2] = bu[k];
-                        segmeta[q * 4 + 3] = nu[k];
+                        segmeta[q * 8 + 0] = u;
+                        segmeta[q * 8 + 1] = eu[k];
+                        segmeta[q * 8 + 2] = bu[k];
+                        segmeta[q * 8 + 3] = nu[k];
                     }
                 }
             }
@@ -219,10 +228,12 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         }
     }
     __syncthreads();
-    // (thread 0) the segment after next: looked up while this one runs, its
-    // loads issued in one phase and used in a later one, so that they wait on
-    // nothing (touched index and id, then first pair and count)
-    int la_s = 0, la_u = segmeta[4], la_e = 0, la_b0 = 0, la_b1 = 0;
+    // (thread 0) the segment after next: claimed and looked up while this one
+    // runs, each load issued in one phase and used in a later one, so that they
+    // wait on nothing (claim; touched index and id; first pair and count)
+    int la_s = n_seg, la_u = segmeta[8 + 4] < n_seg ? segmeta[8] : 0, la_e = 0, la_b0 = 0,
+        la_b1 = 0;
+    bool la_off = false;   // first pair and count requested
     uint64_t* bars = ring_bars + warp * kStagesE;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * kStagesE * kStageE;
 
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     auto seg_of = [&](int s, int slot) {
         Seg q{};
         if (s >= n_seg) return q;   // none: no units
-        const int* m = segmeta + slot * 4;
+        const int* m = segmeta + slot * 8;
         const int u = m[0], b0 = m[2], n_e = m[3];
         q.e = m[1];
         // the expert's bank segment and its plane in that segment (both banks of
@@ -298,10 +309,11 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     int issued = 0;     // this warp's units issued so far (lane 0): never more than kglob + stages
     int nseg_cta = 0;   // segments this CTA has taken so far (scale buffer and phase)
     bool failed = false;
-    Seg cur = seg_of(blockIdx.x, 0);
+    int s_cur = segmeta[4];
+    Seg cur = seg_of(s_cur, 0);
     int sc_pend = -1;   // (thread 0) buffer of a scale copy not yet seen complete
     uint32_t sc_pend_par = 0;
-    if (tid == 0 && blockIdx.x < n_seg) {
+    if (tid == 0 && s_cur < n_seg) {
         issue_scales(cur, 0);
         sc_pend = 0;
     }
@@ -311,9 +323,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     }
     if (tid == 0) seg_odd[0] = 0;
 
-    for (int s = blockIdx.x; s < n_seg; s += gridDim.x, ++nseg_cta) {
+    for (int s = s_cur; s < n_seg; ++nseg_cta) {
         const int bi = nseg_cta & 1;
-        const Seg nxt = seg_of(s + gridDim.x, bi ^ 1);
+        const int s_nxt = segmeta[(bi ^ 1) * 8 + 4];
+        const Seg nxt = seg_of(s_nxt, bi ^ 1);
         // the next unit of this warp's stream (this segment's, then the next one's)
         auto issue_next = [&]() {
             const int j = issued - kglob;
@@ -335,11 +348,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         }
         if (tid == 0) {
             seg_odd[bi ^ 1] = 0;
-            la_s = s + 2 * static_cast<int>(gridDim.x);
-            if (la_s < n_seg) {
-                while (segst[la_u + 1] <= la_s) ++la_u;
-                la_e = __ldg(plan.touched + la_u);
-            }
+            la_s = atomicAdd(plan.hdr + 4, 1);
+            la_off = false;
         }
         // column sets of this segment: NP >= its pairs
         const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
@@ -383,8 +393,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         }
         __syncthreads();
         if (tid == 0 && la_s < n_seg) {
-            la_b0 = __ldg(plan.offsets + la_e);
-            la_b1 = __ldg(plan.offsets + la_e + 1);
+            while (segst[la_u + 1] <= la_s) ++la_u;
+            la_e = __ldg(plan.touched + la_u);
         }
         // pair q's power of two p: its largest |x| into [2^14, 2^15) (p = 14 -
         // floor(log2 m) from m's exponent field; a subnormal m takes the cap,
@@ -555,6 +565,11 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 fence_proxy_async_smem();
                 issue_next();
             }
+            if (tid == 0 && !la_off && la_s < n_seg) {
+                la_b0 = __ldg(plan.offsets + la_e);
+                la_b1 = __ldg(plan.offsets + la_e + 1);
+                la_off = true;
+            }
         }
         if (failed) {
             // let this warp's copies in flight land before the CTA can exit
@@ -562,15 +577,22 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
         }
         kglob += cur.n_units;
-        if (tid == 0 && la_s < n_seg) {   // the segment after next, for the next iteration
-            segmeta[bi * 4 + 0] = la_u;
-            segmeta[bi * 4 + 1] = la_e;
-            segmeta[bi * 4 + 2] = la_b0;
-            segmeta[bi * 4 + 3] = la_b1 - la_b0;
+        if (tid == 0) {   // the segment after next, for the next iteration
+            if (la_s < n_seg) {
+                if (!la_off) {
+                    la_b0 = __ldg(plan.offsets + la_e);
+                    la_b1 = __ldg(plan.offsets + la_e + 1);
+                }
+                segmeta[bi * 8 + 0] = la_u;
+                segmeta[bi * 8 + 1] = la_e;
+                segmeta[bi * 8 + 2] = la_b0;
+                segmeta[bi * 8 + 3] = la_b1 - la_b0;
+            }
+            segmeta[bi * 8 + 4] = la_s;
         }
         failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales
         // the next segment's scale rows go to the other buffer
-        if (tid == 0 && !failed && s + static_cast<int>(gridDim.x) < n_seg) {
+        if (tid == 0 && !failed && s_nxt < n_seg) {
             issue_scales(nxt, bi ^ 1);
             sc_pend = bi ^ 1;
             sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
@@ -619,6 +641,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         }
         if (failed) break;   // the same in every thread
         cur = nxt;
+        s = s_nxt;
     }
     // a failed CTA may still have copies of a next segment in flight: wait for them
     if (failed) {
@@ -629,6 +652,16 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         if (tid == 0 && sc_pend >= 0) mbar_wait(&sbar[sc_pend], sc_pend_par, kWaitE);
     }
     if (failed && lane == 0) atomicOr(&g_fault_moetc, 1);
+    // the last CTA to finish zeroes the claim counters for the next pass (every
+    // CTA's claims come before its count)
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(plan.hdr + 5, 1) == static_cast<int>(gridDim.x) - 1) {
+            __threadfence();
+            plan.hdr[4] = 0;
+            plan.hdr[5] = 0;
+        }
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_e() {
@@ -719,7 +752,7 @@ cudaError_t launch_e(const Bank& bank0, const Bank& bank1, int n_experts,
 }  // namespace
 
 cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
-                                  int hidden, int top_k, const float* x, const int32_t* hdr,
+                                  int hidden, int top_k, const float* x, int32_t* hdr,
                                   const int32_t* offsets, const int32_t* touched,
                                   const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s) {
     return launch_e<2>(gate, up, n_experts, inter, hidden, top_k, x,
@@ -727,7 +760,7 @@ cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_expert
 }
 
 cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
-                               const float* act, const int32_t* hdr, const int32_t* offsets,
+                               const float* act, int32_t* hdr, const int32_t* offsets,
                                const int32_t* touched, const int32_t* pair_of, float* o_pairs,
                                cudaStream_t s) {
     return launch_e<1>(down, down, n_experts, hidden, inter, 1, act,
