@@ -122,7 +122,16 @@ int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
  *     for bit, whatever the rest of the batch (the page's device test:
  *     "the batch equal to the matvec per token bit for bit").
  *   nb >  MXFP4_MM_SMALL_MAX: the tensor-core path of mxfp4_mm_bf16 (below):
- *     X is rounded to bfloat16 first. */
+ *     X is rounded to bfloat16 first.  The weights and X are converted to
+ *     bfloat16 once ("rlx-cpu 0.2.17 src/gguf_matmul.rs": dense after
+ *     dequant, as mxfp4_mm_bf16_ws) into a device workspace the library keeps
+ *     per (device, stream): allocated on the stream (stream-ordered) by the
+ *     first call that needs it, grown by later ones, never while the stream is
+ *     being captured into a graph, and kept until the process ends
+ *     (mxfp4_mm_bf16_workspace_bytes(rows, cols, nb) bytes).  Without one (a
+ *     capture before any eager call on that stream, or an allocation failure)
+ *     the conversion runs inside the GEMM (mxfp4_mm_bf16); the results are the
+ *     same bit for bit either way. */
 #define MXFP4_MM_SMALL_MAX 64
 int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y,
              cudaStream_t stream);

@@ -6,6 +6,9 @@
 // rows == 0, cols % 32 != 0 or short buffers are refused), without its CPU
 // fallback.
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "../../include/mxfp4.h"
 #include "kernels.h"
@@ -50,6 +53,39 @@ int check_product(const void* w, int rows, int cols, const float* X, int nb, con
 }
 
 const uint8_t* u8(const void* p) { return static_cast<const uint8_t*>(p); }
+
+// The workspace of mxfp4_mm's large batches (weights and activations in bf16,
+// dense after dequant), one per (device, stream): used only in that stream's
+// order, so concurrent streams never share one.  Grown by stream-ordered
+// allocation (the old one freed after the work already queued on the stream);
+// never allocated while the stream is being captured into a graph; kept for the
+// life of the process.  nullptr when none can be had: the caller then takes the
+// path that needs no workspace (the same results bit for bit).
+void* stream_workspace(cudaStream_t s, size_t need) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    std::pair<void*, size_t>& e = cache[{dev, s}];
+    if (e.first != nullptr && e.second >= need) return e.first;
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess || st != cudaStreamCaptureStatusNone) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, need, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (e.first != nullptr) (void)cudaFreeAsync(e.first, s);
+    e = {p, need};
+    return p;
+}
 
 }  // namespace
 
@@ -151,6 +187,13 @@ int mxfp4_mm(const void* w, int rows, int cols, const float* X, int nb, float* Y
         if (e != cudaErrorNotSupported) return from_cuda(e);
         (void)cudaGetLastError();
         return from_cuda(mxk::launch_matmat_fp32(u8(w), rows, cols, X, nb, Y, stream));
+    }
+    // dense after dequant through the stream's workspace when it can be had,
+    // else the conversion inside the GEMM (bit-identical results)
+    if (void* ws = stream_workspace(stream, mxk::dense_ws_bytes(rows, cols, nb))) {
+        const cudaError_t e = mxk::launch_mm_dense(u8(w), rows, cols, X, nb, Y, ws, stream);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        (void)cudaGetLastError();
     }
     return from_cuda(mxk::launch_mm_tcgen05(u8(w), rows, cols, X, nb, Y, stream));
 }

@@ -160,3 +160,34 @@ def test_prefill_config_full_token_bands(mx, fn):
         np.testing.assert_allclose(ref[:, 1000:1004], win, rtol=0, atol=1e-12 * win_l1.max())
         assert_within(Y[t0:t0 + 128], ref, l1, REL_BF16, f"{fn} band {t0}")
         assert_within(Y[t0:t0 + 128], ref, l1, REL_FP32, f"{fn} band {t0}, FP32 bound")
+
+
+def test_mm_large_batches_workspace_per_stream_and_under_capture(mx):
+    # mxfp4_mm's large batches convert W and X to bf16 once into a workspace
+    # the library keeps per stream; where none can be had (a stream captured
+    # before any eager call) the conversion runs inside the GEMM.  Every way
+    # gives the same bits as mxfp4_mm_bf16.
+    import torch
+    rows, cols = 256, 1024
+    w_h = synth.mxfp4_matrix(rows, cols, 11, 118, 130)
+    wd = to_dev(w_h)
+    for nb in (70, 100):   # the second size grows the workspaces made by the first
+        X = synth.normal_f32(12 + nb, nb * cols).reshape(nb, cols)
+        xd = to_dev(X)
+        ref = run(mx, "mxfp4_mm_bf16", w_h, rows, cols, X, nb)
+        fresh = torch.cuda.Stream()
+        Y_cap = empty(nb * rows)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=fresh):
+            mx.mxfp4_mm(wd, rows, cols, xd, nb, Y_cap)
+        g.replay()
+        outs = [Y_cap]
+        for st in (torch.cuda.Stream(), torch.cuda.current_stream()):
+            Y = empty(nb * rows)
+            with torch.cuda.stream(st):
+                mx.mxfp4_mm(wd, rows, cols, xd, nb, Y)
+            outs.append(Y)
+        torch.cuda.synchronize()
+        for Y in outs:
+            got = host(Y).reshape(nb, rows)
+            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
