@@ -173,3 +173,32 @@ def test_layer_with_many_experts(mx, E):
     ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
                              x, T, K, ids, wts)
     assert_within(y, ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32, f"{E} experts")
+
+
+def test_passes_repeated_on_one_workspace(mx):
+    # the passes' CTAs claim segments from a counter in the workspace, which the
+    # plan zeroes and the last CTA of every pass zeroes again: the down pass run
+    # three times on one plan, then a new plan on the same workspace, give the
+    # same bits each time (about 1000 gate/up and 250 down segments, several
+    # claims per CTA)
+    cfg, gate, up, down, x, ids, wts = make_case(64, 1024, 2048, 64, 4, 17)
+    act, ws = run_gate_up(mx, cfg, gate, up, x, ids)
+    act0 = host(act).copy()
+    outs = []
+    for _ in range(3):
+        y = empty(cfg.n_tokens * cfg.hidden)
+        mx.mxfp4_moe_down(to_dev(down), cfg.n_experts, cfg.hidden, cfg.inter, act,
+                          cfg.n_tokens, cfg.top_k, to_dev(ids), to_dev(wts), y, ws)
+        outs.append(host(y))
+    run_gate_up(mx, cfg, gate, up, x, ids, ws=ws, act=act)
+    assert_bits_equal(host(act), act0, "gate/up again on the same workspace")
+    y = empty(cfg.n_tokens * cfg.hidden)
+    mx.mxfp4_moe_down(to_dev(down), cfg.n_experts, cfg.hidden, cfg.inter, act, cfg.n_tokens,
+                      cfg.top_k, to_dev(ids), to_dev(wts), y, ws)
+    outs.append(host(y))
+    for o in outs[1:]:
+        assert_bits_equal(o, outs[0], "down again on the same workspace")
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, cfg.n_experts,
+                             cfg.hidden, cfg.inter, x, cfg.n_tokens, cfg.top_k, ids, wts)
+    assert_within(outs[0].reshape(cfg.n_tokens, cfg.hidden), ref["out"],
+                  ref["bound_l1"] + ref["bound_prop"], REL_FP32, "MoE layer")
