@@ -67,6 +67,12 @@ _SIG = {
     "mxo_moe_plan": (_I, [_P, _I, _I, _P, _P]),
     "mxo_moe_forward_ex": (None, [_P, _P, _P, _SZ, _SZ, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P,
                                   _I, ctypes.c_float, _P, _P, _P, _P]),
+    "mxo_q4k_nbytes": (_SZ, [_I, _I]),
+    "mxo_f16": (ctypes.c_float, [ctypes.c_uint]),
+    "mxo_q4k_scale_min": (None, [_P, _I, _P, _P]),
+    "mxo_q4k_weight_at": (ctypes.c_float, [_P, _I, _I, _I, _I]),
+    "mxo_q4k_dequant": (None, [_P, _I, _I, _P]),
+    "mxo_q4k_matmat": (None, [_P, _I, _I, _P, _I, _I, _I, _P, _P]),
 }
 
 
@@ -249,3 +255,39 @@ def moe_forward_ex(gate_bank, up_bank, down_bank, gu_stride, down_stride, n_slot
                              ctypes.addressof(n_cold))
     res["cold"] = cold[:n_cold.value].copy()
     return res
+
+
+# --- the second codec: GGUF Q4_K ------------------------------------------------
+
+def q4k_nbytes(rows: int, cols: int) -> int:
+    return int(lib().mxo_q4k_nbytes(rows, cols))
+
+
+def f16(bits: int) -> float:
+    return float(np.float32(lib().mxo_f16(bits)))
+
+
+def q4k_scale_min(scales12, j: int) -> tuple[int, int]:
+    q = _u8(scales12)
+    assert q.size >= 12
+    sc, m = np.zeros(1, dtype=np.uint32), np.zeros(1, dtype=np.uint32)
+    lib().mxo_q4k_scale_min(_ptr(q), j, _ptr(sc), _ptr(m))
+    return int(sc[0]), int(m[0])
+
+
+def q4k_dequant(w, rows: int, cols: int) -> np.ndarray:
+    w = _u8(w)
+    out = np.empty((rows, cols), dtype=np.float32)
+    lib().mxo_q4k_dequant(_ptr(w), rows, cols, _ptr(out))
+    return out
+
+
+def q4k_matmat(w, rows: int, cols: int, x, nb: int, r0: int = 0, r1: int | None = None):
+    """(y, l1), both float64 [nb, r1-r0]."""
+    r1 = rows if r1 is None else r1
+    w, x = _u8(w), _f32(x)
+    assert x.size >= nb * cols
+    y = np.empty((nb, r1 - r0), dtype=np.float64)
+    l1 = np.empty_like(y)
+    lib().mxo_q4k_matmat(_ptr(w), rows, cols, _ptr(x), nb, r0, r1, _ptr(y), _ptr(l1))
+    return y, l1

@@ -435,3 +435,86 @@ int mxo_moe_plan(const int32_t* ids, int n_pairs, int n_experts, int32_t* offset
     return invalid;
 }
 
+
+// ---- GGUF Q4_K (the second codec) ----------------------------------------
+
+namespace {
+constexpr int kQK = 256;          // elements per super-block
+constexpr int kQ4KBytes = 144;    // 2 + 2 + 12 + 128
+}  // namespace
+
+size_t mxo_q4k_nbytes(int rows, int cols) {
+    if (rows <= 0 || cols <= 0 || cols % kQK != 0) return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols / kQK) * kQ4KBytes;
+}
+
+// IEEE 754 binary16: sign bit 15, exponent bits 10-14 (bias 15), fraction bits
+// 0-9; exponent 0 is zero or subnormal (fraction * 2^-24), 31 is infinity or NaN.
+float mxo_f16(unsigned bits) {
+    const unsigned sign = (bits >> 15) & 1u, e = (bits >> 10) & 31u, f = bits & 1023u;
+    float v;
+    if (e == 0u) v = std::ldexp(static_cast<float>(f), -24);
+    else if (e == 31u) v = f == 0u ? std::numeric_limits<float>::infinity()
+                                   : std::numeric_limits<float>::quiet_NaN();
+    else v = std::ldexp(static_cast<float>(1024u + f), static_cast<int>(e) - 25);
+    return sign ? -v : v;
+}
+
+// q4k_scale_min_x86: sub-blocks 0-3 keep their 6-bit scale and min in the low six
+// bits of bytes j and j + 4; sub-blocks 4-7 take their low four bits from the two
+// nibbles of byte j + 4 and their high two bits from the top of bytes j - 4
+// (scale) and j (min).
+void mxo_q4k_scale_min(const uint8_t* q, int j, unsigned* sc, unsigned* m) {
+    if (j < 4) {
+        *sc = q[j] & 63u;
+        *m = q[j + 4] & 63u;
+    } else {
+        *sc = (q[j + 4] & 0x0Fu) | ((q[j - 4] >> 6) << 4);
+        *m = (q[j + 4] >> 4) | ((q[j] >> 6) << 4);
+    }
+}
+
+float mxo_q4k_weight_at(const uint8_t* w, int rows, int cols, int r, int c) {
+    (void)rows;
+    const uint8_t* blk =
+        w + (static_cast<size_t>(r) * (cols / kQK) + static_cast<size_t>(c / kQK)) * kQ4KBytes;
+    const int e = c % kQK, s = e / 64, p = e % 64;
+    const int j = 2 * s + (p >= 32 ? 1 : 0);                       // sub-block
+    const uint8_t byte = blk[16 + 32 * s + (p % 32)];
+    const unsigned q = p < 32 ? (byte & 0x0Fu) : (byte >> 4);
+    unsigned sc = 0, m = 0;
+    mxo_q4k_scale_min(blk + 4, j, &sc, &m);
+    const float d = mxo_f16(static_cast<unsigned>(blk[0]) | (static_cast<unsigned>(blk[1]) << 8));
+    const float dmin =
+        mxo_f16(static_cast<unsigned>(blk[2]) | (static_cast<unsigned>(blk[3]) << 8));
+    // d*sc*q and dmin*m are exact in float (at most 11+6+4 and 11+6 significant
+    // bits); the difference rounds once (the build has contraction off)
+    const float scaled = (d * static_cast<float>(sc)) * static_cast<float>(q);
+    const float mins = dmin * static_cast<float>(m);
+    return scaled - mins;
+}
+
+void mxo_q4k_dequant(const uint8_t* w, int rows, int cols, float* out) {
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c)
+            out[static_cast<size_t>(r) * cols + c] = mxo_q4k_weight_at(w, rows, cols, r, c);
+}
+
+void mxo_q4k_matmat(const uint8_t* w, int rows, int cols, const float* x, int nb, int r0,
+                    int r1, double* y, double* l1) {
+    const int nr = r1 - r0;
+    for (int t = 0; t < nb; ++t) {
+        const float* xt = x + static_cast<size_t>(t) * cols;
+        for (int r = r0; r < r1; ++r) {
+            double sum = 0.0, mag = 0.0;
+            for (int c = 0; c < cols; ++c) {
+                const double p = static_cast<double>(mxo_q4k_weight_at(w, rows, cols, r, c)) *
+                                 static_cast<double>(xt[c]);
+                sum += p;
+                mag += std::fabs(p);
+            }
+            y[static_cast<size_t>(t) * nr + (r - r0)] = sum;
+            l1[static_cast<size_t>(t) * nr + (r - r0)] = mag;
+        }
+    }
+}

@@ -167,6 +167,38 @@ void mxo_moe_forward_ex(const uint8_t* gate_bank, const uint8_t* up_bank,
 int mxo_moe_plan(const int32_t* ids, int n_pairs, int n_experts,
                  int32_t* offsets, int32_t* pair_of);
 
+/* ---- The second codec: GGUF Q4_K ("rlx-cpu 0.2.17 src/gguf_matmul.rs",
+ * q4k_dot_q8_block_avx2 and q4k_scale_min_x86, and the exact arm of
+ * gguf_matmul_bt_m1_parallel).  A super-block holds 256 elements in 144 bytes:
+ * d (IEEE binary16, bytes 0-1, little-endian), dmin (binary16, bytes 2-3), the
+ * packed 6-bit scales and mins of its eight 32-element sub-blocks (bytes 4-15)
+ * and 128 bytes of 4-bit codes (bytes 16-143).  Bytes 16 + 32 s + l (s < 4,
+ * l < 32) hold element 64 s + l in the low nibble (sub-block 2 s) and element
+ * 64 s + 32 + l in the high nibble (sub-block 2 s + 1).  A [rows, cols] matrix
+ * (cols a multiple of 256) is rows x cols/256 blocks, row-major.  Element value
+ * (the exact arm's on-the-fly f32 dequantisation): w = d*sc*q - dmin*m, the two
+ * products exact in float and one float rounding of their difference. */
+
+/* rows * cols/256 * 144, or 0 when cols % 256 != 0 or a size is not positive. */
+size_t mxo_q4k_nbytes(int rows, int cols);
+
+/* IEEE binary16 bits -> float (subnormals, infinities and NaN included). */
+float mxo_f16(unsigned bits);
+
+/* Scale and min of sub-block j (0..7) from the block's 12 packed bytes (the
+ * page's q4k_scale_min_x86). */
+void mxo_q4k_scale_min(const uint8_t* scales12, int j, unsigned* sc, unsigned* m);
+
+/* Decoded element w[r][c] as a float, and the whole matrix -> out[r*cols + c]. */
+float mxo_q4k_weight_at(const uint8_t* w, int rows, int cols, int r, int c);
+void mxo_q4k_dequant(const uint8_t* w, int rows, int cols, float* out);
+
+/* y[t*(r1-r0) + (r-r0)] = sum_c w[r][c] * x[t*cols + c] in double (w the decoded
+ * floats), l1 = sum_c |w[r][c] x[t*cols + c]|, for tokens t < nb and rows
+ * r0 <= r < r1. */
+void mxo_q4k_matmat(const uint8_t* w, int rows, int cols, const float* x, int nb, int r0,
+                    int r1, double* y, double* l1);
+
 #ifdef __cplusplus
 }
 #endif

@@ -170,6 +170,49 @@ def routes(seed: int, n_tokens: int, top_k: int, n_experts: int):
     return ids, weights
 
 
+# --- GGUF Q4_K buffers (the second codec) ---------------------------------------
+
+Q4K_BLOCK_BYTES = 144   # one 256-element super-block (layout: the library's q4k.h)
+
+
+def q4k_nbytes(rows: int, cols: int) -> int:
+    return rows * (cols // 256) * Q4K_BLOCK_BYTES
+
+
+def q4k_matrix(rows: int, cols: int, seed: int, d_lo: int = -12, d_hi: int = -9) -> np.ndarray:
+    """rows x cols/256 Q4_K super-blocks of seeded bytes.  Bytes 0-1 (d) and 2-3
+    (dmin) of each block are positive binary16 values 2^e (1 + f/1024), e uniform
+    in [d_lo, d_hi] and f in [0, 1023]; every other byte is uniform (any byte
+    pattern of the scales and codes is a valid encoding)."""
+    assert cols % 256 == 0
+    n_blk = rows * (cols // 256)
+    buf = uniform_int(substream(seed, "q4k/bytes"), n_blk * Q4K_BLOCK_BYTES, 0, 255).astype(
+        np.uint8).reshape(n_blk, Q4K_BLOCK_BYTES)
+    for k, tag in ((0, "q4k/d"), (2, "q4k/dmin")):
+        e = uniform_int(substream(seed, tag + "/e"), n_blk, d_lo, d_hi)
+        f = uniform_int(substream(seed, tag + "/f"), n_blk, 0, 1023)
+        bits = ((e + 15) << 10) | f
+        buf[:, k] = (bits & 0xFF).astype(np.uint8)
+        buf[:, k + 1] = (bits >> 8).astype(np.uint8)
+    return buf.reshape(-1)
+
+
+@dataclass(frozen=True)
+class Q4kConfig:
+    name: str
+    rows: int
+    cols: int
+    nb: int
+    seed: int
+
+    def weights(self) -> np.ndarray:
+        return q4k_matrix(self.rows, self.cols, self.seed)
+
+    def activations(self) -> np.ndarray:
+        return normal_f32(substream(self.seed, "x"), self.nb * self.cols).reshape(
+            self.nb, self.cols)
+
+
 # --- the workloads -----------------------------------------------------------
 
 @dataclass(frozen=True)
@@ -238,4 +281,6 @@ DECODE = MatConfig("mxfp4_mv decode GEMV 14336x4096", 14336, 4096, 1, seed=1)
 MM8 = MatConfig("mxfp4_mm small batch 4096x14336 nb=8", 4096, 14336, 8, seed=2)
 MOE = MoeConfig("MoE 64 experts 2880x2880 top-4, 32 tokens", 64, 2880, 2880, 32, 4, seed=3)
 PREFILL = MatConfig("mxfp4_mm prefill 4096x4096 nb=2048", 4096, 4096, 2048, seed=4)
+# the second codec: the same decode GEMV shape in GGUF Q4_K, f32 activations
+Q4K_DECODE = Q4kConfig("q4k_mv decode GEMV 14336x4096 (GGUF Q4_K)", 14336, 4096, 1, seed=5)
 CONFIGS = {"tiny": TINY, "decode": DECODE, "mm8": MM8, "moe": MOE, "prefill": PREFILL}
