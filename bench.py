@@ -301,6 +301,31 @@ class PrefillMm(Prefill):
         self.mx.mxfp4_mm(self.w, c.rows, c.cols, self.X, c.nb, self.Y)
 
 
+class Q4kDecode(Workload):
+    """The second codec: LAYERS distinct 14336x4096 GGUF Q4_K matrices, one token
+    (q4k_mv each, FP32 exact arm)."""
+
+    def __init__(self, mx, layers=LAYERS):
+        import torch
+        import synth
+        c = synth.Q4K_DECODE
+        self.mx, self.c = mx, c
+        self.name = c.name
+        w0 = c.weights()
+        self.ws = [_dev(w0) for _ in range(layers)]
+        self.x = _dev(c.activations().reshape(-1))
+        self.Y = torch.empty(layers, c.rows, dtype=torch.float32, device="cuda")
+        self.launches_per_step = layers
+        self.bytes_per_launch = mx.q4k_nbytes(c.rows, c.cols) + 4 * c.cols + 4 * c.rows
+        self.bytes_per_step = layers * self.bytes_per_launch
+        self.dominant = "q4k_mv (k_q4k_mm<1>: FP32, decoded values exact as the exact arm's)"
+
+    def step(self):
+        c = self.c
+        for w, y in zip(self.ws, self.Y):
+            self.mx.q4k_mv(w, c.rows, c.cols, self.x, y)
+
+
 class Dequant(Workload):
     """Standalone decode of the decode-GEMV matrix to float (mxfp4_dequant)."""
 
@@ -548,7 +573,7 @@ def run_profile(args):
     mx.mxfp4_set_launch_overlap(True)   # as in the timed bench
     cls = {"decode": DecodeGemv, "decode_fp32": DecodeGemvFp32, "mm8": SmallBatch,
            "moe": MoeLayer, "prefill": Prefill, "prefill_mm": PrefillMm,
-           "dequant": Dequant}
+           "dequant": Dequant, "q4k": Q4kDecode}
     w = cls[args.profile](mx)
     for _ in range(args.warmup):
         w.step()
@@ -573,7 +598,7 @@ def main():
                     help="extra seconds of the main step replayed while the clocks are sampled")
     ap.add_argument("--profile",
                     choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm",
-                             "dequant"],
+                             "dequant", "q4k"],
                     help="run only this workload's warm-up and timed steps (eagerly, one "
                          "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()
@@ -636,7 +661,7 @@ def main():
 
     workloads = {}
     if not args.only_main:
-        for cls in (SmallBatch, MoeLayer, Prefill, PrefillMm, Tiny):
+        for cls in (SmallBatch, MoeLayer, Prefill, PrefillMm, Q4kDecode, Tiny):
             try:
                 w = cls(mx)
                 k = max(args.steps, 20)

@@ -1,4 +1,4 @@
-"""Python binding of libmxfp4.so (the C ABI in include/mxfp4.h).
+"""Python binding of libmxfp4.so (the C ABI in include/mxfp4.h and include/q4k.h).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels of the library.  Tensors are torch CUDA tensors (device memory and
@@ -19,7 +19,7 @@ __all__ = [
     "mxfp4_moe_workspace_bytes", "mxfp4_moe_gate_up", "mxfp4_moe_down",
     "mxfp4_moe_plan_errors", "mxfp4_moe_layer_noalloc", "mxfp4_moe_gate_up_ex",
     "mxfp4_moe_down_ex", "mxfp4_moe_cold_pairs", "mxfp4_moe_gate_up_seg", "mxfp4_moe_down_seg",
-    "MOE_MODE_F32", "MOE_MODE_V41",
+    "MOE_MODE_F32", "MOE_MODE_V41", "q4k_nbytes", "q4k_dequant", "q4k_mv", "q4k_mm",
     "mxfp4_status_string", "MM_SMALL_MAX", "EXPORTED_SYMBOLS",
 ]
 
@@ -59,6 +59,11 @@ _SIG = {
     "mxfp4_moe_gate_up_seg": (_I, [_P, _P, _I, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _I,
                                    ctypes.c_float, _P, _P, _SZ, _P]),
     "mxfp4_moe_down_seg": (_I, [_P, _I, _I, _I, _I, _P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
+    # the second codec (include/q4k.h)
+    "q4k_nbytes": (_SZ, [_I, _I]),
+    "q4k_dequant": (_I, [_P, _I, _I, _P, _P]),
+    "q4k_mv": (_I, [_P, _I, _I, _P, _P, _P]),
+    "q4k_mm": (_I, [_P, _I, _I, _P, _I, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIG)
 _lib = None
@@ -293,3 +298,23 @@ def mxfp4_moe_down_seg(down_segments, segment_slots, hidden, inter, act, n_token
     _check("mxfp4_moe_down_seg", lib().mxfp4_moe_down_seg(
         ctypes.cast(d, _P), len(down_segments), segment_slots, hidden, inter, _addr(act), n_tokens,
         top_k, _addr(route_w), int(mode), _addr(y), _addr(workspace), ws_bytes, _stream(stream)))
+
+
+# --- the second codec: GGUF Q4_K (include/q4k.h) --------------------------------
+
+def q4k_nbytes(rows: int, cols: int) -> int:
+    return int(lib().q4k_nbytes(rows, cols))
+
+
+def q4k_dequant(w, rows, cols, out, stream=None):
+    _check("q4k_dequant", lib().q4k_dequant(_addr(w), rows, cols, _addr(out),
+                                            _stream(stream)))
+
+
+def q4k_mv(w, rows, cols, x, y, stream=None):
+    _check("q4k_mv", lib().q4k_mv(_addr(w), rows, cols, _addr(x), _addr(y), _stream(stream)))
+
+
+def q4k_mm(w, rows, cols, X, nb, Y, stream=None):
+    _check("q4k_mm", lib().q4k_mm(_addr(w), rows, cols, _addr(X), nb, _addr(Y),
+                                  _stream(stream)))

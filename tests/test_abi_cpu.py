@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds and loads, exports every entry
-point include/mxfp4.h declares, and refuses bad arguments with the documented
+point include/*.h declares, and refuses bad arguments with the documented
 status codes before touching CUDA."""
 import ctypes
 import os
@@ -20,10 +20,14 @@ def mx():
 
 
 def header_functions():
-    with open(os.path.join(ROOT, "include", "mxfp4.h")) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mxfp4_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            with open(os.path.join(inc, fn)) as f:
+                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+            names |= set(re.findall(r"\b((?:mxfp4|q4k)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported(mx):
@@ -31,7 +35,7 @@ def test_every_declared_symbol_is_exported(mx):
     assert len(names) >= 14, names
     h = ctypes.CDLL(mx.library_path)
     for n in names:
-        assert hasattr(h, n), f"{n} declared in include/mxfp4.h but not exported"
+        assert hasattr(h, n), f"{n} declared in include/*.h but not exported"
     assert set(names) == set(mx.EXPORTED_SYMBOLS), "binding and header disagree"
 
 
@@ -118,3 +122,18 @@ def test_product_path_does_not_touch_the_oracle():
                 assert "oracle" not in text.replace("Oracle", "oracle").split("\n#")[0] or \
                     "import oracle" not in text, fn
                 assert "import oracle" not in text and "mxfp4_oracle" not in text, fn
+
+
+def test_q4k_nbytes_and_refusals(mx):
+    # 144 bytes per 256 elements; cols must be a multiple of 256
+    assert mx.q4k_nbytes(14336, 4096) == 14336 * 16 * 144
+    assert mx.q4k_nbytes(1, 256) == 144
+    for bad in [(0, 256), (4, 128), (4, 320), (-1, 256)]:
+        assert mx.q4k_nbytes(*bad) == 0
+    L = mx.lib()
+    assert L.q4k_mv(A, 8, 320, A, A, None) == 1      # cols not a multiple of 256
+    assert L.q4k_mv(A, 0, 256, A, A, None) == 1
+    assert L.q4k_mv(MIS, 8, 256, A, A, None) == 2    # misaligned weights
+    assert L.q4k_mv(A, 8, 256, None, A, None) == 2
+    assert L.q4k_mm(A, 8, 256, A, 0, A, None) == 1   # no tokens
+    assert L.q4k_dequant(A, 8, 256, MIS, None) == 2
