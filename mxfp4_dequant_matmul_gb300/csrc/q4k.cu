@@ -2,16 +2,18 @@
 // and element values in include/q4k.h; "rlx-cpu 0.2.17 src/gguf_matmul.rs",
 // the exact arm of gguf_matmul_bt_m1_parallel and its Q4_K block dot).
 //
-// Work: one warp per row, one 144-byte super-block per step, lane l taking the
-// 32-bit code word at bytes 16 + 4 l: the low nibbles of its four bytes are
+// Work: one warp per row, eight 144-byte super-blocks per step (their loads in
+// flight together, their headers unpacked by the lanes together), lane l taking
+// the 32-bit code word at bytes 16 + 4 l of each: the low nibbles of its four bytes are
 // elements 64 s + 4 (l % 8) + b of sub-block 2 s (s = l / 8), the high nibbles
 // the same positions + 32 of sub-block 2 s + 1.  The word's nibbles are spread
 // into bytes (two logic operations) and each byte lands in the mantissa of
 // 2^23 (one byte permute), so that one FMA gives d sc q exactly and one
-// subtraction rounds d sc q - dmin m once, as the exact arm does; the FP32
-// products with x then go into two chains (low and high nibbles) per word,
-// four sums per lane by super-block index mod 4, ((S0 + S1) + S2) + S3 and a
-// fixed warp tree.  Up to eight tokens share each decoded word.
+// subtraction rounds d sc q - dmin m once, as the exact arm does (two elements
+// per packed FP32x2 operation); the FP32 products with x then go into two
+// chains (even and odd elements) per word, four sums per lane by super-block
+// index mod 4, ((S0 + S1) + S2) + S3 and a fixed warp tree.  Up to eight tokens
+// share each decoded word.
 #include <cstdint>
 
 #include <cuda_fp16.h>
@@ -24,7 +26,7 @@ namespace {
 constexpr int kQK = 256;
 constexpr int kBlk = 144;
 constexpr int kWarpsQ = 8;
-constexpr int kUnrollQ = 4;   // super-blocks whose loads are in flight together
+constexpr int kUnrollQ = 8;   // super-blocks per step: their loads in flight together
 
 __device__ __forceinline__ uint4 ldg_u4(const void* p) {
     uint4 v;
@@ -74,20 +76,33 @@ __device__ __forceinline__ Factors block_factors(const uint4 hdr, int s) {
 // The 8 element values of a code word: v[b] = low nibble of byte b (first
 // sub-block), v[4 + b] = high nibble (second).  q lands in the low mantissa
 // bits of 2^23 (one byte permute), so that for finite factors
-// fma(a, 2^23 + q, -a 2^23) = a q exactly; a block with an infinite or NaN d
-// or dmin takes q as a float and a q as a product, as the definition does.
-__device__ __forceinline__ void word_values(uint32_t word, const Factors& f, float (&v)[8]) {
+// fma(a, 2^23 + q, -a 2^23) = a q exactly; with an infinite or NaN d or dmin
+// (finite = false) q is taken as a float and a q as a product, as the
+// definition does.
+__device__ __forceinline__ void word_values(uint32_t word, const Factors& f, bool finite,
+                                            float (&v)[8]) {
     const uint32_t lo = word & 0x0F0F0F0Fu, hi = (word >> 4) & 0x0F0F0F0Fu;
     const uint32_t magic = 0x4B000000u;
-    if (isfinite(f.a0) && isfinite(f.a1) && isfinite(f.b0) && isfinite(f.b1)) {
-        const float na0 = -f.a0 * 8388608.0f, na1 = -f.a1 * 8388608.0f;
+    if (finite) {
+        // two elements per packed FP32x2 operation (each lane of it rounds as
+        // the scalar operation would)
+        const float2 a0 = make_float2(f.a0, f.a0), a1 = make_float2(f.a1, f.a1);
+        const float2 na0 = make_float2(-f.a0 * 8388608.0f, -f.a0 * 8388608.0f);
+        const float2 na1 = make_float2(-f.a1 * 8388608.0f, -f.a1 * 8388608.0f);
+        const float2 nb0 = make_float2(-f.b0, -f.b0), nb1 = make_float2(-f.b1, -f.b1);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            // byte b of lo / hi into byte 0, bytes 1-3 from magic (0x00, 0x00, 0x4B)
-            const float ql = __uint_as_float(__byte_perm(lo, magic, 0x7650u + b));
-            const float qh = __uint_as_float(__byte_perm(hi, magic, 0x7650u + b));
-            v[b] = __fsub_rn(__fmaf_rn(f.a0, ql, na0), f.b0);
-            v[4 + b] = __fsub_rn(__fmaf_rn(f.a1, qh, na1), f.b1);
+        for (int b = 0; b < 4; b += 2) {
+            // bytes b, b+1 of lo / hi into byte 0, bytes 1-3 from magic (0x00, 0x00, 0x4B)
+            const float2 ql = make_float2(__uint_as_float(__byte_perm(lo, magic, 0x7650u + b)),
+                                          __uint_as_float(__byte_perm(lo, magic, 0x7651u + b)));
+            const float2 qh = make_float2(__uint_as_float(__byte_perm(hi, magic, 0x7650u + b)),
+                                          __uint_as_float(__byte_perm(hi, magic, 0x7651u + b)));
+            const float2 wl = __fadd2_rn(__ffma2_rn(a0, ql, na0), nb0);
+            const float2 wh = __fadd2_rn(__ffma2_rn(a1, qh, na1), nb1);
+            v[b] = wl.x;
+            v[b + 1] = wl.y;
+            v[4 + b] = wh.x;
+            v[4 + b + 1] = wh.y;
         }
     } else {
 #pragma unroll
@@ -123,36 +138,43 @@ __global__ void __launch_bounds__(kWarpsQ * 32)
     for (int t = 0; t < NB; ++t) xt[t] = X + static_cast<size_t>(t0 + min(t, nbt - 1)) * cols;
 
     for (int b0 = 0; b0 < bpr; b0 += kUnrollQ) {
-        uint4 hdr[kUnrollQ];
+        // the step's eight headers are read and unpacked by the lanes together:
+        // lane l takes super-block b0 + l / 4 and its sub-blocks 2 (l % 4) and
+        // 2 (l % 4) + 1; the lanes of sub-blocks 2 s, 2 s + 1 then fetch theirs
+        // from lane 4 u + s for super-block b0 + u
+        const uint4 hdr = ldg_u4(rb + static_cast<size_t>(min(b0 + (lane >> 2), bpr - 1)) * kBlk);
         uint32_t code[kUnrollQ];
 #pragma unroll
         for (int u = 0; u < kUnrollQ; ++u) {
             const int b = min(b0 + u, bpr - 1);   // (past the row's end: a repeat, unused)
-            hdr[u] = ldg_u4(rb + static_cast<size_t>(b) * kBlk);
             code[u] = ldg_u32(rb + static_cast<size_t>(b) * kBlk + 16 + 4 * lane);
         }
+        const Factors fl = block_factors(hdr, lane & 3);
+        const bool finite = __all_sync(0xffffffffu, isfinite(fl.a0) && isfinite(fl.b0) &&
+                                                        isfinite(fl.a1) && isfinite(fl.b1));
 #pragma unroll
         for (int u = 0; u < kUnrollQ; ++u) {
             const int b = b0 + u;
+            Factors f;
+            f.a0 = __shfl_sync(0xffffffffu, fl.a0, 4 * u + s);
+            f.b0 = __shfl_sync(0xffffffffu, fl.b0, 4 * u + s);
+            f.a1 = __shfl_sync(0xffffffffu, fl.a1, 4 * u + s);
+            f.b1 = __shfl_sync(0xffffffffu, fl.b1, 4 * u + s);
             if (b < bpr) {
-                const Factors f = block_factors(hdr[u], s);
                 float v[8];
-                word_values(code[u], f, v);
+                word_values(code[u], f, finite, v);
 #pragma unroll
                 for (int t = 0; t < NB; ++t) {
                     if (NB > 1 && t >= nbt) break;
                     const float* xb = xt[t] + static_cast<size_t>(b) * kQK + e_lo;
                     const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
                     const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 32));
-                    float cl = __fmul_rn(v[0], xl.x);
-                    cl = __fmaf_rn(v[1], xl.y, cl);
-                    cl = __fmaf_rn(v[2], xl.z, cl);
-                    cl = __fmaf_rn(v[3], xl.w, cl);
-                    float ch = __fmul_rn(v[4], xh.x);
-                    ch = __fmaf_rn(v[5], xh.y, ch);
-                    ch = __fmaf_rn(v[6], xh.z, ch);
-                    ch = __fmaf_rn(v[7], xh.w, ch);
-                    acc[t][u] = __fadd_rn(acc[t][u], __fadd_rn(cl, ch));
+                    // packed products: chain .x takes the even elements, .y the odd
+                    float2 c = __fmul2_rn(make_float2(v[0], v[1]), make_float2(xl.x, xl.y));
+                    c = __ffma2_rn(make_float2(v[2], v[3]), make_float2(xl.z, xl.w), c);
+                    c = __ffma2_rn(make_float2(v[4], v[5]), make_float2(xh.x, xh.y), c);
+                    c = __ffma2_rn(make_float2(v[6], v[7]), make_float2(xh.z, xh.w), c);
+                    acc[t][u & 3] = __fadd_rn(acc[t][u & 3], __fadd_rn(c.x, c.y));
                 }
             }
         }
@@ -181,7 +203,9 @@ __global__ void k_q4k_dequant(const uint8_t* __restrict__ w, int rows, int cols,
         const uint32_t code = ldg_u32(p + 16 + 4 * lane);
         const int s = lane >> 3;
         float v[8];
-        word_values(code, block_factors(hdr, s), v);
+        const Factors f = block_factors(hdr, s);
+        word_values(code, f, isfinite(f.a0) && isfinite(f.b0) && isfinite(f.a1) && isfinite(f.b1),
+                    v);
         const size_t row = blk / bpr, b = blk - row * bpr;
         float* o = out + row * cols + b * kQK + 64 * s + 4 * (lane & 7);
         *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
