@@ -120,72 +120,74 @@ __global__ void __launch_bounds__(kWarpsQ * 32)
     k_q4k_mm(const uint8_t* __restrict__ w, int rows, int cols, const float* __restrict__ X,
              int nb, float* __restrict__ Y) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row = blockIdx.x * kWarpsQ + warp;
-    if (row >= rows) return;
     const int t0 = blockIdx.y * NB;
     const int nbt = min(NB, nb - t0);
     const int bpr = cols / kQK;
     const int s = lane >> 3;
     const int e_lo = 64 * s + 4 * (lane & 7);   // this lane's first low-nibble element
-    const uint8_t* rb = w + static_cast<size_t>(row) * bpr * kBlk;
-    float acc[NB][4];
-#pragma unroll
-    for (int t = 0; t < NB; ++t)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
     const float* xt[NB];
 #pragma unroll
     for (int t = 0; t < NB; ++t) xt[t] = X + static_cast<size_t>(t0 + min(t, nbt - 1)) * cols;
+    // rows dealt to the warps in turn (a grid of one wave)
+    for (int row = blockIdx.x * kWarpsQ + warp; row < rows;
+         row += static_cast<int>(gridDim.x) * kWarpsQ) {
+        const uint8_t* rb = w + static_cast<size_t>(row) * bpr * kBlk;
+        float acc[NB][4];
+#pragma unroll
+        for (int t = 0; t < NB; ++t)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
 
-    for (int b0 = 0; b0 < bpr; b0 += kUnrollQ) {
-        // the step's eight headers are read and unpacked by the lanes together:
-        // lane l takes super-block b0 + l / 4 and its sub-blocks 2 (l % 4) and
-        // 2 (l % 4) + 1; the lanes of sub-blocks 2 s, 2 s + 1 then fetch theirs
-        // from lane 4 u + s for super-block b0 + u
-        const uint4 hdr = ldg_u4(rb + static_cast<size_t>(min(b0 + (lane >> 2), bpr - 1)) * kBlk);
-        uint32_t code[kUnrollQ];
+        for (int b0 = 0; b0 < bpr; b0 += kUnrollQ) {
+            // the step's eight headers are read and unpacked by the lanes together:
+            // lane l takes super-block b0 + l / 4 and its sub-blocks 2 (l % 4) and
+            // 2 (l % 4) + 1; the lanes of sub-blocks 2 s, 2 s + 1 then fetch theirs
+            // from lane 4 u + s for super-block b0 + u
+            const uint4 hdr = ldg_u4(rb + static_cast<size_t>(min(b0 + (lane >> 2), bpr - 1)) * kBlk);
+            uint32_t code[kUnrollQ];
 #pragma unroll
-        for (int u = 0; u < kUnrollQ; ++u) {
-            const int b = min(b0 + u, bpr - 1);   // (past the row's end: a repeat, unused)
-            code[u] = ldg_u32(rb + static_cast<size_t>(b) * kBlk + 16 + 4 * lane);
-        }
-        const Factors fl = block_factors(hdr, lane & 3);
-        const bool finite = __all_sync(0xffffffffu, isfinite(fl.a0) && isfinite(fl.b0) &&
-                                                        isfinite(fl.a1) && isfinite(fl.b1));
+            for (int u = 0; u < kUnrollQ; ++u) {
+                const int b = min(b0 + u, bpr - 1);   // (past the row's end: a repeat, unused)
+                code[u] = ldg_u32(rb + static_cast<size_t>(b) * kBlk + 16 + 4 * lane);
+            }
+            const Factors fl = block_factors(hdr, lane & 3);
+            const bool finite = __all_sync(0xffffffffu, isfinite(fl.a0) && isfinite(fl.b0) &&
+                                                            isfinite(fl.a1) && isfinite(fl.b1));
 #pragma unroll
-        for (int u = 0; u < kUnrollQ; ++u) {
-            const int b = b0 + u;
-            Factors f;
-            f.a0 = __shfl_sync(0xffffffffu, fl.a0, 4 * u + s);
-            f.b0 = __shfl_sync(0xffffffffu, fl.b0, 4 * u + s);
-            f.a1 = __shfl_sync(0xffffffffu, fl.a1, 4 * u + s);
-            f.b1 = __shfl_sync(0xffffffffu, fl.b1, 4 * u + s);
-            if (b < bpr) {
-                float v[8];
-                word_values(code[u], f, finite, v);
+            for (int u = 0; u < kUnrollQ; ++u) {
+                const int b = b0 + u;
+                Factors f;
+                f.a0 = __shfl_sync(0xffffffffu, fl.a0, 4 * u + s);
+                f.b0 = __shfl_sync(0xffffffffu, fl.b0, 4 * u + s);
+                f.a1 = __shfl_sync(0xffffffffu, fl.a1, 4 * u + s);
+                f.b1 = __shfl_sync(0xffffffffu, fl.b1, 4 * u + s);
+                if (b < bpr) {
+                    float v[8];
+                    word_values(code[u], f, finite, v);
 #pragma unroll
-                for (int t = 0; t < NB; ++t) {
-                    if (NB > 1 && t >= nbt) break;
-                    const float* xb = xt[t] + static_cast<size_t>(b) * kQK + e_lo;
-                    const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
-                    const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 32));
-                    // packed products: chain .x takes the even elements, .y the odd
-                    float2 c = __fmul2_rn(make_float2(v[0], v[1]), make_float2(xl.x, xl.y));
-                    c = __ffma2_rn(make_float2(v[2], v[3]), make_float2(xl.z, xl.w), c);
-                    c = __ffma2_rn(make_float2(v[4], v[5]), make_float2(xh.x, xh.y), c);
-                    c = __ffma2_rn(make_float2(v[6], v[7]), make_float2(xh.z, xh.w), c);
-                    acc[t][u & 3] = __fadd_rn(acc[t][u & 3], __fadd_rn(c.x, c.y));
+                    for (int t = 0; t < NB; ++t) {
+                        if (NB > 1 && t >= nbt) break;
+                        const float* xb = xt[t] + static_cast<size_t>(b) * kQK + e_lo;
+                        const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
+                        const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 32));
+                        // packed products: chain .x takes the even elements, .y the odd
+                        float2 c = __fmul2_rn(make_float2(v[0], v[1]), make_float2(xl.x, xl.y));
+                        c = __ffma2_rn(make_float2(v[2], v[3]), make_float2(xl.z, xl.w), c);
+                        c = __ffma2_rn(make_float2(v[4], v[5]), make_float2(xh.x, xh.y), c);
+                        c = __ffma2_rn(make_float2(v[6], v[7]), make_float2(xh.z, xh.w), c);
+                        acc[t][u & 3] = __fadd_rn(acc[t][u & 3], __fadd_rn(c.x, c.y));
+                    }
                 }
             }
         }
-    }
 #pragma unroll
-    for (int t = 0; t < NB; ++t) {
-        if (NB > 1 && t >= nbt) break;
-        float v = __fadd_rn(__fadd_rn(__fadd_rn(acc[t][0], acc[t][1]), acc[t][2]), acc[t][3]);
+        for (int t = 0; t < NB; ++t) {
+            if (NB > 1 && t >= nbt) break;
+            float v = __fadd_rn(__fadd_rn(__fadd_rn(acc[t][0], acc[t][1]), acc[t][2]), acc[t][3]);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (lane == 0) Y[static_cast<size_t>(t0 + t) * rows + row] = v;
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) Y[static_cast<size_t>(t0 + t) * rows + row] = v;
+        }
     }
 }
 
@@ -216,8 +218,20 @@ __global__ void k_q4k_dequant(const uint8_t* __restrict__ w, int rows, int cols,
 template <int NB>
 cudaError_t launch_q4k(const uint8_t* w, int rows, int cols, const float* X, int nb, float* Y,
                        cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>((rows + kWarpsQ - 1) / kWarpsQ),
-                    static_cast<unsigned>((nb + NB - 1) / NB));
+    // one wave: as many CTAs as the SMs hold at once, each warp taking rows in turn
+    static mxk::PerDevice memo;
+    const int per_wave = memo.get([] {
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_q4k_mm<NB>, kWarpsQ * 32,
+                                                          0) != cudaSuccess)
+            return 0;
+        return sms * per_sm;
+    });
+    const int need = (rows + kWarpsQ - 1) / kWarpsQ;
+    const int gx = per_wave > 0 && per_wave < need ? per_wave : need;
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>((nb + NB - 1) / NB));
     k_q4k_mm<NB><<<grid, kWarpsQ * 32, 0, s>>>(w, rows, cols, X, nb, Y);
     return cudaGetLastError();
 }
