@@ -127,7 +127,8 @@ int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
  *     dequant, as mxfp4_mm_bf16_ws) into a device workspace the library keeps
  *     per (device, stream): allocated on the stream (stream-ordered) by the
  *     first call that needs it, grown by later ones, never while the stream is
- *     being captured into a graph, and kept until the process ends
+ *     being captured into a graph, and kept while the context lives (one
+ *     made before a device reset is dropped, not reused)
  *     (mxfp4_mm_bf16_workspace_bytes(rows, cols, nb) bytes).  Without one (a
  *     capture before any eager call on that stream, or an allocation failure)
  *     the conversion runs inside the GEMM (mxfp4_mm_bf16); the results are the

@@ -142,6 +142,10 @@ cudaError_t read_fault_moetc(int* value, bool reset);
 // Records a CUDA error for mxfp4_last_cuda_error() (this thread).
 void record_cuda_error(int err);
 
+// Unique id of the calling thread's current context (0 if the driver cannot
+// say): an address cached under one context is not used under another.
+unsigned long long current_context_id();
+
 // A value computed once per device and then reused: kernel attributes (the
 // dynamic shared-memory limit), SM counts and occupancies belong to a device,
 // so a value obtained with one device current is never reused on another.

@@ -36,30 +36,6 @@ std::mutex g_addr_mu;
 void* g_addr[kMaxDevices] = {};
 unsigned long long g_addr_ctx[kMaxDevices] = {};
 
-// Unique id of the calling thread's current context (0 if the driver cannot
-// say): an address cached under one context is not used under another.
-unsigned long long current_context_id() {
-    static std::once_flag once;
-    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
-    static PFN_cuCtxGetId_v12000 get_id = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-    });
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
-        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
-        return 0;
-    return id;
-}
-
 // Device address of g_moe_scratch on the current device: looked up on the
 // first call per device (and again after the device's context was replaced),
 // then cached.
@@ -70,7 +46,7 @@ cudaError_t scratch_address(void** out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     // 0 before the runtime has made a context current: then the lookup below
     // runs (and makes it current), and the next call caches under its id
-    const unsigned long long ctx = current_context_id();
+    const unsigned long long ctx = mxk::current_context_id();
     std::lock_guard<std::mutex> lock(g_addr_mu);
     if (g_addr[dev] == nullptr || ctx == 0 || ctx != g_addr_ctx[dev]) {
         void* p = nullptr;
@@ -92,6 +68,30 @@ bool shape_ok(int rows, int cols) {
 }
 
 }  // namespace
+
+// Unique id of the calling thread's current context (0 if the driver cannot
+// say): an address cached under one context is not used under another.
+unsigned long long mxk::current_context_id() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 extern "C" int mxfp4_moe_layer_noalloc(const void* gate_bank, const void* up_bank,
                                        const void* down_bank, int n_experts, int hidden,

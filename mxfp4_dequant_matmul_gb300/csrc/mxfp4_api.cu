@@ -59,19 +59,29 @@ const uint8_t* u8(const void* p) { return static_cast<const uint8_t*>(p); }
 // order, so concurrent streams never share one.  Grown by stream-ordered
 // allocation (the old one freed after the work already queued on the stream);
 // never allocated while the stream is being captured into a graph; kept for the
-// life of the process.  nullptr when none can be had: the caller then takes the
-// path that needs no workspace (the same results bit for bit).
+// life of the context (an entry made under another context, before a device
+// reset, is dropped: its memory went with that context).  nullptr when none can
+// be had: the caller then takes the path that needs no workspace (the same
+// results bit for bit).
 void* stream_workspace(cudaStream_t s, size_t need) {
+    struct Entry {
+        void* ptr;
+        size_t bytes;
+        unsigned long long ctx;
+    };
     static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> cache;
+    static std::map<std::pair<int, cudaStream_t>, Entry> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return nullptr;
     }
+    const unsigned long long ctx = mxk::current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    std::pair<void*, size_t>& e = cache[{dev, s}];
-    if (e.first != nullptr && e.second >= need) return e.first;
+    Entry& e = cache[{dev, s}];
+    if (e.ptr != nullptr && (ctx == 0 || e.ctx != ctx)) e = Entry{nullptr, 0, 0};
+    if (e.ptr != nullptr && e.bytes >= need) return e.ptr;
+    if (ctx == 0) return nullptr;
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &st) != cudaSuccess || st != cudaStreamCaptureStatusNone) {
         (void)cudaGetLastError();
@@ -82,8 +92,8 @@ void* stream_workspace(cudaStream_t s, size_t need) {
         (void)cudaGetLastError();
         return nullptr;
     }
-    if (e.first != nullptr) (void)cudaFreeAsync(e.first, s);
-    e = {p, need};
+    if (e.ptr != nullptr) (void)cudaFreeAsync(e.ptr, s);
+    e = Entry{p, need, ctx};
     return p;
 }
 
