@@ -7,10 +7,10 @@
 // the 32-bit code word at bytes 16 + 4 l of each: the low nibbles of its four bytes are
 // elements 64 s + 4 (l % 8) + b of sub-block 2 s (s = l / 8), the high nibbles
 // the same positions + 32 of sub-block 2 s + 1.  The word's nibbles are spread
-// into bytes (two logic operations) and each byte lands in the mantissa of
-// 2^23 (one byte permute), so that one FMA gives d sc q exactly and one
-// subtraction rounds d sc q - dmin m once, as the exact arm does (two elements
-// per packed FP32x2 operation); the FP32 products with x then go into two
+// into bytes (two logic operations), each byte lands in the mantissa of 2^23
+// (one byte permute), one subtraction of 2^23 gives q and one FMA rounds
+// d sc q - dmin m once, as the exact arm does (two elements per packed FP32x2
+// operation); the FP32 products with x then go into two
 // chains (even and odd elements) per word, four sums per lane by super-block
 // index mod 4, ((S0 + S1) + S2) + S3 and a fixed warp tree.  Up to eight tokens
 // share each decoded word.
@@ -75,8 +75,8 @@ __device__ __forceinline__ Factors block_factors(const uint4 hdr, int s) {
 
 // The 8 element values of a code word: v[b] = low nibble of byte b (first
 // sub-block), v[4 + b] = high nibble (second).  q lands in the low mantissa
-// bits of 2^23 (one byte permute), so that for finite factors
-// fma(a, 2^23 + q, -a 2^23) = a q exactly; with an infinite or NaN d or dmin
+// bits of 2^23 (one byte permute), one subtraction of 2^23 gives q exactly and
+// fma(a, q, -b) rounds the exact a q - b once; with an infinite or NaN d or dmin
 // (finite = false) q is taken as a float and a q as a product, as the
 // definition does.
 __device__ __forceinline__ void word_values(uint32_t word, const Factors& f, bool finite,
@@ -87,9 +87,8 @@ __device__ __forceinline__ void word_values(uint32_t word, const Factors& f, boo
         // two elements per packed FP32x2 operation (each lane of it rounds as
         // the scalar operation would)
         const float2 a0 = make_float2(f.a0, f.a0), a1 = make_float2(f.a1, f.a1);
-        const float2 na0 = make_float2(-f.a0 * 8388608.0f, -f.a0 * 8388608.0f);
-        const float2 na1 = make_float2(-f.a1 * 8388608.0f, -f.a1 * 8388608.0f);
         const float2 nb0 = make_float2(-f.b0, -f.b0), nb1 = make_float2(-f.b1, -f.b1);
+        const float2 n23 = make_float2(-8388608.0f, -8388608.0f);
 #pragma unroll
         for (int b = 0; b < 4; b += 2) {
             // bytes b, b+1 of lo / hi into byte 0, bytes 1-3 from magic (0x00, 0x00, 0x4B)
@@ -97,8 +96,9 @@ __device__ __forceinline__ void word_values(uint32_t word, const Factors& f, boo
                                           __uint_as_float(__byte_perm(lo, magic, 0x7651u + b)));
             const float2 qh = make_float2(__uint_as_float(__byte_perm(hi, magic, 0x7650u + b)),
                                           __uint_as_float(__byte_perm(hi, magic, 0x7651u + b)));
-            const float2 wl = __fadd2_rn(__ffma2_rn(a0, ql, na0), nb0);
-            const float2 wh = __fadd2_rn(__ffma2_rn(a1, qh, na1), nb1);
+            // q = (2^23 + q) - 2^23 exactly; a q - b rounded once by the FMA
+            const float2 wl = __ffma2_rn(a0, __fadd2_rn(ql, n23), nb0);
+            const float2 wh = __ffma2_rn(a1, __fadd2_rn(qh, n23), nb1);
             v[b] = wl.x;
             v[b + 1] = wl.y;
             v[4 + b] = wh.x;
@@ -161,22 +161,22 @@ __global__ void __launch_bounds__(kWarpsQ * 32)
                 f.b0 = __shfl_sync(0xffffffffu, fl.b0, 4 * u + s);
                 f.a1 = __shfl_sync(0xffffffffu, fl.a1, 4 * u + s);
                 f.b1 = __shfl_sync(0xffffffffu, fl.b1, 4 * u + s);
-                if (b < bpr) {
-                    float v[8];
-                    word_values(code[u], f, finite, v);
+                // (past the row's end: the last block again, its sum not added,
+                // so that the control flow stays the same for every lane)
+                float v[8];
+                word_values(code[u], f, finite, v);
 #pragma unroll
-                    for (int t = 0; t < NB; ++t) {
-                        if (NB > 1 && t >= nbt) break;
-                        const float* xb = xt[t] + static_cast<size_t>(b) * kQK + e_lo;
-                        const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
-                        const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 32));
-                        // packed products: chain .x takes the even elements, .y the odd
-                        float2 c = __fmul2_rn(make_float2(v[0], v[1]), make_float2(xl.x, xl.y));
-                        c = __ffma2_rn(make_float2(v[2], v[3]), make_float2(xl.z, xl.w), c);
-                        c = __ffma2_rn(make_float2(v[4], v[5]), make_float2(xh.x, xh.y), c);
-                        c = __ffma2_rn(make_float2(v[6], v[7]), make_float2(xh.z, xh.w), c);
-                        acc[t][u & 3] = __fadd_rn(acc[t][u & 3], __fadd_rn(c.x, c.y));
-                    }
+                for (int t = 0; t < NB; ++t) {
+                    if (NB > 1 && t >= nbt) break;
+                    const float* xb = xt[t] + static_cast<size_t>(min(b, bpr - 1)) * kQK + e_lo;
+                    const float4 xl = __ldg(reinterpret_cast<const float4*>(xb));
+                    const float4 xh = __ldg(reinterpret_cast<const float4*>(xb + 32));
+                    // packed products: chain .x takes the even elements, .y the odd
+                    float2 c = __fmul2_rn(make_float2(v[0], v[1]), make_float2(xl.x, xl.y));
+                    c = __ffma2_rn(make_float2(v[2], v[3]), make_float2(xl.z, xl.w), c);
+                    c = __ffma2_rn(make_float2(v[4], v[5]), make_float2(xh.x, xh.y), c);
+                    c = __ffma2_rn(make_float2(v[6], v[7]), make_float2(xh.z, xh.w), c);
+                    if (b < bpr) acc[t][u & 3] = __fadd_rn(acc[t][u & 3], __fadd_rn(c.x, c.y));
                 }
             }
         }
