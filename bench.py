@@ -251,7 +251,7 @@ class MoeLayer(Workload):
         self.bytes_per_step = (self.touched * per_expert + 4 * c.n_tokens * c.hidden * 2 +
                                4 * P * c.inter * 2 + 8 * P)
         self.units_per_step = c.n_tokens
-        self.launches_per_step = 4   # plan, gate/up, down, combine
+        self.launches_per_step = 6   # plan, x split, gate/up, act split, down, combine
         self.dominant = "k_moe_tc<2> (gate/up) + k_moe_tc<1> (down)"
 
     def step(self):

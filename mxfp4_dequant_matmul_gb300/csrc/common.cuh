@@ -181,6 +181,13 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
     return p;
 }
 
+// L2 policy for data that many CTAs read again: evict last.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // mma.sync m16n8k16, f16 inputs, FP32 accumulator d += A B.  Lane (g = lane / 4,
 // t = lane % 4) holds A rows g (a0, a2) and g + 8 (a1, a3) at K 2t, 2t + 1 (a0,
 // a1) and 2t + 8, 2t + 9 (a2, a3), B column g at K 2t, 2t + 1 (b0) and 2t + 8,

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -121,16 +122,22 @@ cudaError_t moe_plan_errors(const void* ws, int* n_invalid, cudaStream_t s);
 cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold,
                            int32_t* pairs_host, int cap, cudaStream_t s);
 
-// Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu;
+// Tensor-core expert passes (moe_tc.cu) over the plan arrays of moe.cu.  Each
+// first splits its vectors (x by token for gate/up, act by pair for down) into
+// the B-fragment blocks the pass copies per segment, in `frag`
+// (moe_frag_bytes(n_vectors, cols) bytes, 16-byte aligned), then runs the pass.
+// The gate/up pass calls `before` (the routing plan's launch) first.
 // cudaErrorNotSupported, with nothing launched, for shapes they cannot take.
+size_t moe_frag_bytes(int n_vec, int cols);
 cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
-                                  int hidden, int top_k, const float* x, int32_t* hdr,
-                                  const int32_t* offsets, const int32_t* touched,
+                                  int hidden, int top_k, const float* x, int n_tokens,
+                                  uint8_t* frag, const std::function<cudaError_t()>& before,
+                                  int32_t* hdr, const int32_t* offsets, const int32_t* touched,
                                   const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s);
 cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
-                               const float* act, int32_t* hdr, const int32_t* offsets,
-                               const int32_t* touched, const int32_t* pair_of, float* o_pairs,
-                               cudaStream_t s);
+                               const float* act, int n_pairs, uint8_t* frag, int32_t* hdr,
+                               const int32_t* offsets, const int32_t* touched,
+                               const int32_t* pair_of, float* o_pairs, cudaStream_t s);
 
 // Device fault words (set when a bounded wait gives up); read and optionally clear.
 cudaError_t read_fault_matvec(int* value, bool reset);

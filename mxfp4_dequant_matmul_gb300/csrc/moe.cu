@@ -28,14 +28,18 @@
 namespace mxk {
 namespace {
 
-// Workspace layout (all offsets 16-byte aligned; o_pairs 256-byte aligned).
+// Workspace layout (all offsets 16-byte aligned; o_pairs and the fragment
+// blocks 256-byte aligned).
 struct WsLayout {
-    size_t hdr, offsets, touched, pair_of, pair_slot, cold, o_pairs, total;
+    size_t hdr, offsets, touched, pair_of, pair_slot, cold, o_pairs, frag_x, frag_a, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-WsLayout ws_layout(int n_slots, int n_pairs, int hidden) {
+// (hdr, offsets, touched, pair_of, pair_slot and cold depend on n_slots and
+// the pair count only)
+WsLayout ws_layout(int n_slots, int n_tokens, int top_k, int hidden, int inter) {
+    const int n_pairs = n_tokens * top_k;
     WsLayout l;
     // int32[8]: invalid pairs, touched experts, cold pairs, -, the tensor-core
     // passes' segment claim counter and finished-CTA counter, -, -
@@ -46,7 +50,10 @@ WsLayout ws_layout(int n_slots, int n_pairs, int hidden) {
     l.pair_slot = align_up(l.pair_of + 4 * static_cast<size_t>(n_pairs), 16);   // int32[pairs]
     l.cold = align_up(l.pair_slot + 4 * static_cast<size_t>(n_pairs), 16);      // int32[pairs]
     l.o_pairs = align_up(l.cold + 4 * static_cast<size_t>(n_pairs), 256);
-    l.total = l.o_pairs + 4 * static_cast<size_t>(n_pairs) * hidden;
+    // the tensor-core passes' B-fragment blocks: of each token's x, of each pair's act
+    l.frag_x = align_up(l.o_pairs + 4 * static_cast<size_t>(n_pairs) * hidden, 256);
+    l.frag_a = align_up(l.frag_x + moe_frag_bytes(n_tokens, hidden), 256);
+    l.total = l.frag_a + moe_frag_bytes(n_pairs, inter);
     return l;
 }
 
@@ -58,17 +65,21 @@ struct Plan {
     int32_t* pair_slot;   // the pair's bank slot; -1 invalid, -2 cold
     int32_t* cold;        // cold pairs, increasing
     float* o_pairs;
+    uint8_t* frag_x;
+    uint8_t* frag_a;
 };
 
-Plan plan_view(void* ws, int n_slots, int n_pairs, int hidden) {
-    const WsLayout l = ws_layout(n_slots, n_pairs, hidden);
+Plan plan_view(void* ws, int n_slots, int n_tokens, int top_k, int hidden, int inter) {
+    const WsLayout l = ws_layout(n_slots, n_tokens, top_k, hidden, inter);
     char* b = static_cast<char*>(ws);
     return Plan{reinterpret_cast<int32_t*>(b + l.hdr), reinterpret_cast<int32_t*>(b + l.offsets),
                 reinterpret_cast<int32_t*>(b + l.touched),
                 reinterpret_cast<int32_t*>(b + l.pair_of),
                 reinterpret_cast<int32_t*>(b + l.pair_slot),
                 reinterpret_cast<int32_t*>(b + l.cold),
-                reinterpret_cast<float*>(b + l.o_pairs)};
+                reinterpret_cast<float*>(b + l.o_pairs),
+                reinterpret_cast<uint8_t*>(b + l.frag_x),
+                reinterpret_cast<uint8_t*>(b + l.frag_a)};
 }
 
 constexpr int32_t kSlotInvalid = -1, kSlotCold = -2;
@@ -427,8 +438,7 @@ cudaError_t launch_pass(const Bank& bank0, const Bank& bank1, int n_experts, int
 }  // namespace
 
 size_t moe_workspace_bytes(int n_slots, int n_tokens, int top_k, int hidden, int inter) {
-    (void)inter;
-    return ws_layout(n_slots, n_tokens * top_k, hidden).total;
+    return ws_layout(n_slots, n_tokens, top_k, hidden, inter).total;
 }
 
 cudaError_t launch_moe_gate_up(const Bank& gate, const Bank& up, int n_slots, int hidden,
@@ -436,20 +446,24 @@ cudaError_t launch_moe_gate_up(const Bank& gate, const Bank& up, int n_slots, in
                                const int32_t* ids, const int32_t* slot_of, int n_ids,
                                MoeAct epi, float* act, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
-    const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
-    if (n_slots <= kPlanSmemExperts)
-        k_moe_plan_s<<<1, 1024,
-                       4 * (static_cast<size_t>(n_slots) +
-                            static_cast<size_t>(n_pairs <= kPlanSmemPairs ? n_pairs : 0)),
-                       s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
-    else
-        k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = launch_moe_tc_gate_up(gate, up, n_slots, inter, hidden, top_k, x, plan.hdr, plan.offsets,
-                              plan.touched, plan.pair_of, epi, act, s);
+    const Plan plan = plan_view(ws, n_slots, n_tokens, top_k, hidden, inter);
+    const std::function<cudaError_t()> launch_plan = [&]() -> cudaError_t {
+        if (n_slots <= kPlanSmemExperts)
+            k_moe_plan_s<<<1, 1024,
+                           4 * (static_cast<size_t>(n_slots) +
+                                static_cast<size_t>(n_pairs <= kPlanSmemPairs ? n_pairs : 0)),
+                           s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
+        else
+            k_moe_plan<<<1, 1024, 0, s>>>(ids, n_pairs, n_slots, slot_of, n_ids, plan);
+        return cudaGetLastError();
+    };
+    cudaError_t e = launch_moe_tc_gate_up(gate, up, n_slots, inter, hidden, top_k, x, n_tokens,
+                                          plan.frag_x, launch_plan, plan.hdr, plan.offsets,
+                                          plan.touched, plan.pair_of, epi, act, s);
     if (e != cudaErrorNotSupported) return e;
-    (void)cudaGetLastError();
+    (void)cudaGetLastError();   // nothing launched: the plan and the FP32 pass
+    e = launch_plan();
+    if (e != cudaSuccess) return e;
     return launch_pass<Pass::kGateUp>(gate, up, n_slots, inter, hidden, top_k, x, plan, epi, act,
                                       s);
 }
@@ -458,9 +472,10 @@ cudaError_t launch_moe_down(const Bank& down, int n_slots, int hidden, int inter
                             const float* act, int n_tokens, int top_k, const float* route_w,
                             int bf16, float* y, void* ws, cudaStream_t s) {
     const int n_pairs = n_tokens * top_k;
-    const Plan plan = plan_view(ws, n_slots, n_pairs, hidden);
-    cudaError_t e = launch_moe_tc_down(down, n_slots, hidden, inter, act, plan.hdr, plan.offsets,
-                                       plan.touched, plan.pair_of, plan.o_pairs, s);
+    const Plan plan = plan_view(ws, n_slots, n_tokens, top_k, hidden, inter);
+    cudaError_t e = launch_moe_tc_down(down, n_slots, hidden, inter, act, n_pairs, plan.frag_a,
+                                       plan.hdr, plan.offsets, plan.touched, plan.pair_of,
+                                       plan.o_pairs, s);
     if (e == cudaErrorNotSupported) {
         (void)cudaGetLastError();
         e = launch_pass<Pass::kDown>(down, down, n_slots, hidden, inter, top_k, act, plan,
@@ -487,7 +502,7 @@ cudaError_t launch_moe_down(const Bank& down, int n_slots, int hidden, int inter
 
 cudaError_t moe_cold_pairs(const void* ws, int n_slots, int n_pairs, int* n_cold,
                            int32_t* pairs_host, int cap, cudaStream_t s) {
-    const WsLayout l = ws_layout(n_slots, n_pairs, 32);
+    const WsLayout l = ws_layout(n_slots, n_pairs, 1, 32, 32);
     const char* b = static_cast<const char*>(ws);
     int32_t n = 0;
     cudaError_t e = cudaMemcpyAsync(&n, b + l.hdr + 8, sizeof(n), cudaMemcpyDeviceToHost, s);

@@ -19,8 +19,10 @@
 // Work: a segment is (touched expert, up to four of its pairs, 128 rows of its
 // gate and up matrices or 256 rows of its down matrix); persistent CTAs claim
 // the segments of all touched experts in order from a counter in the
-// workspace, two ahead of use.  For each segment a CTA copies the rows' scale
-// bytes with one bulk copy per matrix, builds the pairs' B fragments, and its 16 warps stream
+// workspace, two ahead of use.  The vectors' B fragments are made once per
+// pass by k_moe_split (a block per vector in the workspace); for each segment a
+// CTA copies the rows' scale bytes with one bulk copy per matrix and its pairs'
+// fragment blocks with one bulk copy per pair, and its 16 warps stream
 // (matrix, 32-row unit, chunk range) units of 32 rows x 8 groups through
 // per-warp rings of TMA tile loads (a 3-D tensor map over the bank: bytes,
 // rows, experts).  Partial sums are added in chunk order; the gate/up pass
@@ -28,6 +30,7 @@
 // o[pair][row].  Every order depends on the shapes and the routing only (not
 // on which CTA takes a segment).
 #include <cstdint>
+#include <functional>
 #include <mutex>
 #include <type_traits>
 
@@ -55,6 +58,13 @@ constexpr int kGMaxE = 128;                 // groups per row (B fragments in sh
 constexpr int kMaxExpertsE = 1024;
 constexpr uint32_t kSmemMaxE = 227 * 1024;
 constexpr uint32_t kWaitE = 1u << 22;
+constexpr int kSplitThreads = 256;
+
+// Bytes of one vector's fragment block: 16 header bytes (its power of two p as
+// an int32, then zeros) and 128 bytes per group.
+__host__ __device__ constexpr uint32_t frag_block(int gpr) {
+    return 16u + static_cast<uint32_t>(gpr) * 128u;
+}
 
 __device__ int g_fault_moetc;   // set when a bounded wait gives up
 
@@ -69,6 +79,77 @@ __device__ __forceinline__ uint32_t pack_f16x2_e(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// The B fragments of vectors of `cols` floats (a token's x for the gate/up
+// pass, a pair's act row for the down pass), made once per pass instead of once
+// per segment that reads them.  Vector v becomes the block of frag_block(gpr)
+// bytes at frag + v * frag_block(gpr):
+//   bytes 0-15            p (int32), then zeros: the power of two that puts the
+//                         vector's largest finite |x| in [2^14, 2^15) (p = 14 -
+//                         floor(log2 m) from m's exponent field; a subnormal m
+//                         takes the cap, 126, which keeps 2^-p normal; 0 for a
+//                         vector of zeros)
+//   16 + 128 j + 16 w     f16 hi of x * 2^p for elements 32 j + 8 w .. + 7 of
+//                         group j, two to a 32-bit word
+//   16 + 128 j + 64 + 16 w  f16 lo = f16(x * 2^p - hi) of the same elements
+// so that lanes 8 q .. 8 q + 7 of a warp, reading 16 bytes each at 16 + 128 j +
+// 16 (lane % 8) of pair q's block, hold B columns 2 q (hi) and 2 q + 1 (lo) of
+// mma.sync m16n8k16 for group j.  A block of threads per vector (grid-stride).
+// wait_first: the vectors come from the previous kernel (wait for it before
+// reading); else they are inputs already complete and the wait comes last, so
+// that the pass launched after this kernel also sees the previous kernel done.
+__global__ void __launch_bounds__(kSplitThreads) k_moe_split(const float* __restrict__ vec,
+                                                             int n_vec, int cols,
+                                                             uint8_t* __restrict__ frag,
+                                                             int wait_first) {
+    __shared__ unsigned s_max;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gpr = cols / kGroup, n_items = gpr * 4;
+    const size_t vb = frag_block(gpr);
+    const int lane = threadIdx.x & 31;
+    for (int v = blockIdx.x; v < n_vec; v += gridDim.x) {
+        if (threadIdx.x == 0) s_max = 0u;
+        __syncthreads();
+        const float4* src = reinterpret_cast<const float4*>(vec + static_cast<size_t>(v) * cols);
+        float mx = 0.0f;
+        for (int i = threadIdx.x; i < n_items; i += kSplitThreads) {
+            const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float m = fabsf(f[k]);
+                mx = fmaxf(mx, m <= 3.402823466e38f ? m : 0.0f);   // NaN and inf do not count
+            }
+        }
+        const unsigned mb_w = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+        if (lane == 0 && mb_w != 0u) atomicMax(&s_max, mb_w);
+        __syncthreads();
+        const unsigned mb = s_max;
+        const int e = static_cast<int>(mb >> 23);
+        const int p = mb != 0u ? (e == 0 ? 126 : min(141 - e, 126)) : 0;
+        const float pm = exp2i_e(p);
+        uint8_t* blk = frag + static_cast<size_t>(v) * vb;
+        if (threadIdx.x == 0) *reinterpret_cast<int4*>(blk) = make_int4(p, 0, 0, 0);
+        for (int i = threadIdx.x; i < n_items; i += kSplitThreads) {
+            const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float f0 = __fmul_rn(f[2 * k], pm), f1 = __fmul_rn(f[2 * k + 1], pm);
+                hi[k] = pack_f16x2_e(f0, f1);
+                const float2 h = f16x2_to_f32x2(hi[k]);
+                lo[k] = pack_f16x2_e(__fsub_rn(f0, h.x), __fsub_rn(f1, h.y));
+            }
+            uint4* d = reinterpret_cast<uint4*>(blk + 16 + 128 * (i >> 2) + 16 * (i & 3));
+            d[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            d[4] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        __syncthreads();   // s_max is reset for the next vector
+    }
+    if (!wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Plan arrays written by the routing plan kernel (moe.cu).
@@ -88,18 +169,18 @@ struct ELayout {
 };
 __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     ELayout l;
-    l.xf = 0;                                                          // [gpr][32] uint4
-    l.sc = l.xf + static_cast<uint32_t>(gpr) * 512;                    // [2][NM][sc_bytes]
+    l.xf = 0;                                                          // [4][frag_block(gpr)]
+    l.sc = l.xf + kTokSeg * frag_block(gpr);                           // [2][NM][sc_bytes]
     l.sc_bytes = (static_cast<uint32_t>(ru_seg(NM) * kRowsUE) * gpr + 32u + 15u) & ~15u;
     const uint32_t part_bytes = kWarpsE * kRowsUE * kTokSeg * 4;      // [warps][32][4] f32
     const uint32_t buf = NM * l.sc_bytes > part_bytes ? NM * l.sc_bytes : part_bytes;
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;   // tmax[2][4], pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][8]
+    l.misc = l.lut + 1024;   // -, pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][8]
     l.segst = l.misc + 192;                                           // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
-    l.ring = (l.bars + (kWarpsE * kStagesE + 2) * 8 + 1023u) & ~1023u;
+    l.ring = (l.bars + (kWarpsE * kStagesE + 3) * 8 + 1023u) & ~1023u;
     l.total = l.ring + kWarpsE * kStagesE * kStageE + 1024;           // + alignment slack
     return l;
 }
@@ -116,18 +197,17 @@ template <int NM>
 __global__ void __launch_bounds__(kThreadsE, 1)
     k_moe_tc(const __grid_constant__ BankMaps tm0, const __grid_constant__ BankMaps tm1,
              const Bank bank0, const Bank bank1, int rows, int cols, int top_k, int n_experts,
-             const float* __restrict__ vec, PlanRef plan, MoeAct epi, float* __restrict__ out) {
+             const uint8_t* __restrict__ frag, PlanRef plan, MoeAct epi, float* __restrict__ out) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int gpr = cols / kGroup;
     const ELayout L = e_layout(NM, gpr, n_experts);
-    uint4* xf = reinterpret_cast<uint4*>(smem + L.xf);
+    const uint32_t vb = frag_block(gpr);   // one pair's fragment block in xf
     float* lut = reinterpret_cast<float*>(smem + L.lut);
     // per segment, double-buffered (buffer = the CTA's segment count mod 2, so
-    // that the next segment's are set while this one runs): the pairs' largest
-    // |x|, the pair ids and the flag of an odd scale byte
-    unsigned* tmax = reinterpret_cast<unsigned*>(smem + L.misc);        // [2][4]
+    // that the next segment's are set while this one runs): the pair ids and
+    // the flag of an odd scale byte
     int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [2][4]
     int* lead = reinterpret_cast<int*>(smem + L.misc + 64);             // [2 buffers][2 matrices]
     const uint32_t zero16 = smem_u32(smem + L.misc + 80);               // 16 zero bytes
@@ -135,7 +215,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     int* segmeta = reinterpret_cast<int*>(smem + L.misc + 112);   // [2][u, e, b0, n_e, s, -, -, -]
     int* segst = reinterpret_cast<int*>(smem + L.segst);
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
-    uint64_t* ring_bars = sbar + 2;
+    uint64_t* xbar = sbar + 2;                                          // the fragment blocks
+    uint64_t* ring_bars = sbar + 3;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -155,6 +236,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     if (tid == 0) {
         mbar_init(&sbar[0], 1);
         mbar_init(&sbar[1], 1);
+        mbar_init(xbar, 1);
         for (int i = 0; i < kWarpsE * kStagesE; ++i) mbar_init(&ring_bars[i], 1);
         fence_mbar_init();
         // segments are claimed in order from a counter of the workspace (zeroed by
@@ -233,7 +315,6 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     // wait on nothing (claim; touched index and id; first pair and count)
     int la_s = n_seg, la_u = segmeta[8 + 4] < n_seg ? segmeta[8] : 0, la_e = 0, la_b0 = 0,
         la_b1 = 0;
-    bool la_off = false;   // first pair and count requested
     uint64_t* bars = ring_bars + warp * kStagesE;
     uint8_t* ring = smem + L.ring + static_cast<size_t>(warp) * kStagesE * kStageE;
 
@@ -305,23 +386,71 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             bulk_g2s(smem + L.sc + (bi * NM + mm) * L.sc_bytes, a0[mm], sz[mm], &sbar[bi], policy);
     };
 
+    // the fragment blocks of segment q's pairs (ids pr) into xf (thread 0): one
+    // bulk copy per pair, kept in L2 (every segment of the pair's expert reads them)
+    const uint64_t keep = l2_evict_last();
+    auto issue_frags = [&](const Seg& q, const int* pr) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(q.npair) * vb);
+        for (int k = 0; k < q.npair; ++k) {
+            const size_t v = NM == 2 ? static_cast<size_t>(pr[k] / top_k) : static_cast<size_t>(pr[k]);
+            bulk_g2s(smem + L.xf + k * vb, frag + v * vb, vb, xbar, keep);
+        }
+    };
+    // every thread: wait for segment q's scale rows in buffer b and flag an odd
+    // byte.  "Plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits
+    // k << 23 and the rows' sums may stay in the 2^p domain (|sum| below 128*32 *
+    // 6 * 2^(200-127) * 2^15): any other byte of the segment sends it through the
+    // table and 2^-p per group.  False if the wait gave up.
+    auto check_scales = [&](const Seg& q, int b, uint32_t parity) {
+        if (!mbar_wait(&sbar[b], parity, kWaitE)) return false;
+        bool odd = false;
+        for (int mm = 0; mm < NM; ++mm) {
+            const uint8_t* sbuf = smem + L.sc + (b * NM + mm) * L.sc_bytes;
+            const int lo = lead[b * 2 + mm], hi = lo + q.nrow * gpr;
+            for (int c = tid; 16 * c < hi; c += kThreadsE) {
+                const int b0 = 16 * c;
+                if (b0 + 16 <= lo) continue;
+                if (b0 >= lo && b0 + 16 <= hi) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(sbuf + b0);
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        odd |= (__vcmpeq4(wv[k], 0u) | __vcmpgtu4(wv[k], 200u * 0x01010101u)) != 0u;
+                } else {
+                    for (int bb = max(b0, lo); bb < min(b0 + 16, hi); ++bb)
+                        odd |= sbuf[bb] == 0 || sbuf[bb] > 200;
+                }
+            }
+        }
+        if (odd) atomicOr(&seg_odd[b], 1);
+        return true;
+    };
+
     int kglob = 0;      // this warp's units consumed so far (ring phase)
     int issued = 0;     // this warp's units issued so far (lane 0): never more than kglob + stages
-    int nseg_cta = 0;   // segments this CTA has taken so far (scale buffer and phase)
+    int nseg_cta = 0;   // segments this CTA has taken so far (buffers and phases)
     bool failed = false;
     int s_cur = segmeta[4];
     Seg cur = seg_of(s_cur, 0);
     int sc_pend = -1;   // (thread 0) buffer of a scale copy not yet seen complete
     uint32_t sc_pend_par = 0;
+    bool x_pend = false;   // (thread 0) a fragment copy not yet seen complete
+    uint32_t x_pend_par = 0;
     if (tid == 0 && s_cur < n_seg) {
         issue_scales(cur, 0);
         sc_pend = 0;
+        int pr[kTokSeg];
+        for (int k = 0; k < cur.npair; ++k) pr[k] = plan.pair_of[cur.beg + k];
+        issue_frags(cur, pr);
+        x_pend = true;
     }
-    if (tid < kTokSeg) {   // the first segment's pairs and maxima (its first barrier below)
-        tmax[tid] = 0u;
-        spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
+    if (tid < kTokSeg) spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
+    if (tid == 0) {
+        seg_odd[0] = 0;
+        seg_odd[1] = 0;
     }
-    if (tid == 0) seg_odd[0] = 0;
+    __syncthreads();
 
     for (int s = s_cur; s < n_seg; ++nseg_cta) {
         const int bi = nseg_cta & 1;
@@ -338,121 +467,38 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         };
         const int stream_end = kglob + cur.n_units + nxt.n_units;
 
-        // --- prologue: the pairs' vectors -> B fragments
-        __syncthreads();   // the last segment is done with the fragments and the pairs
+        // --- prologue (the last segment's epilogue is done: barrier at its end)
         const int* sp = spair + bi * kTokSeg;
-        unsigned* tm = tmax + bi * kTokSeg;
-        if (tid < kTokSeg) {   // the next segment's (the last one is done with them)
-            tmax[(bi ^ 1) * kTokSeg + tid] = 0u;
-            spair[(bi ^ 1) * kTokSeg + tid] = tid < nxt.npair ? plan.pair_of[nxt.beg + tid] : 0;
-        }
+        // the next segment's pair ids: requested now, stored before this one's
+        // units end (spair[bi ^ 1] may still be read by the last epilogue's stores)
+        const int nxt_pair = tid < kTokSeg && tid < nxt.npair ? plan.pair_of[nxt.beg + tid] : 0;
+        int la_step = 0;   // (thread 0) 1: touched index and id looked up, 2: first pair and count
         if (tid == 0) {
-            seg_odd[bi ^ 1] = 0;
+            seg_odd[bi ^ 1] = 0;   // read by the last segment before its end
             la_s = atomicAdd(plan.hdr + 4, 1);
-            la_off = false;
         }
         // column sets of this segment: NP >= its pairs
         const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
-        constexpr int kXU = (kTokSeg * kGMaxE * 4 + kThreadsE - 1) / kThreadsE;
-        const int n_items = kTokSeg * gpr * 4;
-        float xv[kXU][8];
-#pragma unroll
-        for (int uu = 0; uu < kXU; ++uu) {
-            const int i = tid + uu * kThreadsE;
-            const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
-            if (i < n_items && tok < cur.npair) {
-                const int pr = sp[tok];
-                const size_t vrow = NM == 2 ? static_cast<size_t>(pr / top_k) : static_cast<size_t>(pr);
-                const float4* src = reinterpret_cast<const float4*>(vec + vrow * cols + 8 * rem);
-                const float4 a = __ldg(src), bb = __ldg(src + 1);
-                xv[uu][0] = a.x; xv[uu][1] = a.y; xv[uu][2] = a.z; xv[uu][3] = a.w;
-                xv[uu][4] = bb.x; xv[uu][5] = bb.y; xv[uu][6] = bb.z; xv[uu][7] = bb.w;
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) xv[uu][k] = 0.0f;
-            }
-        }
         // weights: fill the ring (some units may have been issued already)
         if (lane == 0) {
             fence_proxy_async_smem();
             while (issued < kglob + kStagesE && issued < stream_end) issue_next();
         }
-#pragma unroll
-        for (int uu = 0; uu < kXU; ++uu) {
-            const int i = tid + uu * kThreadsE;
-            const int tok = min(i / (gpr * 4), kTokSeg - 1);
-            float mx = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float a = fabsf(xv[uu][k]);
-                mx = fmaxf(mx, a <= 3.402823466e38f ? a : 0.0f);   // NaN and inf do not count
-            }
-            const unsigned same = __match_any_sync(0xffffffffu, tok);
-            const unsigned mb = __reduce_max_sync(same, __float_as_uint(mx));
-            if (mb != 0u && lane == __ffs(same) - 1) atomicMax(&tm[tok], mb);
-        }
-        __syncthreads();
-        if (tid == 0 && la_s < n_seg) {
-            while (segst[la_u + 1] <= la_s) ++la_u;
-            la_e = __ldg(plan.touched + la_u);
-        }
-        // pair q's power of two p: its largest |x| into [2^14, 2^15) (p = 14 -
-        // floor(log2 m) from m's exponent field; a subnormal m takes the cap,
-        // 126, which keeps 2^-p normal; 0 for zeros)
-        auto p_of = [&](int q) {
-            const unsigned mb = tm[q];
-            const int e = static_cast<int>(mb >> 23);
-            return mb != 0u ? (e == 0 ? 126 : min(141 - e, 126)) : 0;
-        };
-#pragma unroll
-        for (int uu = 0; uu < kXU; ++uu) {
-            const int i = tid + uu * kThreadsE;
-            const int tok = i / (gpr * 4), rem = i - tok * gpr * 4;
-            if (i < n_items && tok < np) {
-                const int j = rem >> 2, tw = rem & 3;
-                const float pm = exp2i_e(p_of(tok));
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float f0 = __fmul_rn(xv[uu][2 * k], pm), f1 = __fmul_rn(xv[uu][2 * k + 1], pm);
-                    hi[k] = pack_f16x2_e(f0, f1);
-                    const float2 h = f16x2_to_f32x2(hi[k]);
-                    lo[k] = pack_f16x2_e(__fsub_rn(f0, h.x), __fsub_rn(f1, h.y));
-                }
-                xf[j * 8 * np + (2 * tok) * 4 + tw] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                xf[j * 8 * np + (2 * tok + 1) * 4 + tw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-        }
-        if (!mbar_wait(&sbar[bi], static_cast<uint32_t>(nseg_cta >> 1) & 1u, kWaitE)) {
+        // this segment's fragment blocks (copied at the end of the last one) and
+        // its scale rows
+        if (!mbar_wait(xbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE)) failed = true;
+        if (!failed && !check_scales(cur, bi, static_cast<uint32_t>(nseg_cta >> 1) & 1u))
             failed = true;
-        } else {
-            if (tid == 0) sc_pend = -1;
-            // "plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits
-            // k << 23 and the rows' sums may stay in the 2^p domain (|sum| below
-            // 128*32 * 6 * 2^(200-127) * 2^15): any other byte of the segment sends
-            // it through the table and 2^-p per group
-            bool odd = false;
-            for (int mm = 0; mm < NM; ++mm) {
-                const uint8_t* sbuf = smem + L.sc + (bi * NM + mm) * L.sc_bytes;
-                const int lo = lead[bi * 2 + mm], hi = lo + cur.nrow * gpr;
-                for (int c = tid; 16 * c < hi; c += kThreadsE) {
-                    const int b0 = 16 * c;
-                    if (b0 + 16 <= lo) continue;
-                    if (b0 >= lo && b0 + 16 <= hi) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(sbuf + b0);
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            odd |= (__vcmpeq4(wv[q], 0u) | __vcmpgtu4(wv[q], 200u * 0x01010101u)) != 0u;
-                    } else {
-                        for (int b = max(b0, lo); b < min(b0 + 16, hi); ++b)
-                            odd |= sbuf[b] == 0 || sbuf[b] > 200;
-                    }
-                }
-            }
-            if (odd) atomicOr(&seg_odd[bi], 1);
-        }
         failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
+        if (tid == 0 && !failed) {
+            sc_pend = -1;
+            x_pend = false;
+        }
+        // pair q's power of two (the head of its fragment block; 0 for column
+        // sets past the segment's pairs)
+        auto p_of = [&](int q) {
+            return q < cur.npair ? *reinterpret_cast<const int*>(smem + L.xf + q * vb) : 0;
+        };
         // the whole segment in the 2^p domain: no odd scale byte, every pair's p >= 0
         bool fast = seg_odd[bi] == 0;
 #pragma unroll
@@ -462,9 +508,13 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         float acc[4] = {0.f, 0.f, 0.f, 0.f};   // rows g, g+8, g+16, g+24, this lane's groups
         const int slot = t / np, tok = t % np;   // D columns 2t, 2t + 1: group slot, pair
         const float pinv = exp2i_e(-p_of(tok));
-        // B: lanes 8 np s .. 8 np s + 8 np - 1 hold the fragment of group slot s
+        // B: lanes 8 np s .. 8 np s + 8 np - 1 hold the fragment of group slot s,
+        // lanes 8 q .. 8 q + 7 of them pair q's (the last pair's for column sets
+        // past the segment's pairs, whose D columns are not used)
         const int b_slot = lane / (8 * np);
-        const uint32_t xf_lane = smem_u32(xf) + static_cast<uint32_t>(lane % (8 * np)) * 16;
+        const int b_pair = min((lane % (8 * np)) >> 3, cur.npair - 1);
+        const uint32_t xf_lane = smem_u32(smem + L.xf) + static_cast<uint32_t>(b_pair) * vb + 16u +
+                                 static_cast<uint32_t>(lane & 7) * 16u;
         const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
         // the groups of a unit, GP to an accumulator
         auto unit_groups = [&](auto gp_c, auto fast_c, uint32_t row_addr, int gc0, int ngc,
@@ -487,8 +537,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                             e2m1x8_to_f16x2x4(cwd[2], h2);
                             e2m1x8_to_f16x2x4(cwd[3], h3);
                             const uint4 bf = lds128(
-                                b_slot == sl ? xf_lane + static_cast<uint32_t>(gc0 + j) * (128 * np)
-                                             : zero16);
+                                b_slot == sl ? xf_lane + static_cast<uint32_t>(gc0 + j) * 128u : zero16);
                             if (sl == 0) {
                                 mma16816_z(d0, h0[0], h1[0], h0[1], h1[1], bf.x, bf.y);
                                 mma16816_z(d1, h2[0], h3[0], h2[1], h3[1], bf.x, bf.y);
@@ -565,10 +614,16 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 fence_proxy_async_smem();
                 issue_next();
             }
-            if (tid == 0 && !la_off && la_s < n_seg) {
-                la_b0 = __ldg(plan.offsets + la_e);
-                la_b1 = __ldg(plan.offsets + la_e + 1);
-                la_off = true;
+            // (thread 0) the segment after next, one dependent step per unit
+            if (tid == 0 && la_s < n_seg && la_step < 2) {
+                if (la_step == 0) {
+                    while (segst[la_u + 1] <= la_s) ++la_u;
+                    la_e = __ldg(plan.touched + la_u);
+                } else {
+                    la_b0 = __ldg(plan.offsets + la_e);
+                    la_b1 = __ldg(plan.offsets + la_e + 1);
+                }
+                ++la_step;
             }
         }
         if (failed) {
@@ -579,7 +634,11 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         kglob += cur.n_units;
         if (tid == 0) {   // the segment after next, for the next iteration
             if (la_s < n_seg) {
-                if (!la_off) {
+                if (la_step < 1) {
+                    while (segst[la_u + 1] <= la_s) ++la_u;
+                    la_e = __ldg(plan.touched + la_u);
+                }
+                if (la_step < 2) {
                     la_b0 = __ldg(plan.offsets + la_e);
                     la_b1 = __ldg(plan.offsets + la_e + 1);
                 }
@@ -590,12 +649,17 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             }
             segmeta[bi * 8 + 4] = la_s;
         }
-        failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales
-        // the next segment's scale rows go to the other buffer
+        if (tid < kTokSeg) spair[(bi ^ 1) * kTokSeg + tid] = nxt_pair;
+        failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales and xf
+        // the next segment's scale rows go to the other buffer, its pairs'
+        // fragment blocks to xf
         if (tid == 0 && !failed && s_nxt < n_seg) {
             issue_scales(nxt, bi ^ 1);
             sc_pend = bi ^ 1;
             sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
+            issue_frags(nxt, spair + (bi ^ 1) * kTokSeg);
+            x_pend = true;
+            x_pend_par = static_cast<uint32_t>(nseg_cta + 1) & 1u;
         }
         float* part = reinterpret_cast<float*>(smem + L.sc + bi * NM * L.sc_bytes);
         // pair n: the slots' sums in lanes (g, s np + n), added in slot order into lane (g, n)
@@ -650,6 +714,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             for (int kq = kglob; kq < issued; ++kq)
                 mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
         if (tid == 0 && sc_pend >= 0) mbar_wait(&sbar[sc_pend], sc_pend_par, kWaitE);
+        if (tid == 0 && x_pend) mbar_wait(xbar, x_pend_par, kWaitE);
     }
     if (failed && lane == 0) atomicOr(&g_fault_moetc, 1);
     // the last CTA to finish zeroes the claim counters for the next pass (every
@@ -707,9 +772,13 @@ int sm_count_e() {
     return n > 0 ? n : 1;
 }
 
+// Checks and tensor maps first (cudaErrorNotSupported with nothing launched),
+// then `before` (the routing plan of the gate/up pass), the vectors' split and
+// the pass, each launched dependent on the kernel before it.
 template <int NM>
-cudaError_t launch_e(const Bank& bank0, const Bank& bank1, int n_experts,
-                     int rows, int cols, int top_k, const float* vec, PlanRef plan, MoeAct epi,
+cudaError_t launch_e(const Bank& bank0, const Bank& bank1, int n_experts, int rows, int cols,
+                     int top_k, const float* vec, int n_vec, uint8_t* frag,
+                     const std::function<cudaError_t()>& before, PlanRef plan, MoeAct epi,
                      float* out, cudaStream_t s) {
     const int gpr = cols / kGroup;
     if (gpr > kGMaxE || n_experts > kMaxExpertsE) return cudaErrorNotSupported;
@@ -733,37 +802,60 @@ cudaError_t launch_e(const Bank& bank0, const Bank& bank1, int n_experts,
             if (!bank_map(&m1.m[i], bank1.seg[i], bank1.stride, bank1.seg_slots, rows, cols))
                 return cudaErrorNotSupported;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sm_count_e()));
-    cfg.blockDim = dim3(kThreadsE);
-    cfg.dynamicSmemBytes = l.total;
-    cfg.stream = s;
+    cudaError_t e = cudaSuccess;
+    if (before) {
+        e = before();
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const int sms = sm_count_e();
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(n_vec < 4 * sms ? n_vec : 4 * sms));
+        cfg.blockDim = dim3(kSplitThreads);
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // the gate/up pass's x is an input (complete before the plan started);
+        // the down pass's act comes from the previous kernel
+        e = cudaLaunchKernelEx(&cfg, k_moe_split, vec, n_vec, cols, frag, NM == 1 ? 1 : 0);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms));
+    cfg.blockDim = dim3(kThreadsE);
+    cfg.dynamicSmemBytes = l.total;
+    cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, bank0, bank1, rows, cols, top_k,
-                                             n_experts, vec, plan, epi, out);
+    e = cudaLaunchKernelEx(&cfg, kernel, m0, m1, bank0, bank1, rows, cols, top_k, n_experts,
+                           static_cast<const uint8_t*>(frag), plan, epi, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t moe_frag_bytes(int n_vec, int cols) {
+    return static_cast<size_t>(n_vec) * frag_block(cols / kGroup);
+}
+
 cudaError_t launch_moe_tc_gate_up(const Bank& gate, const Bank& up, int n_experts, int inter,
-                                  int hidden, int top_k, const float* x, int32_t* hdr,
-                                  const int32_t* offsets, const int32_t* touched,
+                                  int hidden, int top_k, const float* x, int n_tokens,
+                                  uint8_t* frag, const std::function<cudaError_t()>& before,
+                                  int32_t* hdr, const int32_t* offsets, const int32_t* touched,
                                   const int32_t* pair_of, MoeAct epi, float* act, cudaStream_t s) {
-    return launch_e<2>(gate, up, n_experts, inter, hidden, top_k, x,
+    return launch_e<2>(gate, up, n_experts, inter, hidden, top_k, x, n_tokens, frag, before,
                        PlanRef{hdr, offsets, touched, pair_of}, epi, act, s);
 }
 
 cudaError_t launch_moe_tc_down(const Bank& down, int n_experts, int hidden, int inter,
-                               const float* act, int32_t* hdr, const int32_t* offsets,
-                               const int32_t* touched, const int32_t* pair_of, float* o_pairs,
-                               cudaStream_t s) {
-    return launch_e<1>(down, down, n_experts, hidden, inter, 1, act,
+                               const float* act, int n_pairs, uint8_t* frag, int32_t* hdr,
+                               const int32_t* offsets, const int32_t* touched,
+                               const int32_t* pair_of, float* o_pairs, cudaStream_t s) {
+    return launch_e<1>(down, down, n_experts, hidden, inter, 1, act, n_pairs, frag, nullptr,
                        PlanRef{hdr, offsets, touched, pair_of}, MoeAct{nullptr, 0.0f, 0}, o_pairs,
                        s);
 }
