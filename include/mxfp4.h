@@ -188,7 +188,11 @@ int mxfp4_matmat_host(const void* w, int rows, int cols, const float* X_host, in
  * (the page's gg_sel / gd_wt in their [batch, slots] layout).
  * -------------------------------------------------------------------------- */
 
-/* Workspace bytes the two passes need (routing plan + per-pair down outputs). */
+/* Workspace bytes the two passes need: the routing plan, the per-pair down
+ * outputs, and the tensor-core passes' split copies of the vectors (each token's
+ * x and each pair's act row as f16 hi/lo fragments with one power of two per
+ * vector, made once per pass and read by every segment of the vector's expert).
+ * The same workspace serves one layer at a time (gate/up, then down). */
 size_t mxfp4_moe_workspace_bytes(int n_experts, int n_tokens, int top_k, int hidden,
                                  int inter);
 

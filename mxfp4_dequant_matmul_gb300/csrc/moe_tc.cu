@@ -95,50 +95,66 @@ __device__ __forceinline__ uint32_t pack_f16x2_e(float lo, float hi) {
 //   16 + 128 j + 64 + 16 w  f16 lo = f16(x * 2^p - hi) of the same elements
 // so that lanes 8 q .. 8 q + 7 of a warp, reading 16 bytes each at 16 + 128 j +
 // 16 (lane % 8) of pair q's block, hold B columns 2 q (hi) and 2 q + 1 (lo) of
-// mma.sync m16n8k16 for group j.  A block of threads per vector (grid-stride).
+// mma.sync m16n8k16 for group j.  A block of threads per vector (grid-stride),
+// each thread holding its (at most kSplitItems) 8-element pieces in registers.
 // wait_first: the vectors come from the previous kernel (wait for it before
 // reading); else they are inputs already complete and the wait comes last, so
 // that the pass launched after this kernel also sees the previous kernel done.
+constexpr int kSplitItems = (kGMaxE * 4 + kSplitThreads - 1) / kSplitThreads;
+
 __global__ void __launch_bounds__(kSplitThreads) k_moe_split(const float* __restrict__ vec,
                                                              int n_vec, int cols,
                                                              uint8_t* __restrict__ frag,
                                                              int wait_first) {
-    __shared__ unsigned s_max;
+    __shared__ unsigned s_max[3];   // by vector index mod 3: one barrier per vector
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int gpr = cols / kGroup, n_items = gpr * 4;
+    const int gpr = cols / kGroup, n_items = gpr * 4;   // gpr <= kGMaxE
     const size_t vb = frag_block(gpr);
     const int lane = threadIdx.x & 31;
-    for (int v = blockIdx.x; v < n_vec; v += gridDim.x) {
-        if (threadIdx.x == 0) s_max = 0u;
-        __syncthreads();
+    if (threadIdx.x == 0) s_max[0] = 0u;
+    __syncthreads();
+    for (int v = blockIdx.x, it = 0; v < n_vec; v += gridDim.x, ++it) {
+        unsigned* sm = &s_max[it % 3];
+        // the next vector's slot: last read before the previous vector's barrier,
+        // next written after this vector's
+        if (threadIdx.x == 0) s_max[(it + 1) % 3] = 0u;
         const float4* src = reinterpret_cast<const float4*>(vec + static_cast<size_t>(v) * cols);
+        float f[kSplitItems][8];
         float mx = 0.0f;
-        for (int i = threadIdx.x; i < n_items; i += kSplitThreads) {
-            const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
-            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int u = 0; u < kSplitItems; ++u) {
+            const int i = threadIdx.x + u * kSplitThreads;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (i < n_items) {
+                a = __ldg(src + 2 * i);
+                b = __ldg(src + 2 * i + 1);
+            }
+            f[u][0] = a.x; f[u][1] = a.y; f[u][2] = a.z; f[u][3] = a.w;
+            f[u][4] = b.x; f[u][5] = b.y; f[u][6] = b.z; f[u][7] = b.w;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float m = fabsf(f[k]);
+                const float m = fabsf(f[u][k]);
                 mx = fmaxf(mx, m <= 3.402823466e38f ? m : 0.0f);   // NaN and inf do not count
             }
         }
         const unsigned mb_w = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
-        if (lane == 0 && mb_w != 0u) atomicMax(&s_max, mb_w);
+        if (lane == 0 && mb_w != 0u) atomicMax(sm, mb_w);
         __syncthreads();
-        const unsigned mb = s_max;
+        const unsigned mb = *sm;
         const int e = static_cast<int>(mb >> 23);
         const int p = mb != 0u ? (e == 0 ? 126 : min(141 - e, 126)) : 0;
         const float pm = exp2i_e(p);
         uint8_t* blk = frag + static_cast<size_t>(v) * vb;
         if (threadIdx.x == 0) *reinterpret_cast<int4*>(blk) = make_int4(p, 0, 0, 0);
-        for (int i = threadIdx.x; i < n_items; i += kSplitThreads) {
-            const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
-            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int u = 0; u < kSplitItems; ++u) {
+            const int i = threadIdx.x + u * kSplitThreads;
+            if (i >= n_items) continue;
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float f0 = __fmul_rn(f[2 * k], pm), f1 = __fmul_rn(f[2 * k + 1], pm);
+                const float f0 = __fmul_rn(f[u][2 * k], pm), f1 = __fmul_rn(f[u][2 * k + 1], pm);
                 hi[k] = pack_f16x2_e(f0, f1);
                 const float2 h = f16x2_to_f32x2(hi[k]);
                 lo[k] = pack_f16x2_e(__fsub_rn(f0, h.x), __fsub_rn(f1, h.y));
@@ -147,7 +163,6 @@ __global__ void __launch_bounds__(kSplitThreads) k_moe_split(const float* __rest
             d[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             d[4] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        __syncthreads();   // s_max is reset for the next vector
     }
     if (!wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -324,6 +339,24 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         bool active;
     };
     // segment s from its expert's entry in meta slot `slot`
+    // this warp's share of a segment of n_ru row units: (active, row unit, first
+    // chunk, chunk count); the full segments' once, the last row block's when met
+    struct Share {
+        bool active;
+        int WK, my_ru, c_lo, n_units;
+    };
+    auto share_of = [&](int n_ru) {
+        Share h;
+        h.WK = min(n_c, kWarpsE / (NM * n_ru));
+        h.active = warp < NM * n_ru * h.WK;
+        const int qq = warp / NM;
+        h.my_ru = qq % n_ru;
+        const int kk = qq / n_ru;
+        h.c_lo = h.active ? kk * n_c / h.WK : 0;
+        h.n_units = h.active ? (kk + 1) * n_c / h.WK - h.c_lo : 0;
+        return h;
+    };
+    const Share full_share = share_of(ru_seg(NM));
     auto seg_of = [&](int s, int slot) {
         Seg q{};
         if (s >= n_seg) return q;   // none: no units
@@ -341,14 +374,13 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         q.row0 = b * kSegRows;
         q.nrow = min(kSegRows, rows - q.row0);
         q.n_ru = (q.nrow + kRowsUE - 1) / kRowsUE;
-        q.WK = min(n_c, kWarpsE / (NM * q.n_ru));
-        q.active = warp < NM * q.n_ru * q.WK;
         q.m = warp % NM;
-        const int qq = warp / NM;
-        q.my_ru = qq % q.n_ru;
-        const int kk = qq / q.n_ru;
-        q.c_lo = q.active ? kk * n_c / q.WK : 0;
-        q.n_units = q.active ? (kk + 1) * n_c / q.WK - q.c_lo : 0;
+        const Share h = q.n_ru == ru_seg(NM) ? full_share : share_of(q.n_ru);
+        q.WK = h.WK;
+        q.active = h.active;
+        q.my_ru = h.my_ru;
+        q.c_lo = h.c_lo;
+        q.n_units = h.n_units;
         return q;
     };
     // this warp's unit k of segment q into stage st (lane 0): expert slot q.e is
@@ -414,9 +446,15 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 if (b0 >= lo && b0 + 16 <= hi) {
                     const uint4 w = *reinterpret_cast<const uint4*>(sbuf + b0);
                     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                    // per byte b, in bit 7: b == 0 (the borrow of b - 1 with b's
+                    // own top bit clear) or b > 200 (top bit set and its low
+                    // seven bits + 55 reaching 128); no carry crosses a byte
+                    uint32_t flag = 0u;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        odd |= (__vcmpeq4(wv[k], 0u) | __vcmpgtu4(wv[k], 200u * 0x01010101u)) != 0u;
+                        flag |= ((wv[k] - 0x01010101u) & ~wv[k]) |
+                                (((wv[k] & 0x7F7F7F7Fu) + 0x37373737u) & wv[k]);
+                    odd |= (flag & 0x80808080u) != 0u;
                 } else {
                     for (int bb = max(b0, lo); bb < min(b0 + 16, hi); ++bb)
                         odd |= sbuf[bb] == 0 || sbuf[bb] > 200;
