@@ -104,9 +104,13 @@ int mxfp4_dequant(const void* w, int rows, int cols, float* out, cudaStream_t st
  * exact), the group sum is scaled by its E8M0 factor and 2^-p in FP32 and
  * added to one of the row's four FP32 sums (groups by index mod 4), which are
  * added in order at the end.  x: [cols] floats, y: [rows] floats.  Error
- * bound: |y - exact| <= 1e-5 * sum_c |W[r][c] x[c]| (a NaN scale makes the
- * row NaN).  Deterministic: the order of every sum depends on the shape
- * only.  (PEROP mxfp4_mv.) */
+ * bound: |y - exact| <= 1e-5 * sum_c |W[r][c] x[c]| + 2^-39 * max_c |x[c]| *
+ * sum_c |W[r][c]| (a NaN scale makes the row NaN).  The second term comes from
+ * the f16 subnormal spacing under hi and lo: elements below about 2^-38 of the
+ * largest |x| are lost, which matters only for an x spanning more than ~2^30
+ * whose large elements meet small weights (mxfp4_mm_fp32 has no such term).
+ * Deterministic: the order of every sum depends on the shape only.  (PEROP
+ * mxfp4_mv.) */
 int mxfp4_mv(const void* w, int rows, int cols, const float* x, float* y,
              cudaStream_t stream);
 
@@ -217,7 +221,9 @@ int mxfp4_moe_gate_up(const void* gate_bank, const void* up_bank, int n_experts,
  *   y[t*hidden + r] = sum_j route_w[t*top_k + j] * o_{t*top_k + j}[r]
  * summed over j in slot order (dsv4_global_down_mxfp4's generic f32 mode, which
  * fuses the combine; rlx-cpu grouped_moe_unpermute_out).  A pair with an
- * invalid id contributes nothing.  y: [n_tokens, hidden]. */
+ * invalid id contributes nothing.  y: [n_tokens, hidden].  Both passes' dot
+ * products carry mxfp4_mv's error bound, with x the token's x (gate/up) or the
+ * pair's act row (down). */
 int mxfp4_moe_down(const void* down_bank, int n_experts, int hidden, int inter,
                    const float* act, int n_tokens, int top_k, const int32_t* expert_ids,
                    const float* route_w, float* y, void* workspace, size_t ws_bytes,

@@ -192,7 +192,7 @@ __host__ __device__ inline ELayout e_layout(int NM, int gpr, int n_experts) {
     l.sc_bytes = buf / NM;   // (>= the scale rows; the buffer also holds the partial sums)
     l.sc_bytes = (l.sc_bytes + 15u) & ~15u;
     l.lut = l.sc + 2 * NM * l.sc_bytes;                                // [256] f32
-    l.misc = l.lut + 1024;   // -, pairs[2][4], lead[4], 16 zeros, odd flag[2], meta[2][8]
+    l.misc = l.lut + 1024;   // -, pairs[2][4], lead[4], 16 zeros, -, meta[2][8]
     l.segst = l.misc + 192;                                           // [touched + 1] int
     l.bars = (l.segst + 4u * (static_cast<uint32_t>(n_experts) + 1u) + 7u) & ~7u;
     l.ring = (l.bars + (kWarpsE * kStagesE + 3) * 8 + 1023u) & ~1023u;
@@ -221,12 +221,10 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     const uint32_t vb = frag_block(gpr);   // one pair's fragment block in xf
     float* lut = reinterpret_cast<float*>(smem + L.lut);
     // per segment, double-buffered (buffer = the CTA's segment count mod 2, so
-    // that the next segment's are set while this one runs): the pair ids and
-    // the flag of an odd scale byte
+    // that the next segment's are set while this one runs): the pair ids
     int* spair = reinterpret_cast<int*>(smem + L.misc + 32);            // [2][4]
     int* lead = reinterpret_cast<int*>(smem + L.misc + 64);             // [2 buffers][2 matrices]
     const uint32_t zero16 = smem_u32(smem + L.misc + 80);               // 16 zero bytes
-    int* seg_odd = reinterpret_cast<int*>(smem + L.misc + 96);          // [2]
     int* segmeta = reinterpret_cast<int*>(smem + L.misc + 112);   // [2][u, e, b0, n_e, s, -, -, -]
     int* segst = reinterpret_cast<int*>(smem + L.segst);
     uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + L.bars);       // [2 buffers]
@@ -429,42 +427,6 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             bulk_g2s(smem + L.xf + k * vb, frag + v * vb, vb, xbar, keep);
         }
     };
-    // every thread: wait for segment q's scale rows in buffer b and flag an odd
-    // byte.  "Plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits
-    // k << 23 and the rows' sums may stay in the 2^p domain (|sum| below 128*32 *
-    // 6 * 2^(200-127) * 2^15): any other byte of the segment sends it through the
-    // table and 2^-p per group.  False if the wait gave up.
-    auto check_scales = [&](const Seg& q, int b, uint32_t parity) {
-        if (!mbar_wait(&sbar[b], parity, kWaitE)) return false;
-        bool odd = false;
-        for (int mm = 0; mm < NM; ++mm) {
-            const uint8_t* sbuf = smem + L.sc + (b * NM + mm) * L.sc_bytes;
-            const int lo = lead[b * 2 + mm], hi = lo + q.nrow * gpr;
-            for (int c = tid; 16 * c < hi; c += kThreadsE) {
-                const int b0 = 16 * c;
-                if (b0 + 16 <= lo) continue;
-                if (b0 >= lo && b0 + 16 <= hi) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(sbuf + b0);
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-                    // per byte b, in bit 7: b == 0 (the borrow of b - 1 with b's
-                    // own top bit clear) or b > 200 (top bit set and its low
-                    // seven bits + 55 reaching 128); no carry crosses a byte
-                    uint32_t flag = 0u;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        flag |= ((wv[k] - 0x01010101u) & ~wv[k]) |
-                                (((wv[k] & 0x7F7F7F7Fu) + 0x37373737u) & wv[k]);
-                    odd |= (flag & 0x80808080u) != 0u;
-                } else {
-                    for (int bb = max(b0, lo); bb < min(b0 + 16, hi); ++bb)
-                        odd |= sbuf[bb] == 0 || sbuf[bb] > 200;
-                }
-            }
-        }
-        if (odd) atomicOr(&seg_odd[b], 1);
-        return true;
-    };
-
     int kglob = 0;      // this warp's units consumed so far (ring phase)
     int issued = 0;     // this warp's units issued so far (lane 0): never more than kglob + stages
     int nseg_cta = 0;   // segments this CTA has taken so far (buffers and phases)
@@ -484,10 +446,6 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         x_pend = true;
     }
     if (tid < kTokSeg) spair[tid] = tid < cur.npair ? plan.pair_of[cur.beg + tid] : 0;
-    if (tid == 0) {
-        seg_odd[0] = 0;
-        seg_odd[1] = 0;
-    }
     __syncthreads();
 
     for (int s = s_cur; s < n_seg; ++nseg_cta) {
@@ -505,16 +463,15 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         };
         const int stream_end = kglob + cur.n_units + nxt.n_units;
 
-        // --- prologue (the last segment's epilogue is done: barrier at its end)
+        // --- prologue, every warp for itself (no barrier: the last segment's
+        // epilogue reads only its partial sums and pair ids, which nothing
+        // before this segment's final barrier overwrites)
         const int* sp = spair + bi * kTokSeg;
-        // the next segment's pair ids: requested now, stored before this one's
-        // units end (spair[bi ^ 1] may still be read by the last epilogue's stores)
+        // the next segment's pair ids: requested now, stored after this one's
+        // units (spair[bi ^ 1] may still be read by the last epilogue's stores)
         const int nxt_pair = tid < kTokSeg && tid < nxt.npair ? plan.pair_of[nxt.beg + tid] : 0;
         int la_step = 0;   // (thread 0) 1: touched index and id looked up, 2: first pair and count
-        if (tid == 0) {
-            seg_odd[bi ^ 1] = 0;   // read by the last segment before its end
-            la_s = atomicAdd(plan.hdr + 4, 1);
-        }
+        if (tid == 0) la_s = atomicAdd(plan.hdr + 4, 1);
         // column sets of this segment: NP >= its pairs
         const int np = cur.npair <= 1 ? 1 : cur.npair <= 2 ? 2 : 4;
         // weights: fill the ring (some units may have been issued already)
@@ -523,22 +480,51 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             while (issued < kglob + kStagesE && issued < stream_end) issue_next();
         }
         // this segment's fragment blocks (copied at the end of the last one) and
-        // its scale rows
-        if (!mbar_wait(xbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE)) failed = true;
-        if (!failed && !check_scales(cur, bi, static_cast<uint32_t>(nseg_cta >> 1) & 1u))
-            failed = true;
-        failed = __syncthreads_or(failed) != 0;   // every thread takes the same way
+        // its scale rows (the lanes of a warp agree on the outcome)
+        const bool landed = mbar_wait(xbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE) &&
+                            mbar_wait(&sbar[bi], static_cast<uint32_t>(nseg_cta >> 1) & 1u, kWaitE);
+        failed = failed || !__all_sync(0xffffffffu, landed);
         if (tid == 0 && !failed) {
             sc_pend = -1;
             x_pend = false;
+        }
+        const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
+        // "Plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits k << 23
+        // and the rows' sums may stay in the 2^p domain (|sum| below 128*32 * 6 *
+        // 2^(200-127) * 2^15).  A warp with any other byte among its units' (lane
+        // l: row 32 ru + l of its matrix over its chunk range) takes the table and
+        // 2^-p per group.  Per byte b, in bit 7: b == 0 (the borrow of b - 1 with
+        // b's own top bit clear) or b > 200 (top bit set and its low seven bits +
+        // 55 reaching 128); no carry crosses a byte.
+        bool odd = false;
+        if (!failed && cur.active) {
+            const int r = cur.my_ru * kRowsUE + lane;
+            const int g0 = cur.c_lo * kChunkE;
+            const int ng = min(gpr, (cur.c_lo + cur.n_units) * kChunkE) - g0;
+            if (r < cur.nrow) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(scm + r * gpr + g0);
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
+                const uint32_t sh = 8u * static_cast<uint32_t>(a & 3u);
+                uint32_t flag = 0u, w0 = wp[0];
+                for (int o = 0; o < ng; o += 4) {
+                    const uint32_t w1 = wp[(o >> 2) + 1];
+                    uint32_t w = __funnelshift_r(w0, w1, sh);
+                    w0 = w1;
+                    const int left = ng - o;   // bytes of the row left; past them: 1s
+                    if (left < 4)
+                        w = (w & (0xFFFFFFFFu >> (8 * (4 - left)))) | (0x01010101u << (8 * left));
+                    flag |= ((w - 0x01010101u) & ~w) | (((w & 0x7F7F7F7Fu) + 0x37373737u) & w);
+                }
+                odd = (flag & 0x80808080u) != 0u;
+            }
         }
         // pair q's power of two (the head of its fragment block; 0 for column
         // sets past the segment's pairs)
         auto p_of = [&](int q) {
             return q < cur.npair ? *reinterpret_cast<const int*>(smem + L.xf + q * vb) : 0;
         };
-        // the whole segment in the 2^p domain: no odd scale byte, every pair's p >= 0
-        bool fast = seg_odd[bi] == 0;
+        // this warp's units in the 2^p domain: no odd scale byte, every pair's p >= 0
+        bool fast = !__any_sync(0xffffffffu, odd);
 #pragma unroll
         for (int q = 0; q < kTokSeg; ++q) fast = fast && p_of(q) >= 0;
 
@@ -553,7 +539,6 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         const int b_pair = min((lane % (8 * np)) >> 3, cur.npair - 1);
         const uint32_t xf_lane = smem_u32(smem + L.xf) + static_cast<uint32_t>(b_pair) * vb + 16u +
                                  static_cast<uint32_t>(lane & 7) * 16u;
-        const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
         // the groups of a unit, GP to an accumulator
         auto unit_groups = [&](auto gp_c, auto fast_c, uint32_t row_addr, int gc0, int ngc,
                                const uint32_t (&sb)[4][2]) {
@@ -611,7 +596,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         int k = 0;
         for (; k < cur.n_units && !failed; ++k) {
             const int kg = kglob + k, st = kg % kStagesE;
-            if (!mbar_wait(&bars[st], static_cast<uint32_t>(kg / kStagesE) & 1u, kWaitE)) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bars[st], static_cast<uint32_t>(kg / kStagesE) & 1u, kWaitE))) {
                 failed = true;
                 break;
             }
@@ -687,15 +673,19 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             }
             segmeta[bi * 8 + 4] = la_s;
         }
+        // every warp is done with the scales and xf and past the last epilogue
+        failed = __syncthreads_or(failed) != 0;
         if (tid < kTokSeg) spair[(bi ^ 1) * kTokSeg + tid] = nxt_pair;
-        failed = __syncthreads_or(failed) != 0;   // every warp is done with the scales and xf
+        int nxt_pr[kTokSeg];   // (warp 0) the next segment's pair ids
+#pragma unroll
+        for (int q = 0; q < kTokSeg; ++q) nxt_pr[q] = __shfl_sync(0xffffffffu, nxt_pair, q);
         // the next segment's scale rows go to the other buffer, its pairs'
         // fragment blocks to xf
         if (tid == 0 && !failed && s_nxt < n_seg) {
             issue_scales(nxt, bi ^ 1);
             sc_pend = bi ^ 1;
             sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
-            issue_frags(nxt, spair + (bi ^ 1) * kTokSeg);
+            issue_frags(nxt, nxt_pr);
             x_pend = true;
             x_pend_par = static_cast<uint32_t>(nseg_cta + 1) & 1u;
         }

@@ -202,3 +202,73 @@ def test_passes_repeated_on_one_workspace(mx):
                              cfg.hidden, cfg.inter, x, cfg.n_tokens, cfg.top_k, ids, wts)
     assert_within(outs[0].reshape(cfg.n_tokens, cfg.hidden), ref["out"],
                   ref["bound_l1"] + ref["bound_prop"], REL_FP32, "MoE layer")
+
+
+def plant_scale(bank, stride, rows, cols, e, r, g, byte):
+    """Set the E8M0 scale byte of (row r, group g) of expert e's matrix."""
+    bank[e * stride + rows * cols // 2 + r * (cols // 32) + g] = byte
+
+
+def test_layer_with_odd_scale_bytes_and_large_activations(mx):
+    # scale bytes outside 1..200 in a few rows (0: the subnormal scale 2^-127 in
+    # gate, up and down; 201 and 210: scales of 2^74 and 2^83 and 255: NaN, in
+    # down only, so that no act row spans more than the split's range) and a
+    # token whose largest |x| is over 2^15 (a negative power of two) send some
+    # warps' units, not whole segments, through the table path and 2^-p per
+    # group, next to warps of the same segment that stay in the 2^p domain.  NaN
+    # where the oracle has NaN.
+    E, hidden, inter, T, K = 12, 512, 640, 24, 4
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 29)
+    gate, up, down, x = gate.copy(), up.copy(), down.copy(), x.copy()
+    e0, e1 = int(ids[0, 0]), int(ids[1, 1])
+    plant_scale(gate, cfg.gu_stride, inter, hidden, e0, 5, 3, 0)
+    plant_scale(up, cfg.gu_stride, inter, hidden, e1, 100, 0, 0)
+    plant_scale(down, cfg.down_stride, hidden, inter, e0, 300, 7, 201)
+    plant_scale(down, cfg.down_stride, hidden, inter, e0, 301, 2, 210)
+    plant_scale(down, cfg.down_stride, hidden, inter, e1, 33, 12, 255)
+    plant_scale(down, cfg.down_stride, hidden, inter, e1, 400, 19, 0)
+    t_big = next(t for t in range(T) if e0 not in ids[t] and e1 not in ids[t])
+    x[t_big] *= np.float32(2.0 ** 14)
+    y, _ = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
+                             x, T, K, ids, wts)
+    assert np.isnan(ref["out"]).any() and (np.abs(ref["out"]) > 2.0 ** 60).any()
+    assert_within(y, ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32,
+                  "MoE layer with odd scale bytes")
+
+
+def test_down_stage_error_floor_of_a_wide_range_act(mx):
+    # The split of a vector into f16 hi and lo after scaling by 2^p (largest |x|
+    # into [2^14, 2^15)) represents each element to within 2^-22 of itself or an
+    # absolute 2^-25 * 2^-p (the f16 subnormal spacing), whichever is larger:
+    # elements below about 2^-38 of the largest are lost.  Rows whose weight is
+    # zero or small where the act row peaks can then be off by more than 1e-5 of
+    # their L1 sum, by at most 2^-39 * max|act| * sum_c |w[r][c]|.  An act row
+    # with one element of 2^60 among N(0, 1) elements checks that floor.
+    E, hidden, inter, T, K = 6, 256, 512, 10, 2
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 31)
+    P = T * K
+    act = synth.normal_f32(1031, P * inter).reshape(P, inter)
+    act[3, 17] = np.float32(2.0 ** 60)
+    act[8, 500] = np.float32(-(2.0 ** 50))
+    act_d, ws = run_gate_up(mx, cfg, gate, up, x, ids)
+    act_d.copy_(to_dev(act.reshape(-1)))
+    y = empty(T * hidden)
+    mx.mxfp4_moe_down(to_dev(down), E, hidden, inter, act_d, T, K, to_dev(ids), to_dev(wts),
+                      y, ws)
+    ref = oracle.moe_down(down, cfg.down_stride, E, hidden, inter, act.reshape(-1), T, K, ids,
+                          wts)
+    # sum_j |w_tj| * 2^-39 * max|act[pair]| * sum_c |down_e[r][c]|
+    floor = np.zeros((T, hidden))
+    for t in range(T):
+        for j in range(K):
+            e, p = int(ids[t, j]), t * K + j
+            w = oracle.dequant(down[e * cfg.down_stride:(e + 1) * cfg.down_stride], hidden, inter)
+            floor[t] += abs(float(wts[t, j])) * 2.0 ** -39 * np.abs(act[p]).max() * \
+                np.abs(w).sum(axis=1)
+    got = host(y).reshape(T, hidden)
+    err = np.abs(got.astype(np.float64) - ref["out"].reshape(T, hidden))
+    tol = REL_FP32 * ref["l1_out"].reshape(T, hidden) + floor
+    assert (err <= tol).all(), f"worst err/tol {np.max(err / tol):.3g}"
+    # the floor is what lets it pass: somewhere the plain 1e-5 * L1 is exceeded
+    assert (err > REL_FP32 * ref["l1_out"].reshape(T, hidden)).any()
