@@ -187,6 +187,26 @@ def test_mm_wide_dynamic_range_activations(mx, nb):
     assert_within(Y, ref, l1, REL_FP32, f"wide range nb={nb}")
 
 
+@pytest.mark.parametrize("nb", [1, 8])
+def test_mm_error_floor_of_an_outlier_activation(mx, nb):
+    # one element of 2^60 among N(0, 1) values: x * 2^p puts the N(0, 1) part
+    # below the f16 subnormal spacing, so rows whose weight is zero where x
+    # peaks lose it and exceed 1e-5 * L1; the stated bound adds 2^-39 * max|x|
+    # * sum_c |w[r][c]| and holds everywhere
+    rows, cols = 256, 512
+    w_h = synth.mxfp4_matrix(rows, cols, 90 + nb, 118, 130)
+    X = synth.normal_f32(91 + nb, nb * cols).reshape(nb, cols)
+    X[:, 17] = np.float32(2.0 ** 60)
+    Y = run_mm(mx, w_h, rows, cols, X, nb)
+    ref, l1 = oracle.matmat(w_h, rows, cols, X, nb)
+    ref, l1 = ref.reshape(nb, rows), l1.reshape(nb, rows)
+    wsum = np.abs(oracle.dequant(w_h, rows, cols)).sum(axis=1)
+    floor = 2.0 ** -39 * np.abs(X).max(axis=1, keepdims=True) * wsum[None, :]
+    err = np.abs(Y.astype(np.float64) - ref)
+    assert (err <= REL_FP32 * l1 + floor).all(), f"worst {np.max(err / (REL_FP32 * l1 + floor)):.3g}"
+    assert (err > REL_FP32 * l1).any()
+
+
 @pytest.mark.parametrize("nb", [1, 8, 11])
 def test_mm_wide_weight_scales(mx, nb):
     # scale bytes over 0..240 inside every row, rows whose largest-scale group
