@@ -329,7 +329,7 @@ int mxfp4_moe_cold_pairs(const void* workspace, size_t ws_bytes, int n_slots, in
  *     host threads) race on the array: serialise them.
  *   - Out-of-range expert ids are skipped as in mxfp4_moe_gate_up /
  *     mxfp4_moe_down; their count is not reported by this entry point. */
-#define MXFP4_MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MXFP4_MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int mxfp4_moe_layer_noalloc(const void* gate_bank, const void* up_bank, const void* down_bank,
                             int n_experts, int hidden, int inter, const float* x, int n_tokens,
                             int top_k, const int32_t* expert_ids, const float* route_w, float* y,

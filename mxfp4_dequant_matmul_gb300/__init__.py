@@ -221,7 +221,7 @@ def mxfp4_moe_plan_errors(workspace, ws_bytes=None, stream=None) -> int:
     return n.value
 
 
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def mxfp4_moe_layer_noalloc(gate_bank, up_bank, down_bank, n_experts, hidden, inter, x,

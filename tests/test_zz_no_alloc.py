@@ -24,6 +24,8 @@ pytestmark = pytest.mark.gpu
 
 SMALL = dict(E=4, hidden=256, inter=128, T=3, K=2)
 LARGE = dict(E=64, hidden=512, inter=384, T=32, K=4)
+# the bench's MoE layer: its plan, fragment blocks, per-pair outputs and act take 4.8 MB
+LAYER = dict(E=64, hidden=2880, inter=2880, T=32, K=4)
 
 
 def _case(seed, E, hidden, inter, T, K):
@@ -69,9 +71,16 @@ def test_noalloc_layer_matches_the_oracle_large_then_small():
     _call_and_check(mx, 33, SMALL, check_memory=True)
 
 
+def test_noalloc_layer_takes_the_bench_moe_shape():
+    mx = cuda()
+    assert (mx.mxfp4_moe_workspace_bytes(64, 32, 4, 2880, 2880) + 255) // 256 * 256 + \
+        32 * 4 * 2880 * 4 <= mx.NOALLOC_SCRATCH_BYTES
+    _call_and_check(mx, 3, LAYER, check_memory=True)
+
+
 def test_noalloc_layer_refuses_problems_larger_than_its_array():
     mx = cuda()
     A = 1 << 20   # never dereferenced: the size check comes first
-    # 64 tokens x top-4 x inter 8192 floats of act alone is 8 MiB > 4 MiB
-    status = mx.lib().mxfp4_moe_layer_noalloc(A, A, A, 8, 256, 8192, A, 64, 4, A, A, A, None)
+    # 64 tokens x top-4 x inter 32768 floats of act alone is 32 MiB > 16 MiB
+    status = mx.lib().mxfp4_moe_layer_noalloc(A, A, A, 8, 256, 32768, A, 64, 4, A, A, A, None)
     assert status == 4, mx.mxfp4_status_string(status)
