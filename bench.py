@@ -227,10 +227,10 @@ class SmallBatch(Workload):
 
 
 class MoeLayer(Workload):
-    def __init__(self, mx):
+    def __init__(self, mx, cfg=None):
         import torch
         import synth
-        c = synth.MOE
+        c = synth.MOE if cfg is None else cfg
         self.mx, self.c = mx, c
         self.name = c.name
         gate, up, down = c.banks()
@@ -342,6 +342,71 @@ class Dequant(Workload):
 
     def step(self):
         self.mx.mxfp4_dequant(self.w, self.c.rows, self.c.cols, self.out)
+
+
+class Q4kDequant(Workload):
+    """Standalone decode of the Q4_K decode-GEMV matrix to float (q4k_dequant)."""
+
+    def __init__(self, mx):
+        import torch
+        import synth
+        c = synth.Q4K_DECODE
+        self.mx, self.c = mx, c
+        self.name = "q4k_dequant 14336x4096"
+        self.w = _dev(c.weights())
+        self.out = torch.empty(c.rows * c.cols, dtype=torch.float32, device="cuda")
+        self.bytes_per_step = mx.q4k_nbytes(c.rows, c.cols) + 4 * c.rows * c.cols
+        self.dominant = "k_q4k_dequant"
+
+    def step(self):
+        self.mx.q4k_dequant(self.w, self.c.rows, self.c.cols, self.out)
+
+
+class SmallBatchFp32(SmallBatch):
+    """The small-batch workload through the FP32 CUDA-core path (mxfp4_mm_fp32)."""
+
+    def __init__(self, mx):
+        super().__init__(mx)
+        self.name = self.c.name + " through mxfp4_mm_fp32"
+        self.dominant = "k_matmat (mxfp4_mm_fp32)"
+
+    def step(self):
+        c = self.c
+        for w, Y in zip(self.ws, self.Ys):
+            self.mx.mxfp4_mm_fp32(w, c.rows, c.cols, self.X, c.nb, Y)
+
+
+class WideSmallBatch(Workload):
+    """mxfp4_mm with 8 tokens on rows of 36864 columns (1152 groups), past what a
+    cluster of the tensor-core pass stages per row: the fallback k_mma_small."""
+
+    def __init__(self, mx):
+        import torch
+        import synth
+        rows, cols, nb = 128, 36864, 8
+        self.mx, self.shape = mx, (rows, cols, nb)
+        self.name = f"mxfp4_mm {rows}x{cols} nb={nb} (rows of more than 1024 groups)"
+        self.w = _dev(synth.mxfp4_matrix(rows, cols, 61, 118, 130))
+        self.X = _dev(synth.normal_f32(62, nb * cols))
+        self.Y = torch.empty(nb * rows, dtype=torch.float32, device="cuda")
+        self.bytes_per_step = mx.mxfp4_nbytes(rows, cols) + 4 * nb * (cols + rows)
+        self.dominant = "k_mma_small"
+
+    def step(self):
+        rows, cols, nb = self.shape
+        self.mx.mxfp4_mm(self.w, rows, cols, self.X, nb, self.Y)
+
+
+class MoeLayerFp32(MoeLayer):
+    """A routed-expert layer with more experts than the tensor-core passes take
+    (1100 experts of 1024x1024, 32 tokens, top-4): the FP32 passes k_moe_pass."""
+
+    def __init__(self, mx):
+        import synth
+        super().__init__(mx, cfg=synth.MoeConfig("MoE 1100 experts 1024x1024 top-4, 32 tokens",
+                                                 1100, 1024, 1024, 32, 4, seed=7))
+        self.launches_per_step = 4   # plan, gate/up, down, combine
+        self.dominant = "k_moe_pass (gate/up and down)"
 
 
 class Tiny(DecodeGemv):
@@ -573,7 +638,8 @@ def run_profile(args):
     mx.mxfp4_set_launch_overlap(True)   # as in the timed bench
     cls = {"decode": DecodeGemv, "decode_fp32": DecodeGemvFp32, "mm8": SmallBatch,
            "moe": MoeLayer, "prefill": Prefill, "prefill_mm": PrefillMm,
-           "dequant": Dequant, "q4k": Q4kDecode}
+           "dequant": Dequant, "q4k": Q4kDecode, "q4k_dequant": Q4kDequant,
+           "mm8_fp32": SmallBatchFp32, "mm_wide": WideSmallBatch, "moe_fp32": MoeLayerFp32}
     w = cls[args.profile](mx)
     for _ in range(args.warmup):
         w.step()
@@ -598,7 +664,7 @@ def main():
                     help="extra seconds of the main step replayed while the clocks are sampled")
     ap.add_argument("--profile",
                     choices=["decode", "decode_fp32", "mm8", "moe", "prefill", "prefill_mm",
-                             "dequant", "q4k"],
+                             "dequant", "q4k", "q4k_dequant", "mm8_fp32", "mm_wide", "moe_fp32"],
                     help="run only this workload's warm-up and timed steps (eagerly, one "
                          "launch at a time, for a profiler) and print its time; no JSON line")
     args = ap.parse_args()
