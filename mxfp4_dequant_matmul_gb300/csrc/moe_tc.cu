@@ -25,10 +25,13 @@
 // fragment blocks with one bulk copy per pair, and its 16 warps stream
 // (matrix, 32-row unit, chunk range) units of 32 rows x 8 groups through
 // per-warp rings of TMA tile loads (a 3-D tensor map over the bank: bytes,
-// rows, experts).  Partial sums are added in chunk order; the gate/up pass
-// applies SiLU(g) * u and writes act[pair][row], the down pass writes
-// o[pair][row].  Every order depends on the shapes and the routing only (not
-// on which CTA takes a segment).
+// rows, experts).  A warp keeps its sums in the 2^p domain when its units'
+// scale bytes are all in 1..200 and the segment's pairs have p >= 0, else it
+// applies 2^-p and the table scale per group.  Partial sums are added in chunk
+// order; the gate/up pass applies SiLU(g) * u and writes act[pair][row], the
+// down pass writes o[pair][row].  Every order and every choice of arithmetic
+// depends on the shapes, the routing and the data only (not on which CTA takes
+// a segment).
 #include <cstdint>
 #include <functional>
 #include <mutex>
