@@ -272,3 +272,17 @@ def test_down_stage_error_floor_of_a_wide_range_act(mx):
     assert (err <= tol).all(), f"worst err/tol {np.max(err / tol):.3g}"
     # the floor is what lets it pass: somewhere the plain 1e-5 * L1 is exceeded
     assert (err > REL_FP32 * ref["l1_out"].reshape(T, hidden)).any()
+
+
+def test_layer_with_more_vectors_than_split_blocks(mx):
+    # 700 tokens (x split) and 1400 pairs (act split): more vectors than the
+    # split kernel's 4 blocks per SM, so its blocks take several vectors each
+    # (the block maximum's slot rotates per vector)
+    E, hidden, inter, T, K = 16, 256, 128, 700, 2
+    cfg, gate, up, down, x, ids, wts = make_case(E, hidden, inter, T, K, 37)
+    y, ws = run_layer(mx, cfg, gate, up, down, x, ids, wts)
+    assert mx.mxfp4_moe_plan_errors(ws) == 0
+    ref = oracle.moe_forward(gate, up, down, cfg.gu_stride, cfg.down_stride, E, hidden, inter,
+                             x, T, K, ids, wts)
+    assert_within(y, ref["out"], ref["bound_l1"] + ref["bound_prop"], REL_FP32,
+                  "MoE layer, 700 tokens")
