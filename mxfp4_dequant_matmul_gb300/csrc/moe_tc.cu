@@ -438,11 +438,13 @@ __global__ void __launch_bounds__(kThreadsE, 1)
     Seg cur = seg_of(s_cur, 0);
     int sc_pend = -1;   // (thread 0) buffer of a scale copy not yet seen complete
     uint32_t sc_pend_par = 0;
-    bool x_pend = false;   // (thread 0) a fragment copy not yet seen complete
+    bool x_pend = false;   // (thread 32) a fragment copy not yet seen complete
     uint32_t x_pend_par = 0;
     if (tid == 0 && s_cur < n_seg) {
         issue_scales(cur, 0);
         sc_pend = 0;
+    }
+    if (tid == 32 && s_cur < n_seg) {
         int pr[kTokSeg];
         for (int k = 0; k < cur.npair; ++k) pr[k] = plan.pair_of[cur.beg + k];
         issue_frags(cur, pr);
@@ -472,7 +474,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         const int* sp = spair + bi * kTokSeg;
         // the next segment's pair ids: requested now, stored after this one's
         // units (spair[bi ^ 1] may still be read by the last epilogue's stores)
-        const int nxt_pair = tid < kTokSeg && tid < nxt.npair ? plan.pair_of[nxt.beg + tid] : 0;
+        const int nxt_pair =
+            warp == 1 && lane < nxt.npair ? plan.pair_of[nxt.beg + lane] : 0;   // lanes < 4
         int la_step = 0;   // (thread 0) 1: touched index and id looked up, 2: first pair and count
         if (tid == 0) la_s = atomicAdd(plan.hdr + 4, 1);
         // column sets of this segment: NP >= its pairs
@@ -487,10 +490,8 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         const bool landed = mbar_wait(xbar, static_cast<uint32_t>(nseg_cta) & 1u, kWaitE) &&
                             mbar_wait(&sbar[bi], static_cast<uint32_t>(nseg_cta >> 1) & 1u, kWaitE);
         failed = failed || !__all_sync(0xffffffffu, landed);
-        if (tid == 0 && !failed) {
-            sc_pend = -1;
-            x_pend = false;
-        }
+        if (tid == 0 && !failed) sc_pend = -1;
+        if (tid == 32 && !failed) x_pend = false;
         const uint8_t* scm = smem + L.sc + (bi * NM + cur.m) * L.sc_bytes + lead[bi * 2 + cur.m];
         // "Plain" scale bytes (1 .. 200): 2^(k-127) is the float with bits k << 23
         // and the rows' sums may stay in the 2^p domain (|sum| below 128*32 * 6 *
@@ -509,6 +510,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
                 const uint32_t* wp = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
                 const uint32_t sh = 8u * static_cast<uint32_t>(a & 3u);
                 uint32_t flag = 0u, w0 = wp[0];
+#pragma unroll 4
                 for (int o = 0; o < ng; o += 4) {
                     const uint32_t w1 = wp[(o >> 2) + 1];
                     uint32_t w = __funnelshift_r(w0, w1, sh);
@@ -678,19 +680,22 @@ __global__ void __launch_bounds__(kThreadsE, 1)
         }
         // every warp is done with the scales and xf and past the last epilogue
         failed = __syncthreads_or(failed) != 0;
-        if (tid < kTokSeg) spair[(bi ^ 1) * kTokSeg + tid] = nxt_pair;
-        int nxt_pr[kTokSeg];   // (warp 0) the next segment's pair ids
+        if (warp == 1 && lane < kTokSeg) spair[(bi ^ 1) * kTokSeg + lane] = nxt_pair;
+        int nxt_pr[kTokSeg];   // (warp 1) the next segment's pair ids
 #pragma unroll
         for (int q = 0; q < kTokSeg; ++q) nxt_pr[q] = __shfl_sync(0xffffffffu, nxt_pair, q);
-        // the next segment's scale rows go to the other buffer, its pairs'
-        // fragment blocks to xf
-        if (tid == 0 && !failed && s_nxt < n_seg) {
-            issue_scales(nxt, bi ^ 1);
-            sc_pend = bi ^ 1;
-            sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
-            issue_frags(nxt, nxt_pr);
-            x_pend = true;
-            x_pend_par = static_cast<uint32_t>(nseg_cta + 1) & 1u;
+        // the next segment's scale rows go to the other buffer (thread 0), its
+        // pairs' fragment blocks to xf (thread 32), side by side
+        if (!failed && s_nxt < n_seg) {
+            if (tid == 0) {
+                issue_scales(nxt, bi ^ 1);
+                sc_pend = bi ^ 1;
+                sc_pend_par = static_cast<uint32_t>((nseg_cta + 1) >> 1) & 1u;
+            } else if (tid == 32) {
+                issue_frags(nxt, nxt_pr);
+                x_pend = true;
+                x_pend_par = static_cast<uint32_t>(nseg_cta + 1) & 1u;
+            }
         }
         float* part = reinterpret_cast<float*>(smem + L.sc + bi * NM * L.sc_bytes);
         // pair n: the slots' sums in lanes (g, s np + n), added in slot order into lane (g, n)
@@ -745,7 +750,7 @@ __global__ void __launch_bounds__(kThreadsE, 1)
             for (int kq = kglob; kq < issued; ++kq)
                 mbar_wait(&bars[kq % kStagesE], static_cast<uint32_t>(kq / kStagesE) & 1u, kWaitE);
         if (tid == 0 && sc_pend >= 0) mbar_wait(&sbar[sc_pend], sc_pend_par, kWaitE);
-        if (tid == 0 && x_pend) mbar_wait(xbar, x_pend_par, kWaitE);
+        if (tid == 32 && x_pend) mbar_wait(xbar, x_pend_par, kWaitE);
     }
     if (failed && lane == 0) atomicOr(&g_fault_moetc, 1);
     // the last CTA to finish zeroes the claim counters for the next pass (every
