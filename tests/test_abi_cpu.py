@@ -137,3 +137,18 @@ def test_q4k_nbytes_and_refusals(mx):
     assert L.q4k_mv(A, 8, 256, None, A, None) == 2
     assert L.q4k_mm(A, 8, 256, A, 0, A, None) == 1   # no tokens
     assert L.q4k_dequant(A, 8, 256, MIS, None) == 2
+
+
+def test_moe_workspace_holds_the_fragment_blocks(mx):
+    # the workspace grows by 16 + 128 * (cols / 32) bytes per vector: one block per
+    # token's x (hidden columns) and one per pair's act row (inter columns), beside
+    # the per-pair down outputs (4 * hidden bytes per pair); regions 256-aligned
+    E, T, K = 64, 32, 4
+    P = T * K
+    base = mx.mxfp4_moe_workspace_bytes(E, T, K, 2880, 2880)
+    more_inter = mx.mxfp4_moe_workspace_bytes(E, T, K, 2880, 5760)
+    assert abs((more_inter - base) - P * 128 * (5760 - 2880) // 32) < 256
+    more_hidden = mx.mxfp4_moe_workspace_bytes(E, T, K, 5760, 2880)
+    per_hidden = P * 4 * (5760 - 2880) + T * 128 * (5760 - 2880) // 32
+    assert abs((more_hidden - base) - per_hidden) < 512
+    assert base >= P * 4 * 2880 + T * (16 + 90 * 128) + P * (16 + 90 * 128)
